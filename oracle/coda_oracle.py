@@ -1,0 +1,134 @@
+"""Plain fp64 CPU oracle of the CODA GEMM -> residual -> RMSNorm -> GEMM chain.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline / reference legs of ``bench.py``, never by the library.
+
+What it computes is the *unfused* definition of the chain, step by step, in
+float64 with numpy (``@`` is the only library primitive used).  No blocking,
+fusion or reordering is done here; the GPU path's reparameterised form
+``y = r * ((h * gamma) @ W1)`` is deliberately NOT used, so that the oracle can
+check it.
+
+Sources (web pages on the method; cited by title and section):
+
+* [CODA-blog] "CODA：将 Transformer 块重写为 GEMM-Epilogue 程序以消除显存瓶颈"
+  (blog.hotdry.top), section "GEMM-Residual-RMSNorm-GEMM 重参数化": the chain
+  y = RMSNorm(x @ W0 + z, gamma) @ W1 with a per-row inverse-RMS factor r.
+* [CODA-blog], section "反向传播的 GEMM-Epilogue 结构": the row statistic
+  s = sum over columns of (grad_h2 * h2) = sum over columns of (grad_y * y).
+* The RMSNorm backward itself is textbook calculus: with
+  r = (mean_j h_j^2 + eps)^(-1/2) one has dr/dh_j = -r^3 h_j / d.
+
+Readings where the pages are silent (each also listed in the design notes):
+
+* the mean of h^2 is taken over the d features, and eps sits inside the
+  square root (standard RMSNorm);
+* r multiplies the row *after* the residual add and *before* gamma; gamma is
+  an elementwise weight over the d features;
+* the backward returns the RMSNorm-branch gradient only (no upstream residual
+  gradient is added) and uses the r it is given, as saved by the forward.
+
+Inputs are float64 arrays (the GPU's bf16 tensors widened exactly).  Rows are
+independent, so callers may pass any subset of rows of x, z, h, r and grad_y.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass
+class ForwardResult:
+    h: np.ndarray   # [M, d]  new residual stream x @ W0 + z
+    r: np.ndarray   # [M]     inverse RMS factor per row
+    y: np.ndarray   # [M, N1] RMSNorm(h, gamma) @ W1
+
+
+@dataclass
+class BackwardResult:
+    dh: np.ndarray   # [M, d]  gradient w.r.t. h through the RMSNorm branch
+    s: np.ndarray    # [M]     row statistic sum_j grad_h2 * h2
+    dh2: np.ndarray  # [M, d]  gradient w.r.t. the normalised activation h2
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float64)
+    return a
+
+
+def residual_gemm(x, W0, z) -> np.ndarray:
+    """h = x @ W0 + z  ([CODA-blog] reparameterisation section, inner term
+    of RMSNorm(x @ W0 + z, gamma)).  W0 is stored [in, out]."""
+    return _f64(x) @ _f64(W0) + _f64(z)
+
+
+def mean_square(h) -> np.ndarray:
+    """ms[m] = (1/d) * sum_j h[m, j]^2 -- mean over the d features."""
+    h = _f64(h)
+    return np.sum(h * h, axis=1) / h.shape[1]
+
+
+def inverse_rms(ms, eps: float) -> np.ndarray:
+    """r[m] = 1 / sqrt(ms[m] + eps), the per-row inverse RMS factor
+    ([CODA-blog] reparameterisation section)."""
+    return 1.0 / np.sqrt(_f64(ms) + float(eps))
+
+
+def rmsnorm(h, gamma, r) -> np.ndarray:
+    """h2 = RMSNorm(h, gamma) = (r[m] * h[m, j]) * gamma[j]."""
+    return (_f64(r)[:, None] * _f64(h)) * _f64(gamma)[None, :]
+
+
+def forward(x, W0, z, gamma, W1, eps: float) -> ForwardResult:
+    """Unfused forward y = RMSNorm(x @ W0 + z, gamma) @ W1.
+
+    Steps, in the order the definition gives them:
+      1. h  = x @ W0 + z
+      2. ms = mean_j h^2
+      3. r  = 1 / sqrt(ms + eps)
+      4. h2 = r * h * gamma
+      5. y  = h2 @ W1            (W1 stored [in, out])
+    """
+    h = residual_gemm(x, W0, z)
+    r = inverse_rms(mean_square(h), eps)
+    h2 = rmsnorm(h, gamma, r)
+    y = h2 @ _f64(W1)
+    return ForwardResult(h=h, r=r, y=y)
+
+
+def backward_dgrad(dy, W1, h, r, gamma) -> BackwardResult:
+    """RMSNorm-branch data gradient of the chain, given the saved h and r.
+
+    Steps:
+      1. dh2 = dy @ W1^T                       (the dgrad GEMM)
+      2. g   = gamma * dh2                     (through the elementwise weight)
+      3. dh  = r * g - (r^3 / d) * h * sum_j g_j h_j
+             (chain rule through r = (mean h^2 + eps)^(-1/2))
+    Also returns s = sum_j dh2_j * h2_j, the row statistic that [CODA-blog]
+    ("反向传播的 GEMM-Epilogue 结构") moves to the GEMM boundary; s equals
+    r * sum_j g_j h_j, so dh = r * g - (r^2 * s / d) * h.
+    """
+    dy = _f64(dy)
+    h = _f64(h)
+    r = _f64(r)
+    gamma = _f64(gamma)
+    d = h.shape[1]
+    dh2 = dy @ _f64(W1).T
+    g = gamma[None, :] * dh2
+    gh = np.sum(g * h, axis=1)
+    dh = r[:, None] * g - ((r ** 3) / d * gh)[:, None] * h
+    s = np.sum(dh2 * rmsnorm(h, gamma, r), axis=1)
+    return BackwardResult(dh=dh, s=s, dh2=dh2)
+
+
+def normwise_rel_err(got, ref) -> float:
+    """||got - ref||_F / ||ref||_F in float64 (the parity metric)."""
+    got = _f64(got)
+    ref = _f64(ref)
+    num = np.linalg.norm((got - ref).ravel())
+    den = np.linalg.norm(ref.ravel())
+    if den == 0.0:
+        return float(num)
+    return float(num / den)

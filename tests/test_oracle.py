@@ -1,0 +1,301 @@
+"""Pins for the fp64 oracle (CPU only).
+
+The oracle is checked against things other than itself:
+  * a hand-worked example with exact closed-form answers (tests/golden),
+  * brute-force scalar loops on tiny shapes,
+  * library routines: torch.nn.functional.rms_norm and torch autograd (fp64),
+  * central finite differences of the loss sum(dy * y),
+  * invariants: unit RMS before gamma when eps = 0, scale invariance of the
+    RMSNorm backward, the reparameterisation identity
+    r * ((h * gamma) @ W1) == RMSNorm(h, gamma) @ W1 and the row-statistic
+    identity sum(dy * y) == sum(dh2 * h2) (CODA blog, blog.hotdry.top,
+    sections "GEMM-Residual-RMSNorm-GEMM 重参数化" and
+    "反向传播的 GEMM-Epilogue 结构").
+The last test plants plausible mistakes in the oracle and checks that each
+one is caught by at least one of these pins.
+"""
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import coda_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_example.json")
+
+TINY_SHAPES = [(1, 1, 1), (2, 3, 4), (3, 8, 5), (5, 17, 7), (4, 33, 3), (7, 6, 33)]
+
+
+def _exact(expr: str) -> float:
+    """Evaluate 'p/q' or 'sqrt(a/b)*p/q' exactly (Fraction + one sqrt)."""
+    expr = expr.replace(" ", "")
+    if expr.startswith("sqrt("):
+        inner, rest = expr[5:].split(")", 1)
+        root = math.sqrt(Fraction(inner))
+        mult = Fraction(rest[1:]) if rest.startswith("*") else Fraction(1)
+        return root * float(mult)
+    return float(Fraction(expr))
+
+
+def _rand_case(rng, M, d, N1, eps=None):
+    x = rng.standard_normal((M, d))
+    z = rng.standard_normal((M, d))
+    W0 = rng.standard_normal((d, d)) / math.sqrt(d)
+    W1 = rng.standard_normal((d, N1)) / math.sqrt(d)
+    gamma = 1.0 + 0.3 * rng.standard_normal(d)
+    dy = 0.1 * rng.standard_normal((M, N1))
+    if eps is None:
+        eps = float(rng.choice([0.0, 1e-6, 1e-5, 0.5]))
+    return x, W0, z, gamma, W1, dy, eps
+
+
+# ----------------------------------------------------------------------------
+# pin checks (each raises AssertionError on a mismatch); reused by the
+# planted-mistake test below
+# ----------------------------------------------------------------------------
+
+def pin_golden():
+    g = json.load(open(GOLDEN))
+    f = O.forward(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], g["eps"])
+    ex = g["expected"]
+    ev = np.vectorize(_exact, otypes=[float])
+    np.testing.assert_allclose(f.h, ev(np.array(ex["h"])), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(f.r, ev(np.array(ex["r"])), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(f.y, ev(np.array(ex["y"])), rtol=1e-13, atol=1e-15)
+    b = O.backward_dgrad(g["dy"], g["W1"], f.h, f.r, g["gamma"])
+    np.testing.assert_allclose(b.dh, ev(np.array(ex["dh"])), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(b.s, ev(np.array(ex["s"])), rtol=1e-13, atol=0)
+
+
+def _brute_forward(x, W0, z, gamma, W1, eps):
+    M, d = len(x), len(W0)
+    N1 = len(W1[0])
+    h = [[0.0] * d for _ in range(M)]
+    for m in range(M):
+        for j in range(d):
+            acc = 0.0
+            for k in range(d):
+                acc += x[m][k] * W0[k][j]
+            h[m][j] = acc + z[m][j]
+    r = []
+    for m in range(M):
+        ss = 0.0
+        for j in range(d):
+            ss += h[m][j] * h[m][j]
+        r.append(1.0 / math.sqrt(ss / d + eps))
+    y = [[0.0] * N1 for _ in range(M)]
+    for m in range(M):
+        for n in range(N1):
+            acc = 0.0
+            for j in range(d):
+                acc += (h[m][j] * r[m] * gamma[j]) * W1[j][n]
+            y[m][n] = acc
+    return np.array(h), np.array(r), np.array(y)
+
+
+def _brute_backward(dy, W1, h, r, gamma):
+    M, d = len(h), len(h[0])
+    N1 = len(W1[0])
+    dh = np.zeros((M, d))
+    for m in range(M):
+        dh2 = [0.0] * d
+        for j in range(d):
+            acc = 0.0
+            for n in range(N1):
+                acc += dy[m][n] * W1[j][n]
+            dh2[j] = acc
+        # d/dh_i of sum_j dh2_j * gamma_j * h_j * r(h), r = (sum h^2/d + eps)^-1/2
+        dot = 0.0
+        for j in range(d):
+            dot += dh2[j] * gamma[j] * h[m][j]
+        for i in range(d):
+            drdhi = -(r[m] ** 3) * h[m][i] / d
+            dh[m][i] = dh2[i] * gamma[i] * r[m] + dot * drdhi
+    return dh
+
+
+def pin_bruteforce(seed=0):
+    rng = np.random.default_rng(seed)
+    for (M, d, N1) in TINY_SHAPES:
+        x, W0, z, gamma, W1, dy, eps = _rand_case(rng, M, d, N1)
+        f = O.forward(x, W0, z, gamma, W1, eps)
+        h, r, y = _brute_forward(x.tolist(), W0.tolist(), z.tolist(), gamma.tolist(), W1.tolist(), eps)
+        np.testing.assert_allclose(f.h, h, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(f.r, r, rtol=1e-12, atol=0)
+        np.testing.assert_allclose(f.y, y, rtol=1e-11, atol=1e-12)
+        b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+        dh = _brute_backward(dy.tolist(), W1.tolist(), f.h.tolist(), f.r.tolist(), gamma.tolist())
+        np.testing.assert_allclose(b.dh, dh, rtol=1e-10, atol=1e-12)
+
+
+def pin_torch_library(seed=1):
+    """torch.nn.functional.rms_norm and autograd in fp64 on the CPU."""
+    rng = np.random.default_rng(seed)
+    for (M, d, N1) in [(6, 16, 9), (3, 40, 24), (8, 5, 5)]:
+        x, W0, z, gamma, W1, dy, eps = _rand_case(rng, M, d, N1, eps=1e-5)
+        f = O.forward(x, W0, z, gamma, W1, eps)
+        th = torch.tensor(x) @ torch.tensor(W0) + torch.tensor(z)
+        th.requires_grad_(True)
+        ty = torch.nn.functional.rms_norm(th, (d,), weight=torch.tensor(gamma), eps=eps) @ torch.tensor(W1)
+        np.testing.assert_allclose(f.h, th.detach().numpy(), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(f.y, ty.detach().numpy(), rtol=1e-10, atol=1e-12)
+        ty.backward(torch.tensor(dy))
+        b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+        np.testing.assert_allclose(b.dh, th.grad.numpy(), rtol=1e-9, atol=1e-12)
+
+
+def pin_finite_differences(seed=2):
+    """Central differences of L(h) = sum(dy * y(h)), r recomputed from h."""
+    rng = np.random.default_rng(seed)
+    M, d, N1 = 3, 6, 5
+    x, W0, z, gamma, W1, dy, eps = _rand_case(rng, M, d, N1, eps=1e-3)
+    f = O.forward(x, W0, z, gamma, W1, eps)
+    b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+
+    def loss(h):
+        r = 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
+        return float(np.sum(dy * ((r[:, None] * h * gamma) @ W1)))
+
+    step = 1e-6
+    fd = np.zeros_like(f.h)
+    for m in range(M):
+        for j in range(d):
+            hp = f.h.copy()
+            hm = f.h.copy()
+            hp[m, j] += step
+            hm[m, j] -= step
+            fd[m, j] = (loss(hp) - loss(hm)) / (2 * step)
+    np.testing.assert_allclose(b.dh, fd, rtol=1e-5, atol=1e-8)
+
+
+def pin_invariants(seed=3):
+    rng = np.random.default_rng(seed)
+    for (M, d, N1) in [(5, 12, 7), (4, 64, 16)]:
+        # eps = 0: RMSNorm before gamma has unit RMS, and the backward is
+        # orthogonal to h (RMSNorm is scale invariant).
+        x, W0, z, gamma, W1, dy, _ = _rand_case(rng, M, d, N1)
+        f = O.forward(x, W0, z, gamma, W1, 0.0)
+        u = f.r[:, None] * f.h
+        np.testing.assert_allclose(np.sqrt(np.mean(u * u, axis=1)), 1.0, rtol=1e-13)
+        b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+        scale = np.linalg.norm(f.h, axis=1) * np.linalg.norm(b.dh, axis=1)
+        assert np.all(np.abs(np.sum(f.h * b.dh, axis=1)) <= 1e-12 * scale + 1e-300)
+        # eps > 0: sum_j h_j dh_j = r * sum(g*h) * eps / (ms + eps)
+        eps = 0.25
+        f = O.forward(x, W0, z, gamma, W1, eps)
+        b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+        ms = np.mean(f.h * f.h, axis=1)
+        gh = np.sum(gamma * b.dh2 * f.h, axis=1)
+        np.testing.assert_allclose(np.sum(f.h * b.dh, axis=1), f.r * gh * eps / (ms + eps),
+                                   rtol=1e-10, atol=1e-13)
+        # rms(r*h) = sqrt(ms / (ms + eps))
+        u = f.r[:, None] * f.h
+        np.testing.assert_allclose(np.sqrt(np.mean(u * u, axis=1)), np.sqrt(ms / (ms + eps)), rtol=1e-13)
+
+
+def pin_reparameterisation(seed=4):
+    """r * ((h * gamma) @ W1) == RMSNorm(h, gamma) @ W1, and
+    sum(dy * y) == sum(dh2 * h2) == s (the two identities of the method)."""
+    rng = np.random.default_rng(seed)
+    for (M, d, N1) in [(6, 10, 12), (3, 32, 64)]:
+        x, W0, z, gamma, W1, dy, eps = _rand_case(rng, M, d, N1, eps=1e-5)
+        f = O.forward(x, W0, z, gamma, W1, eps)
+        fused = f.r[:, None] * ((f.h * gamma[None, :]) @ W1)
+        np.testing.assert_allclose(fused, f.y, rtol=1e-11, atol=1e-13)
+        b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+        np.testing.assert_allclose(np.sum(dy * f.y, axis=1), b.s, rtol=1e-10, atol=1e-13)
+
+
+def pin_special_case_plain_rmsnorm(seed=5):
+    """W0 = I, z = 0, gamma = 1, W1 = I reduces the chain to a plain RMSNorm
+    of x (checked against torch's rms_norm)."""
+    rng = np.random.default_rng(seed)
+    M, d = 4, 24
+    x = rng.standard_normal((M, d))
+    eye = np.eye(d)
+    for eps in (0.0, 1e-5):
+        f = O.forward(x, eye, np.zeros((M, d)), np.ones(d), eye, eps)
+        ref = torch.nn.functional.rms_norm(torch.tensor(x), (d,), eps=eps).numpy()
+        np.testing.assert_allclose(f.y, ref, rtol=1e-12, atol=1e-14)
+
+
+ALL_PINS = [pin_golden, pin_bruteforce, pin_torch_library, pin_finite_differences,
+            pin_invariants, pin_reparameterisation, pin_special_case_plain_rmsnorm]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin()
+
+
+def test_normwise_rel_err():
+    a = np.array([[3.0, 4.0]])
+    assert O.normwise_rel_err(a, a) == 0.0
+    assert abs(O.normwise_rel_err(a + np.array([[0.0, 0.5]]), a) - 0.1) < 1e-15
+
+
+def test_oracle_rows_are_independent():
+    """Row subsets give exactly the rows of the full result (parity at full
+    size relies on this)."""
+    rng = np.random.default_rng(7)
+    x, W0, z, gamma, W1, dy, eps = _rand_case(rng, 9, 16, 8, eps=1e-5)
+    full = O.forward(x, W0, z, gamma, W1, eps)
+    rows = np.array([0, 4, 8])
+    sub = O.forward(x[rows], W0, z[rows], gamma, W1, eps)
+    np.testing.assert_array_equal(sub.y, full.y[rows])
+    np.testing.assert_array_equal(sub.r, full.r[rows])
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes: each must make at least one pin fail
+# ----------------------------------------------------------------------------
+
+def _bwd_mutant(kind):
+    def bwd(dy, W1, h, r, gamma):
+        dy, h, r, gamma = (np.asarray(a, dtype=np.float64) for a in (dy, h, r, gamma))
+        d = h.shape[1]
+        dh2 = dy @ np.asarray(W1, dtype=np.float64).T
+        g = dh2 if kind == "no_gamma" else gamma[None, :] * dh2
+        gh = np.sum(g * h, axis=1)
+        p = 2 if kind == "r_squared" else 3
+        coef = ((r ** p) / d * gh)[:, None] * h
+        dh = r[:, None] * g + coef if kind == "sign" else r[:, None] * g - coef
+        if kind == "dropped_term":
+            dh = r[:, None] * g
+        s = np.sum(dh2 * O.rmsnorm(h, gamma, r), axis=1)
+        return O.BackwardResult(dh=dh, s=s, dh2=dh2)
+    return bwd
+
+
+MUTANTS = {
+    "dropped_residual": ("residual_gemm", lambda x, W0, z: np.asarray(x, float) @ np.asarray(W0, float)),
+    "transposed_W0": ("residual_gemm",
+                      lambda x, W0, z: np.asarray(x, float) @ np.asarray(W0, float).T + np.asarray(z, float)),
+    "mean_over_d_minus_1": ("mean_square",
+                            lambda h: np.sum(np.asarray(h, float) ** 2, axis=1) / max(np.shape(h)[1] - 1, 1)),
+    "eps_outside_sqrt": ("inverse_rms", lambda ms, eps: 1.0 / np.sqrt(np.asarray(ms, float)) + eps),
+    "dropped_gamma": ("rmsnorm", lambda h, gamma, r: np.asarray(r, float)[:, None] * np.asarray(h, float)),
+    "bwd_sign": ("backward_dgrad", _bwd_mutant("sign")),
+    "bwd_r_squared": ("backward_dgrad", _bwd_mutant("r_squared")),
+    "bwd_no_gamma": ("backward_dgrad", _bwd_mutant("no_gamma")),
+    "bwd_dropped_term": ("backward_dgrad", _bwd_mutant("dropped_term")),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name} was not caught by any pin"

@@ -1,0 +1,47 @@
+"""Host-side checks of the seeded input generator (CPU only)."""
+
+import numpy as np
+import torch
+
+from gemm_epilogue_fusion_gemm0_gb300 import synth
+
+
+def test_shapes_dtypes_and_determinism():
+    a = synth.make_forward_inputs(64, 32, 48, seed=0)
+    b = synth.make_forward_inputs(64, 32, 48, seed=0)
+    for k, shape in (("x", (64, 32)), ("z", (64, 32)), ("W0", (32, 32)), ("W1", (32, 48)), ("gamma", (32,))):
+        assert a[k].dtype == torch.bfloat16 and tuple(a[k].shape) == shape
+        assert torch.equal(a[k], b[k])
+    dy1 = synth.make_grad_output(a["_rng"], 64, 48)
+    dy2 = synth.make_grad_output(b["_rng"], 64, 48)
+    assert torch.equal(dy1, dy2) and dy1.dtype == torch.bfloat16
+    c = synth.make_forward_inputs(64, 32, 48, seed=1)
+    assert not torch.equal(a["x"], c["x"])
+
+
+def test_distributions():
+    M, d, N1 = 512, 256, 512
+    t = synth.make_forward_inputs(M, d, N1, seed=3)
+    f = lambda k: t[k].to(torch.float64).numpy()
+    assert abs(f("x").std() - 1.0) < 0.02 and abs(f("x").mean()) < 0.02
+    assert abs(f("W0").std() - (1 / d) ** 0.5) < 0.003
+    assert abs(f("W1").std() - (1 / d) ** 0.5) < 0.003
+    assert abs(f("gamma").mean() - 1.0) < 0.08 and abs(f("gamma").std() - 0.1 ** 0.5) < 0.05
+    dy = synth.make_grad_output(t["_rng"], M, N1).to(torch.float64).numpy()
+    assert abs(dy.std() - 0.1) < 0.003
+
+
+def test_bf16_rounding_is_nearest_even():
+    # 1 + 2^-8 is halfway between bf16 neighbours 1 and 1 + 2^-7: ties to even -> 1
+    v = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8], dtype=np.float32)
+    out = synth.to_bf16(v).to(torch.float64).numpy()
+    assert out[0] == 1.0 and out[1] == 1.0 + 2 * 2.0 ** -7
+
+
+def test_sample_rows():
+    rows = synth.sample_rows(8192, 512, seed=1)
+    assert len(rows) == 512 and len(np.unique(rows)) == 512
+    for r in (0, 127, 128, 8191):
+        assert r in rows
+    assert np.all(np.diff(rows) > 0)
+    assert np.array_equal(synth.sample_rows(100, 512), np.arange(100))
