@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark: the fused GEMM -> residual -> RMSNorm -> GEMM chain on GB300.
+
+One step = one pass of the whole hot path over one batch: coda_fwd (GEMM0 with
+the residual/gamma/sum-of-squares epilogue, the row reduction, GEMM1 with the
+row-scale epilogue) followed by coda_bwd_dgrad (the data-gradient GEMM with
+the fused RMSNorm backward), on the Llama-7B-shaped workload
+M=8192, d=4096, N1=28672, eps=1e-5 (seeded synthetic bf16 inputs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl coda|reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job TFLOP/s of the two GEMMs
+of the forward plus the data-gradient GEMM, with inputs resident in HBM;
+`e2e` is the same metric through the same C-ABI calls with pinned host
+buffers, host<->device copies inside the timed region.  `--impl reference`
+times the fp64 CPU oracle on a bounded sample of the same workload.
+With N > 1 (torchrun) every rank runs its own batch (weak scaling; the path
+has no cross-row exchange, so there is no collective on the data path).
+"""
+
+import os
+import sys
+
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import argparse  # noqa: E402
+import datetime  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gemm_epilogue_fusion_gemm0_gb300 import synth  # noqa: E402
+
+METRIC = "fused GEMM-Res-RMSNorm-GEMM TFLOP/s (fwd, bwd-dgrad); % of GB300 BF16 peak"
+WORKLOAD = synth.WORKLOADS["llama7b"]
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["csrc/coda.cu", "csrc/gemm.cuh", "csrc/epilogues.cuh", "csrc/ptx.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = {}
+            for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs"):
+                if k in d and isinstance(d[k], (int, float)):
+                    out[k] = float(d[k])
+            if "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gemm_epilogue_fusion_gemm0_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken from the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    ent = d.get("kernels", {}).get(kernel)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.path = None
+        sel = str(device_index)
+        try:
+            pr = torch.cuda.get_device_properties(device_index)
+            if hasattr(pr, "pci_bus_id"):
+                sel = f"{getattr(pr, 'pci_domain_id', 0):08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        except Exception:
+            pass
+        self.sel = sel
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.sel],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        used = inside if inside else sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:2]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {
+            "sm_mhz": statistics.median([r[1] for r in used]) if used else None,
+            "sm_max_mhz": max(r[2] for r in used) if used else None,
+            "reasons": reasons,
+            "samples": len(inside),
+        }
+
+
+def oracle_rows(x, z, dy, W0_64, W1_64, g64, eps, rows):
+    """One oracle pass (fwd + bwd-dgrad) over the given row slice."""
+    import oracle
+
+    f = oracle.forward(x[rows], W0_64, z[rows], g64, W1_64, eps)
+    oracle.backward_dgrad(dy[rows], W1_64, f.h, f.r, g64)
+
+
+def oracle_setup(t, dy):
+    f64 = lambda a: a.to(torch.float64).numpy()
+    return (f64(t["x"]), f64(t["z"]), f64(dy), f64(t["W0"]), f64(t["W1"]), f64(t["gamma"]))
+
+
+def flops_per_row(w):
+    return (w.fwd_flops + w.bwd_flops) / w.M
+
+
+def cpu_baseline(t, dy, w, budget_s=12.0, chunk=128):
+    """The oracle as it stands, on a time-boxed sample of rows of the workload."""
+    x, z, dy64, W0, W1, g = oracle_setup(t, dy)
+    done, spent = 0, 0.0
+    while spent < budget_s and done < w.M:
+        rows = slice(done, min(done + chunk, w.M))
+        t0 = time.perf_counter()
+        oracle_rows(x, z, dy64, W0, W1, g, w.eps, rows)
+        spent += time.perf_counter() - t0
+        done = rows.stop
+    value = done * flops_per_row(w) / spent / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"first {done} of {w.M} rows of {w.name} (fwd + bwd-dgrad), fp64 numpy, "
+                      f"{spent:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOAD
+    t = synth.make_forward_inputs(w.M, w.d, w.N1, seed=0)
+    dy = synth.make_grad_output(t["_rng"], w.M, w.N1)
+    x, z, dy64, W0, W1, g = oracle_setup(t, dy)
+    # calibrate rows per step so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle_rows(x, z, dy64, W0, W1, g, w.eps, slice(0, 32))
+    per_row = (time.perf_counter() - t0) / 32
+    R = int(max(8, min(512, 120.0 / max(1, args.steps + args.warmup) / per_row)))
+    for i in range(args.warmup):
+        oracle_rows(x, z, dy64, W0, W1, g, w.eps, slice(0, R))
+    times = []
+    for i in range(args.steps):
+        s = (i * R) % max(1, w.M - R)
+        t0 = time.perf_counter()
+        oracle_rows(x, z, dy64, W0, W1, g, w.eps, slice(s, s + R))
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = args.steps * R * flops_per_row(w) / tot / 1e12
+    sample = f"{R} of {w.M} rows per step of {w.name} (fwd + bwd-dgrad), fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} fwd + bwd-dgrad (M={w.M}, d={w.d}, N1={w.N1}, eps={w.eps})",
+                   "rows_per_step": R},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_coda(args):
+    import __graft_entry__ as ge
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    ge.build()
+    from gemm_epilogue_fusion_gemm0_gb300 import binding as B
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = WORKLOAD
+    M, d, N1, eps = w.M, w.d, w.N1, w.eps
+    t = synth.make_forward_inputs(M, d, N1, seed=rank)
+    dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    dy = dy_cpu.to(dev)
+    h = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    r = torch.empty((M,), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+    dh = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    ws_f = B.workspace(B.coda_fwd_workspace_bytes(M, d, N1), dev)
+    ws_b = B.workspace(B.coda_bwd_dgrad_workspace_bytes(M, d, N1), dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            B.coda_set_launch_events(ev[1:4])
+        B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                   stream=stream)
+        if ev is not None:
+            B.coda_set_launch_events(ev[4:5])
+        B.coda_bwd_dgrad(dy, g["W1"], h, r, g["gamma"], dh=dh, ws=ws_b, stream=stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    st, detail = B.coda_get_device_status()
+    if st != B.CODA_OK:
+        raise RuntimeError(f"device status after warm-up: {B.status_string(st)} {detail:#x}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for ev in evs:  # create the CUDA events outside the timed region
+        for e in ev:
+            e.record(stream)
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    wall0 = time.time()
+    begin.record(stream)
+    for i in range(K):
+        evs[i][0].record(stream)
+        step(evs[i])
+    end.record(stream)
+    barrier()
+    wall1 = time.time()
+    B.coda_set_launch_events(None)
+    time.sleep(0.15)
+    clocks = sampler.stop(wall0, wall1)
+    st, detail = B.coda_get_device_status()
+    if st != B.CODA_OK:
+        raise RuntimeError(f"device status after timed region: {B.status_string(st)} {detail:#x}")
+
+    ms = begin.elapsed_time(end)
+    names = ["gemm0_residual_gamma_sumsq", "rowreduce_rsqrt", "gemm1_rowscale", "dgrad_rmsnorm_bwd"]
+    per = {n: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+           for j, n in enumerate(names)}
+    fwd_ms = statistics.fmean(evs[i][0].elapsed_time(evs[i][3]) for i in range(K))
+    bwd_ms = per["dgrad_rmsnorm_bwd"]
+
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    flops_step = w.fwd_flops + w.bwd_flops
+    value = world * K * flops_step / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the same C-ABI calls with pinned host buffers
+    host_in = {k: v.pin_memory() for k, v in t.items() if k != "_rng"}
+    host_dy = dy_cpu.pin_memory()
+    host_out = {"h": torch.empty_like(h, device="cpu").pin_memory(),
+                "r": torch.empty_like(r, device="cpu").pin_memory(),
+                "y": torch.empty_like(y, device="cpu").pin_memory(),
+                "dh": torch.empty_like(dh, device="cpu").pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_dy.numel() * 2
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k, v in host_in.items():
+            g[k].copy_(v, non_blocking=True)
+        dy.copy_(host_dy, non_blocking=True)
+        step()
+        host_out["h"].copy_(h, non_blocking=True)
+        host_out["r"].copy_(r, non_blocking=True)
+        host_out["y"].copy_(y, non_blocking=True)
+        host_out["dh"].copy_(dh, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    KE = max(3, min(K, 10))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    ems = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ems], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ems = float(tt.item())
+    e2e_value = world * KE * flops_step / (ems * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    kflops = {"gemm0_residual_gamma_sumsq": 2 * M * d * d, "rowreduce_rsqrt": 0,
+              "gemm1_rowscale": 2 * M * d * N1, "dgrad_rmsnorm_bwd": 2 * M * N1 * d}
+    kernels = {}
+    for n in names:
+        ent = {"ms": per[n]}
+        if kflops[n]:
+            ent["tflops"] = kflops[n] / (per[n] * 1e-3) / 1e12
+            ent["frac"] = ent["tflops"] / peak
+        kernels[n] = ent
+    dom = max((n for n in names if kflops[n]), key=lambda n: per[n])
+    ach = kernels[dom]["tflops"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": profiled_traffic(dom),
+                "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside a long step)",
+                "frac_of_burst_peak": ach / peaks["bf16_tflops"]}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(t, dy_cpu, w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"{w.name} fwd + bwd-dgrad (M={M}, d={d}, N1={N1}, eps={eps})",
+            "M": M, "d": d, "N1": N1, "eps": eps, "step": "coda_fwd + coda_bwd_dgrad",
+            "parallelism": f"replicas x{world} (rows sharded, no collective)",
+            "l2": "no flush: inputs larger than L2 (W1 235 MB, dy 470 MB; ~1.6 GB touched per step)",
+        },
+        "fwd_tflops": w.fwd_flops / (fwd_ms * 1e-3) / 1e12,
+        "bwd_tflops": w.bwd_flops / (bwd_ms * 1e-3) / 1e12,
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "kernels": kernels,
+        "roofline": roofline,
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": KE},
+        "gpu_launches": 4 * K,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, _, _ = dist_env()
+    if args.gpus != world and world == 1 and args.gpus > 1:
+        log("bench.py --gpus N>1 must be launched with torchrun (one process per GPU)")
+        return 2
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_coda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

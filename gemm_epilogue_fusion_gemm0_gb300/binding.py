@@ -1,0 +1,205 @@
+"""ctypes binding of libcoda.so (include/coda.h), same names as the C ABI.
+
+Argument marshalling only: torch tensors are checked for device, dtype and
+contiguity and passed as raw device pointers together with the current CUDA
+stream.  Every step of the computation runs in the library's kernels; if the
+library is missing this module raises at import time.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libcoda.so not found at {LIB_PATH}: build it first "
+        "(python -c 'import __graft_entry__ as g; g.build()')"
+    )
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+CODA_OK = 0
+STATUS_NAMES = {
+    0: "CODA_OK",
+    1: "CODA_ERR_INVALID_ARG",
+    2: "CODA_ERR_UNSUPPORTED_SHAPE",
+    3: "CODA_ERR_MISALIGNED",
+    4: "CODA_ERR_WORKSPACE_TOO_SMALL",
+    5: "CODA_ERR_LAUNCH",
+    6: "CODA_ERR_DEVICE_TIMEOUT",
+    7: "CODA_ERR_NO_DEVICE",
+    8: "CODA_ERR_UNSUPPORTED_DEVICE",
+}
+
+_vp, _i64, _sz, _f32, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_uint64
+_st = ctypes.c_int
+
+EXPORTS = {
+    # name: (restype, argtypes)
+    "coda_fwd_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "coda_bwd_dgrad_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "coda_fwd_unfused_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "coda_fwd": (_st, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "coda_fwd_unfused": (_st, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "coda_bwd_dgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _sz, _vp]),
+    "coda_get_device_status": (_st, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "coda_set_wait_timeout_ns": (None, [_u64]),
+    "coda_status_string": (ctypes.c_char_p, [_st]),
+    "coda_watchdog_selftest": (_st, [_u64, _vp]),
+    "coda_set_launch_events": (None, [_vp, ctypes.c_int]),
+}
+
+for _name, (_res, _args) in EXPORTS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class CodaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def status_string(status: int) -> str:
+    return _lib.coda_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != CODA_OK:
+        raise CodaError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+# --------------------------------------------------------------------------- sizes
+def coda_fwd_workspace_bytes(M: int, d: int, N1: int) -> int:
+    return int(_lib.coda_fwd_workspace_bytes(M, d, N1))
+
+
+def coda_fwd_unfused_workspace_bytes(M: int, d: int, N1: int) -> int:
+    return int(_lib.coda_fwd_unfused_workspace_bytes(M, d, N1))
+
+
+def coda_bwd_dgrad_workspace_bytes(M: int, d: int, N1: int) -> int:
+    return int(_lib.coda_bwd_dgrad_workspace_bytes(M, d, N1))
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A device byte buffer of at least `nbytes` (torch allocates it)."""
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+# --------------------------------------------------------------------------- calls
+def _fwd_common(fn, wsfn, x, W0, z, gamma, W1, eps, h, r, y, ws, stream):
+    M, d = x.shape
+    N1 = W1.shape[1]
+    dev = x.device
+    if h is None:
+        h = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    if r is None:
+        r = torch.empty((M,), dtype=torch.float32, device=dev)
+    if y is None:
+        y = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = workspace(wsfn(M, d, N1), dev)
+    bf = torch.bfloat16
+    args = (
+        _dev(x, bf, (M, d), "x"), _dev(W0, bf, (d, d), "W0"), _dev(z, bf, (M, d), "z"),
+        _dev(gamma, bf, (d,), "gamma"), _dev(W1, bf, (d, N1), "W1"), float(eps), M, d, N1,
+        _dev(h, bf, (M, d), "h"), _dev(r, torch.float32, (M,), "r"), _dev(y, bf, (M, N1), "y"),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream),
+    )
+    _check(fn(*args), fn.__name__)
+    return h, r, y
+
+
+def coda_fwd(x, W0, z, gamma, W1, eps, h=None, r=None, y=None, ws=None, stream=None):
+    """Fused forward; returns (h, r, y).  Outputs are allocated if not given."""
+    return _fwd_common(_lib.coda_fwd, coda_fwd_workspace_bytes, x, W0, z, gamma, W1, eps,
+                       h, r, y, ws, stream)
+
+
+def coda_fwd_unfused(x, W0, z, gamma, W1, eps, h=None, r=None, y=None, ws=None, stream=None):
+    """Unfused reference sequence (measurement only); returns (h, r, y)."""
+    return _fwd_common(_lib.coda_fwd_unfused, coda_fwd_unfused_workspace_bytes, x, W0, z, gamma,
+                       W1, eps, h, r, y, ws, stream)
+
+
+def coda_bwd_dgrad(dy, W1, h, r, gamma, dh=None, ws=None, stream=None):
+    """Fused RMSNorm-branch data gradient; returns dh."""
+    M, N1 = dy.shape
+    d = W1.shape[0]
+    if dh is None:
+        dh = torch.empty((M, d), dtype=torch.bfloat16, device=dy.device)
+    if ws is None:
+        ws = workspace(coda_bwd_dgrad_workspace_bytes(M, d, N1), dy.device)
+    bf = torch.bfloat16
+    st = _lib.coda_bwd_dgrad(
+        _dev(dy, bf, (M, N1), "dy"), _dev(W1, bf, (d, N1), "W1"), _dev(h, bf, (M, d), "h"),
+        _dev(r, torch.float32, (M,), "r"), _dev(gamma, bf, (d,), "gamma"), M, d, N1,
+        _dev(dh, bf, (M, d), "dh"), ws.data_ptr(), ws.numel() * ws.element_size(),
+        _stream_ptr(stream),
+    )
+    _check(st, "coda_bwd_dgrad")
+    return dh
+
+
+def coda_get_device_status(stream=None) -> tuple[int, int]:
+    """(status, detail) after synchronising the stream; clears the status."""
+    detail = ctypes.c_uint32(0)
+    st = _lib.coda_get_device_status(_stream_ptr(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def coda_set_wait_timeout_ns(ns: int) -> None:
+    _lib.coda_set_wait_timeout_ns(int(ns))
+
+
+def coda_watchdog_selftest(timeout_ns: int, stream=None) -> int:
+    return int(_lib.coda_watchdog_selftest(int(timeout_ns), _stream_ptr(stream)))
+
+
+_events_keepalive = None
+
+
+def coda_set_launch_events(events) -> None:
+    """Measurement hook: record events[k] after the k-th kernel launch of each
+    following coda_* call (events: list of torch.cuda.Event, or None)."""
+    global _events_keepalive
+    if not events:
+        _lib.coda_set_launch_events(None, 0)
+        _events_keepalive = None
+        return
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event lazily, on first record
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
+    _events_keepalive = (arr, events)
+    _lib.coda_set_launch_events(ctypes.cast(arr, ctypes.c_void_p), len(events))
+
+
+def raw() -> ctypes.CDLL:
+    """The loaded library (for direct C-ABI calls, e.g. with bad arguments)."""
+    return _lib

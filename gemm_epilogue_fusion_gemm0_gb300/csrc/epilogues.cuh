@@ -1,0 +1,236 @@
+// epilogues.cuh -- the epilogue programs of the chain, one policy class each.
+//
+// Each thread owns one row of the 128 x 256 fp32 accumulator tile (its TMEM
+// lane) and walks it in 32-column chunks (tcgen05.ld 32x32b.x32), so every
+// row reduction below is a plain per-thread sum: no shuffles, no atomics, and
+// a fixed summation order (bit-reproducible results).
+//
+// The primitives used are the method's tile-local ones (CODA blog,
+// blog.hotdry.top, section "五类 Epilogue 原语"): an elementwise map (residual
+// add), a rank-1 vector broadcast (gamma, the per-row r), rank-2 tile loads and
+// stores (z, h), and a partial tile reduction finished by a small pass
+// (per-tile sums of squares / of grad_h2 * gamma * h).
+#pragma once
+
+#include "gemm.cuh"
+
+namespace coda {
+
+struct Chunk8 {
+  uint32_t w[4];
+};
+
+__device__ __forceinline__ Chunk8 ldg8(const __nv_bfloat16* p) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+  return Chunk8{{v.x, v.y, v.z, v.w}};
+}
+
+__device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------------------
+// GEMM0 epilogue (step 1 of the reparameterisation, CODA blog section
+// "GEMM-Residual-RMSNorm-GEMM 重参数化"): residual add, gamma scaling and the
+// tile-local partial sum of squares.
+//   h  = acc + z                (fp32)          -> h_out  bf16
+//   hg = h * gamma              (fp32)          -> hg_out bf16 (GEMM1's A operand)
+//   part[nb][m] = sum over the tile's columns of h^2 (fp32, before rounding)
+// With hg_out == nullptr and part == nullptr it is the plain residual-add
+// epilogue of the unfused reference sequence.
+// ---------------------------------------------------------------------------
+struct EpiResidualGammaSumsq {
+  struct Params {
+    const __nv_bfloat16* z;
+    const __nv_bfloat16* gamma;
+    __nv_bfloat16* h_out;
+    __nv_bfloat16* hg_out;  // may be null (unfused sequence)
+    float* part;            // [nt][M], may be null (unfused sequence)
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const bool fused = p.hg_out != nullptr;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            const Chunk8 zz = ldg8(p.z + rowoff + n);
+            const Chunk8 gg = ldg8(p.gamma + n);
+            uint32_t hw[4], hgw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zz.w[e]);
+              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zz.w[e]);
+              ss = fmaf(h0, h0, ss);
+              ss = fmaf(h1, h1, ss);
+              hw[e] = pack_bf16x2(h0, h1);
+              hgw[e] = pack_bf16x2(h0 * bf16lo(gg.w[e]), h1 * bf16hi(gg.w[e]));
+            }
+            stg8(p.h_out + rowoff + n, hw);
+            if (fused) stg8(p.hg_out + rowoff + n, hgw);
+          }
+        }
+      }
+    }
+    if (row_ok && p.part != nullptr) p.part[static_cast<size_t>(c.nb) * c.M + m] = ss;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// GEMM1 epilogue (step 3): y = r[m] * acc, the row scale applied after the
+// second GEMM.  With r == nullptr it is the plain store of the unfused
+// reference sequence.
+// ---------------------------------------------------------------------------
+struct EpiRowScale {
+  struct Params {
+    const float* r;  // [M], may be null (scale 1)
+    __nv_bfloat16* y_out;
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const float rr = (row_ok && p.r != nullptr) ? __ldg(p.r + m) : 1.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            uint32_t yw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              yw[e] = pack_bf16x2(rr * __uint_as_float(v[g * 8 + 2 * e]),
+                                  rr * __uint_as_float(v[g * 8 + 2 * e + 1]));
+            stg8(p.y_out + rowoff + n, yw);
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Data-gradient epilogue (CODA blog, section "反向传播的 GEMM-Epilogue 结构"):
+// acc = grad_h2 = grad_y @ W1^T for this tile.
+//   pass 1: qpart[nb][m] = sum over the tile's columns of acc * gamma * h;
+//           publish it with a release flag carrying this call's token;
+//   then:   wait until every column tile of this row block has published,
+//           q[m] = sum_nb qpart[nb][m] (fixed order), coef = r^3 q / d;
+//   pass 2: grad_h = r * gamma * acc - coef * h   -> dh_out bf16.
+// q * r = sum_j grad_h2 * h2 is the statistic s of the method.  The flag wait
+// needs every block of the launch resident (cooperative launch) and tiles in
+// row-major order with at most gridDim.x column tiles per row; then every wait
+// depends only on tiles with smaller index and cannot deadlock.
+// ---------------------------------------------------------------------------
+struct EpiRmsNormBackward {
+  struct Params {
+    const __nv_bfloat16* h;
+    const __nv_bfloat16* gamma;
+    const float* r;
+    __nv_bfloat16* dh_out;
+    float* qpart;     // [nt][M]
+    uint64_t* flags;  // [mt][nt]
+    uint64_t token;
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
+                                               const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+
+    float qp = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            const Chunk8 hh = ldg8(p.h + rowoff + n);
+            const Chunk8 gg = ldg8(p.gamma + n);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              qp = fmaf(__uint_as_float(v[g * 8 + 2 * e]) * bf16lo(gg.w[e]), bf16lo(hh.w[e]), qp);
+              qp = fmaf(__uint_as_float(v[g * 8 + 2 * e + 1]) * bf16hi(gg.w[e]), bf16hi(hh.w[e]),
+                        qp);
+            }
+          }
+        }
+      }
+    }
+    if (row_ok) p.qpart[static_cast<size_t>(c.nb) * c.M + m] = qp;
+
+    // Publish this tile's partials, then wait for the whole row block.
+    named_bar_sync(1, kEpiThreads);
+    uint64_t* row_flags = p.flags + static_cast<size_t>(c.mb) * c.nt;
+    if (threadIdx.x == kEpiFirstThread) {
+      __threadfence();
+      st_release_gpu_u64(row_flags + c.nb, p.token);
+      for (int j = 0; j < c.nt; ++j)
+        if (!flag_wait(row_flags + j, p.token, wc, kSiteRowFlags)) break;
+      __threadfence();
+    }
+    named_bar_sync(1, kEpiThreads);
+
+    float q = 0.f;
+    float rr = 0.f;
+    if (row_ok) {
+      for (int j = 0; j < c.nt; ++j) q += __ldcg(p.qpart + static_cast<size_t>(j) * c.M + m);
+      rr = __ldg(p.r + m);
+    }
+    const float coef = rr * rr * rr * q / static_cast<float>(c.N);
+
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            const Chunk8 hh = ldg8(p.h + rowoff + n);
+            const Chunk8 gg = ldg8(p.gamma + n);
+            uint32_t dw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
+                               coef * bf16lo(hh.w[e]);
+              const float d1 = rr * bf16hi(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
+                               coef * bf16hi(hh.w[e]);
+              dw[e] = pack_bf16x2(d0, d1);
+            }
+            stg8(p.dh_out + rowoff + n, dw);
+          }
+        }
+      }
+    }
+  }
+};
+
+}  // namespace coda

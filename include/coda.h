@@ -1,0 +1,182 @@
+/*
+ * coda.h -- C ABI of libcoda.so: the GEMM -> residual -> RMSNorm -> GEMM chain
+ *
+ *     h = x @ W0 + z                      (new residual stream)
+ *     r = 1 / sqrt(mean_j h^2 + eps)      (one float per row)
+ *     y = RMSNorm(h, gamma) @ W1 = r * ((h * gamma) @ W1)
+ *
+ * computed as two GEMM-epilogue programs on an sm_103a GPU, and its
+ * data-gradient twin grad_h = RMSNormBackward(grad_y @ W1^T).
+ *
+ * Source of the method: "CODA：将 Transformer 块重写为 GEMM-Epilogue 程序以消除显存瓶颈"
+ * (blog.hotdry.top), section "GEMM-Residual-RMSNorm-GEMM 重参数化" (the
+ * reparameterisation and its three steps) and section
+ * "反向传播的 GEMM-Epilogue 结构" (the backward keeps the GEMM-epilogue shape; the
+ * row statistic s = sum_cols(grad_h2 * h2) = sum_cols(grad_y * y) is formed at
+ * the GEMM boundary).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers (memory of the current CUDA
+ *    device), row-major and densely packed.  bf16 tensors hold IEEE bfloat16
+ *    bit patterns (coda_bf16).  Weights are stored [in, out]:
+ *    W0 is [d, d], W1 is [d, N1].
+ *  - Every pointer must be 16-byte aligned.  Outputs must not alias inputs or
+ *    each other.
+ *  - Shapes: M >= 0 rows (M == 0 is a no-op that returns CODA_OK), d and N1
+ *    positive multiples of 8 (rows must start on 16-byte boundaries), all
+ *    below 2^31.
+ *  - The caller owns every buffer, including the workspace; the library never
+ *    allocates, frees or synchronises inside coda_fwd / coda_bwd_dgrad.  Work
+ *    is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *  - Argument checks happen before anything is enqueued; on any error nothing
+ *    is launched.  Device-side failures (a bounded wait that ran out) are
+ *    reported later by coda_get_device_status().
+ *  - Numerics: bf16 operands, fp32 accumulation in tensor memory, fp32
+ *    epilogue arithmetic, bf16 round-to-nearest-even stores.
+ */
+#ifndef CODA_H_
+#define CODA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define CODA_API __attribute__((visibility("default")))
+#else
+#define CODA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t coda_bf16; /* IEEE bfloat16 bit pattern */
+
+typedef enum {
+  CODA_OK = 0,
+  CODA_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad eps */
+  CODA_ERR_UNSUPPORTED_SHAPE = 2,  /* d or N1 not a positive multiple of 8, or too large */
+  CODA_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+  CODA_ERR_WORKSPACE_TOO_SMALL = 4,
+  CODA_ERR_LAUNCH = 5,             /* a CUDA launch or tensor-map encode failed */
+  CODA_ERR_DEVICE_TIMEOUT = 6,     /* a bounded device-side wait ran out */
+  CODA_ERR_NO_DEVICE = 7,          /* no CUDA device is current */
+  CODA_ERR_UNSUPPORTED_DEVICE = 8  /* the current device is not compute capability 10.3 */
+} coda_status_t;
+
+/* Bytes of device workspace coda_fwd needs: the bf16 GEMM1 operand
+ * hg = h * gamma ([M, d]) and the fp32 per-(row, column-tile) partial sums of
+ * h^2.  Returns 0 for M == 0. */
+CODA_API size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
+
+/* Bytes of device workspace coda_bwd_dgrad needs: fp32 per-(row, column-tile)
+ * partial row statistics and one 64-bit completion flag per output tile. */
+CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1);
+
+/*
+ * Forward of the chain (the method's three steps, see the file header):
+ *   1. GEMM0 epilogue: h = x @ W0 + z (fp32), stores h and hg = h * gamma as
+ *      bf16, and writes per-(row, 256-column tile) partial sums of h^2
+ *      (fp32, taken before rounding h).
+ *   2. auxiliary row reduction: r[m] = 1 / sqrt(sum of partials / d + eps).
+ *   3. GEMM1 epilogue: y = r[m] * (hg @ W1), stored bf16.
+ * No normalised [M, d] tensor is ever written.
+ *
+ *   x      [M, d]   bf16 in     z     [M, d]  bf16 in (residual)
+ *   W0     [d, d]   bf16 in     gamma [d]     bf16 in (RMSNorm weight)
+ *   W1     [d, N1]  bf16 in     eps   >= 0, finite
+ *   h_out  [M, d]   bf16 out    (new residual stream; saved for backward)
+ *   r_out  [M]      fp32 out    (inverse RMS per row; saved for backward)
+ *   y_out  [M, N1]  bf16 out
+ *   workspace: device memory of at least coda_fwd_workspace_bytes(M, d, N1)
+ *   bytes (contents on entry are ignored; clobbered).
+ */
+CODA_API coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
+                       const coda_bf16* gamma, const coda_bf16* W1, float eps,
+                       int64_t M, int64_t d, int64_t N1,
+                       coda_bf16* h_out, float* r_out, coda_bf16* y_out,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Data gradient through the RMSNorm branch, as one GEMM-epilogue program:
+ *   grad_h2 = grad_y @ W1^T  accumulated in tensor memory, then in the epilogue
+ *   q[m]    = sum_j grad_h2[m,j] * gamma[j] * h[m,j]  (so s = r * q equals
+ *             sum_j grad_h2 * h2 = sum_n grad_y * y), completed across the
+ *             row's column tiles through the workspace, and
+ *   grad_h  = r * gamma * grad_h2 - (r^3 * q / d) * h,  stored bf16.
+ * No separate norm-backward kernel runs and grad_h2 never reaches memory.
+ *
+ *   dy      [M, N1] bf16 in     W1    [d, N1] bf16 in
+ *   h       [M, d]  bf16 in     r     [M]     fp32 in   (both as saved by coda_fwd)
+ *   gamma   [d]     bf16 in
+ *   dh_out  [M, d]  bf16 out
+ *   workspace: at least coda_bwd_dgrad_workspace_bytes(M, d, N1) bytes.  The
+ *   completion flags carry a per-call 64-bit token, so the workspace needs no
+ *   clearing between calls; two calls that share a workspace must not run
+ *   concurrently.
+ * The kernel is a cooperative launch (all its blocks are resident at once).
+ */
+CODA_API coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const coda_bf16* h,
+                             const float* r, const coda_bf16* gamma,
+                             int64_t M, int64_t d, int64_t N1,
+                             coda_bf16* dh_out, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/* Synchronises `stream`, then reports and clears the library's device-side
+ * status word: CODA_OK, or CODA_ERR_DEVICE_TIMEOUT if a bounded wait in any
+ * kernel of this library ran out since the last call.  If `detail` is not
+ * NULL it receives the raw code (0 = none; otherwise which wait gave up).
+ * Returns CODA_ERR_LAUNCH if the stream itself reports a CUDA error. */
+CODA_API coda_status_t coda_get_device_status(cudaStream_t stream, uint32_t* detail);
+
+/* Upper bound, in nanoseconds, of every device-side wait launched after this
+ * call (default 1e9 = 1 s).  A wait that runs out records
+ * CODA_ERR_DEVICE_TIMEOUT and lets its kernel finish without hanging. */
+CODA_API void coda_set_wait_timeout_ns(uint64_t ns);
+
+/* Human-readable name of a status code (static storage). */
+CODA_API const char* coda_status_string(coda_status_t status);
+
+/*
+ * Measurement-only unfused reference sequence, built from the same GEMM
+ * mainloop: GEMM0 with a plain epilogue (h = x @ W0 + z), a standalone
+ * RMSNorm kernel that writes hn = r * h * gamma ([M, d] bf16) and r, then GEMM1
+ * with a plain epilogue (y = hn @ W1).  It exists to show, with hardware
+ * counters, the [M, d] round trip and the extra kernel that coda_fwd removes.
+ * Same arguments and conventions as coda_fwd; workspace of at least
+ * coda_fwd_unfused_workspace_bytes(M, d, N1) bytes.
+ */
+CODA_API size_t coda_fwd_unfused_workspace_bytes(int64_t M, int64_t d, int64_t N1);
+CODA_API coda_status_t coda_fwd_unfused(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
+                               const coda_bf16* gamma, const coda_bf16* W1, float eps,
+                               int64_t M, int64_t d, int64_t N1,
+                               coda_bf16* h_out, float* r_out, coda_bf16* y_out,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Measurement hook.  While `events` is non-NULL, every kernel launch k
+ * (0-based, counted within one coda_fwd / coda_fwd_unfused / coda_bwd_dgrad
+ * call) is followed by cudaEventRecord(events[k], stream) for k < n, so that
+ * a caller that records its own event before the call can time each launch
+ * on the launching stream.  coda_fwd launches 3 kernels (GEMM0, row
+ * reduction, GEMM1), coda_bwd_dgrad 1.  The events are caller-owned; pass
+ * NULL to stop.  Process-wide setting, not thread-safe; no effect on results.
+ */
+CODA_API void coda_set_launch_events(cudaEvent_t* events, int n);
+
+/*
+ * Self-test of the device-side watchdog: launches one block whose waits (on
+ * an mbarrier that nobody arrives on, and on a global flag that nobody sets)
+ * are bounded by `timeout_ns`.  Both waits run out by construction, so a
+ * following coda_get_device_status() must report CODA_ERR_DEVICE_TIMEOUT.
+ * No other work is affected and the CUDA context stays usable.
+ */
+CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CODA_H_ */

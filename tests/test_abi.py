@@ -1,0 +1,102 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+symbol include/coda.h declares; workspace sizes; argument validation that
+returns before anything touches a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "coda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+
+    g.build()
+    from gemm_epilogue_fusion_gemm0_gb300 import binding as B
+
+    return B
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CODA_API\s+[\w\s\*]+?\b(coda_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_symbols()
+    for must in ("coda_fwd", "coda_bwd_dgrad", "coda_fwd_workspace_bytes",
+                 "coda_bwd_dgrad_workspace_bytes", "coda_get_device_status", "coda_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = lib.raw()
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+    assert set(declared_symbols()) == set(lib.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code, name in lib.STATUS_NAMES.items():
+        assert lib.status_string(code) == name
+
+
+def test_workspace_sizes(lib):
+    # hg [M,d] bf16 + partial sums [ceil(d/256), M] fp32, each rounded up to 256 B
+    M, d, N1 = 8192, 4096, 28672
+    assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 16 * M * 4
+    assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == M * d * 2
+    # qpart [16, M] fp32 + flags [64 * 16] u64
+    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 16 * M * 4 + 64 * 16 * 8
+    assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
+    assert lib.coda_fwd_workspace_bytes(300, 328, 776) == 196864 + 2560  # ragged: rounded up
+    assert lib.coda_fwd_workspace_bytes(10, 12, 16) == 0  # d % 8 != 0: unsupported
+
+
+FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced
+
+
+def _fwd(lib, M=128, d=256, N1=512, eps=1e-5, ptrs=None, ws=FAKE, wsb=1 << 30):
+    p = [FAKE] * 8 if ptrs is None else ptrs
+    return lib.raw().coda_fwd(p[0], p[1], p[2], p[3], p[4], eps, M, d, N1, p[5], p[6], p[7],
+                              ws, wsb, None)
+
+
+def _bwd(lib, M=128, d=256, N1=512, ptrs=None, ws=FAKE, wsb=1 << 30):
+    p = [FAKE] * 6 if ptrs is None else ptrs
+    return lib.raw().coda_bwd_dgrad(p[0], p[1], p[2], p[3], p[4], M, d, N1, p[5], ws, wsb, None)
+
+
+def test_argument_validation_before_any_launch(lib):
+    E = {v: k for k, v in lib.STATUS_NAMES.items()}
+    assert _fwd(lib, M=-1) == E["CODA_ERR_INVALID_ARG"]
+    assert _fwd(lib, d=0) == E["CODA_ERR_INVALID_ARG"]
+    assert _fwd(lib, M=0) == E["CODA_OK"]  # empty batch: no-op
+    assert _fwd(lib, d=260) == E["CODA_ERR_UNSUPPORTED_SHAPE"]
+    assert _fwd(lib, N1=100) == E["CODA_ERR_UNSUPPORTED_SHAPE"]
+    assert _fwd(lib, ptrs=[FAKE] * 7 + [0]) == E["CODA_ERR_INVALID_ARG"]
+    assert _fwd(lib, ptrs=[FAKE + 8] + [FAKE] * 7) == E["CODA_ERR_MISALIGNED"]
+    assert _fwd(lib, eps=float("nan")) == E["CODA_ERR_INVALID_ARG"]
+    assert _fwd(lib, eps=-1.0) == E["CODA_ERR_INVALID_ARG"]
+    assert _fwd(lib, wsb=100) == E["CODA_ERR_WORKSPACE_TOO_SMALL"]
+    assert _fwd(lib, ws=0) == E["CODA_ERR_WORKSPACE_TOO_SMALL"]
+    assert _bwd(lib, M=-5) == E["CODA_ERR_INVALID_ARG"]
+    assert _bwd(lib, M=0) == E["CODA_OK"]
+    assert _bwd(lib, d=12) == E["CODA_ERR_UNSUPPORTED_SHAPE"]
+    assert _bwd(lib, ptrs=[FAKE] * 5 + [FAKE + 4]) == E["CODA_ERR_MISALIGNED"]
+    assert _bwd(lib, wsb=8) == E["CODA_ERR_WORKSPACE_TOO_SMALL"]
+
+
+def test_no_device_is_reported_without_gpu(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    E = {v: k for k, v in lib.STATUS_NAMES.items()}
+    assert _fwd(lib) == E["CODA_ERR_NO_DEVICE"]
+    assert _bwd(lib) == E["CODA_ERR_NO_DEVICE"]
