@@ -106,7 +106,8 @@ def test_eps_zero_and_large(B):
 
 
 def test_zero_row(B):
-    """A row with x = z = 0 has h = 0, r = 1/sqrt(eps), y = 0, dh = 0."""
+    """A row with x = z = 0 has h = 0, r = 1/sqrt(eps) and y = 0; its gradient
+    is r * gamma * (dy @ W1^T) (the h-term vanishes), checked with the oracle."""
     dev = torch.device("cuda:0")
     M, d, N1, eps = 130, 256, 256, 1e-5
     t = synth.make_forward_inputs(M, d, N1, seed=3)
@@ -114,11 +115,14 @@ def test_zero_row(B):
     t["z"][129] = 0
     g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
     h, r, y = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps)
-    dy = synth.make_grad_output(t["_rng"], M, N1).to(dev)
-    dh = B.coda_bwd_dgrad(dy, g["W1"], h, r, g["gamma"])
+    dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
+    dh = B.coda_bwd_dgrad(dy_cpu.to(dev), g["W1"], h, r, g["gamma"])
     torch.cuda.synchronize()
-    assert torch.all(h[129] == 0) and torch.all(y[129] == 0) and torch.all(dh[129] == 0)
+    assert torch.all(h[129] == 0) and torch.all(y[129] == 0)
     assert abs(r[129].item() - 1.0 / np.sqrt(np.float32(eps))) <= 1e-3 * r[129].item()
+    bref = oracle.backward_dgrad(f64(dy_cpu), f64(t["W1"]), f64(h), f64(r), f64(t["gamma"]))
+    check("dh", f64(dh), bref.dh, TOL_DH)
+    check("dh[zero row]", f64(dh[129:130]), bref.dh[129:130], TOL_DH)
 
 
 def test_empty_batch_is_noop(B):
