@@ -52,6 +52,7 @@ EXPORTS = {
     "coda_status_string": (ctypes.c_char_p, [_st]),
     "coda_watchdog_selftest": (_st, [_u64, _vp]),
     "coda_set_launch_events": (None, [_vp, ctypes.c_int]),
+    "coda_bwd_dgrad_noalloc": (_st, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
 }
 
 for _name, (_res, _args) in EXPORTS.items():

@@ -470,3 +470,107 @@ coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Data gradient without any allocation: scratch in a static device array.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) at the
+// point where they run the backward: code inside a custom allocator or
+// memory-pool callback, runtimes that forbid allocation while a step is in
+// flight because it could synchronise the device or fragment a pre-sized
+// pool, and embedders whose device memory is fully reserved up front.  For
+// them this entry point takes only inputs and outputs; the partial row
+// statistics and completion flags that coda_bwd_dgrad keeps in the caller's
+// workspace live instead in the fixed array below, which every GPU that
+// loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocPartials = CODA_NOALLOC_MAX_PARTIALS;  // fp32 per-(row, column tile)
+constexpr size_t kNoAllocFlags = CODA_NOALLOC_MAX_TILES;        // u64 per output tile
+constexpr size_t kNoAllocFlagOffset = kNoAllocPartials * sizeof(float);
+constexpr size_t kNoAllocBytes = kNoAllocFlagOffset + kNoAllocFlags * sizeof(uint64_t);
+
+// 2 MiB of partials + 128 KiB of flags.  The flags need no clearing: each
+// call publishes a fresh 64-bit token, so values left by an earlier call never
+// match (and the array starts zeroed, a value no call ever uses).
+static __device__ __align__(256) unsigned char g_noalloc_dgrad_scratch[kNoAllocBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_scratch_addr[kMaxDevices] = {};
+
+// Device address of the static array on the current device, looked up once per
+// device (the name itself is only a host-side stand-in in host code).
+coda_status_t noalloc_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return CODA_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_dgrad_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return CODA_ERR_LAUNCH;
+    }
+    g_noalloc_scratch_addr[dev] = p;
+  }
+  *out = g_noalloc_scratch_addr[dev];
+  return CODA_OK;
+}
+
+}  // namespace
+
+extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_bf16* W1,
+                                                const coda_bf16* h, const float* r,
+                                                const coda_bf16* gamma, int64_t M, int64_t d,
+                                                int64_t N1, coda_bf16* dh_out,
+                                                cudaStream_t stream) {
+  coda_status_t st = check_common(M, d, N1);
+  if (st != CODA_OK) return st;
+  if (M == 0) return CODA_OK;
+  if (!dy || !W1 || !h || !r || !gamma || !dh_out) return CODA_ERR_INVALID_ARG;
+  const void* ptrs[] = {dy, W1, h, r, gamma, dh_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CODA_ERR_MISALIGNED;
+  const int64_t mt64 = cdiv(M, kBM), nt64 = cdiv(d, kBN);
+  if (static_cast<uint64_t>(nt64) * static_cast<uint64_t>(M) > kNoAllocPartials ||
+      static_cast<uint64_t>(mt64) * static_cast<uint64_t>(nt64) > kNoAllocFlags)
+    return CODA_ERR_UNSUPPORTED_SHAPE;  // larger than the static scratch
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != CODA_OK) return st;
+  void* scratch = nullptr;
+  st = noalloc_scratch_address(&scratch);
+  if (st != CODA_OK) return st;
+
+  const int mt = static_cast<int>(mt64);
+  const int nt = static_cast<int>(nt64);
+  const int grid = std::min(sms, mt * nt);
+  if (nt > grid) return CODA_ERR_UNSUPPORTED_SHAPE;
+
+  CUtensorMap mA, mB;
+  bool ok = tmap_2d(&mA, dy, N1, M, kBK, kBM);
+  ok &= tmap_2d(&mB, W1, N1, d, kBK, kBN);
+  if (!ok) return CODA_ERR_LAUNCH;
+
+  EpiRmsNormBackward::Params p;
+  p.h = reinterpret_cast<const __nv_bfloat16*>(h);
+  p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  p.r = r;
+  p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
+  p.qpart = reinterpret_cast<float*>(scratch);
+  p.flags = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(scratch) + kNoAllocFlagOffset);
+  uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
+  if (tok == 0) tok = 1;
+  p.token = tok;
+  cudaError_t e = launch(kDgrad, grid, kThreads, kSmemBytes, stream, true, mA, mB,
+                         static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
+                         g_timeout_ns.load());
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  return CODA_OK;
+}

@@ -175,6 +175,42 @@ CODA_API void coda_set_launch_events(cudaEvent_t* events, int n);
  */
 CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t stream);
 
+/*
+ * coda_bwd_dgrad without a workspace, for callers that cannot allocate.
+ *
+ * The method's pages have no counterpart to this entry point; it exists for
+ * callers that must not allocate device memory when they run the backward:
+ * code running inside an allocator or memory-pool callback, runtimes that
+ * forbid allocation mid-step (an allocation can synchronise the device or
+ * fragment a pool sized up front), and embedders whose device memory is fully
+ * reserved in advance.  It computes exactly what coda_bwd_dgrad computes, with
+ * the same kernel, but takes only inputs and outputs: the per-tile partial row
+ * statistics and the completion flags live in a fixed array inside the
+ * library (CODA_NOALLOC_MAX_PARTIALS floats + CODA_NOALLOC_MAX_TILES 64-bit
+ * flags, about 2.1 MiB), which every GPU that loads the library holds until
+ * the process exits.  It allocates nothing and calls no allocating routine.
+ *
+ *  - Size limit: ceil(d/256) * M <= CODA_NOALLOC_MAX_PARTIALS and
+ *    ceil(M/128) * ceil(d/256) <= CODA_NOALLOC_MAX_TILES, otherwise it returns
+ *    CODA_ERR_UNSUPPORTED_SHAPE without launching (e.g. M = 32768 rows at
+ *    d = 4096, or 16384 rows at d = 8192, fit).
+ *  - The first call on each device looks up the device address of the array
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call uses the same array.  Nothing in it needs clearing (each call
+ *    tags its flags with a fresh 64-bit token), but calls whose kernels
+ *    overlap on the GPU, on different streams or from different host threads,
+ *    race on it and give wrong results: order them (one stream, or events).
+ *  - Otherwise the arguments, checks and errors are those of coda_bwd_dgrad.
+ */
+#define CODA_NOALLOC_MAX_PARTIALS 524288
+#define CODA_NOALLOC_MAX_TILES 16384
+CODA_API coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_bf16* W1,
+                                              const coda_bf16* h, const float* r,
+                                              const coda_bf16* gamma,
+                                              int64_t M, int64_t d, int64_t N1,
+                                              coda_bf16* dh_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
