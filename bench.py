@@ -251,6 +251,8 @@ def run_coda(args):
     ge.build()
     from gemm_epilogue_fusion_gemm0_gb300 import binding as B
 
+    if args.mma_mode is not None:
+        B.coda_set_mma_mode(args.mma_mode)
     dev = torch.device("cuda", torch.cuda.current_device())
     w = WORKLOAD
     M, d, N1, eps = w.M, w.d, w.N1, w.eps
@@ -395,6 +397,7 @@ def run_coda(args):
             "workload": f"{w.name} fwd + bwd-dgrad (M={M}, d={d}, N1={N1}, eps={eps})",
             "M": M, "d": d, "N1": N1, "eps": eps, "step": "coda_fwd + coda_bwd_dgrad",
             "parallelism": f"replicas x{world} (rows sharded, no collective)",
+            "mma": ["cta_group::1 128x256 tiles", "cta_group::2 256x256 tiles"][B.coda_get_mma_mode()],
             "l2": "no flush: inputs larger than L2 (W1 235 MB, dy 470 MB; ~1.6 GB touched per step)",
         },
         "fwd_tflops": w.fwd_flops / (fwd_ms * 1e-3) / 1e12,
@@ -421,6 +424,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mma-mode", type=int, choices=[0, 1], default=None,
+                    help="0: single-CTA tiles, 1: CTA-pair tiles (library default)")
     args = ap.parse_args()
     world, _, _ = dist_env()
     if args.gpus != world and world == 1 and args.gpus > 1:

@@ -53,6 +53,8 @@ EXPORTS = {
     "coda_watchdog_selftest": (_st, [_u64, _vp]),
     "coda_set_launch_events": (None, [_vp, ctypes.c_int]),
     "coda_bwd_dgrad_noalloc": (_st, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
+    "coda_set_mma_mode": (_st, [ctypes.c_int]),
+    "coda_get_mma_mode": (ctypes.c_int, []),
 }
 
 for _name, (_res, _args) in EXPORTS.items():
@@ -172,6 +174,15 @@ def coda_get_device_status(stream=None) -> tuple[int, int]:
     detail = ctypes.c_uint32(0)
     st = _lib.coda_get_device_status(_stream_ptr(stream), ctypes.byref(detail))
     return int(st), int(detail.value)
+
+
+def coda_set_mma_mode(mode: int) -> None:
+    """0: single-CTA 128x256 tiles; 1: CTA-pair 256x256 tiles (tcgen05 cta_group::2)."""
+    _check(_lib.coda_set_mma_mode(int(mode)), "coda_set_mma_mode")
+
+
+def coda_get_mma_mode() -> int:
+    return int(_lib.coda_get_mma_mode())
 
 
 def coda_set_wait_timeout_ns(ns: int) -> None:

@@ -21,6 +21,7 @@
 
 #include "coda.h"
 #include "epilogues.cuh"
+#include "gemm_pair.cuh"
 
 namespace coda {
 
@@ -101,6 +102,9 @@ __global__ void watchdog_selftest_kernel(uint64_t timeout_ns) {
 static auto* const kGemm0 = &gemm_epilogue_kernel<EpiResidualGammaSumsq, true>;
 static auto* const kGemm1 = &gemm_epilogue_kernel<EpiRowScale, true>;
 static auto* const kDgrad = &gemm_epilogue_kernel<EpiRmsNormBackward, false>;
+static auto* const kPairGemm0 = &gemm_pair_epilogue_kernel<EpiResidualGammaSumsq, true>;
+static auto* const kPairGemm1 = &gemm_pair_epilogue_kernel<EpiRowScale, true>;
+static auto* const kPairDgrad = &gemm_pair_epilogue_kernel<EpiRmsNormBackward, false>;
 
 }  // namespace coda
 
@@ -112,18 +116,21 @@ namespace {
 using namespace coda;
 
 constexpr int kMaxDevices = 64;
-constexpr int kGroupM = 16;  // row blocks per L2 group for the forward GEMMs
+constexpr int kGroupM = 16;     // 128-row blocks per L2 group (single-CTA tiles)
+constexpr int kPairGroupM = 8;  // 256-row blocks per L2 group (CTA-pair tiles)
 
 struct DevState {
   bool init = false;
   coda_status_t status = CODA_OK;
   int sms = 0;
+  int max_pairs = 0;  // co-resident clusters of two for the CTA-pair kernels
 };
 
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_mma_mode{1};  // 0: single-CTA 128x256 tiles, 1: CTA-pair 256x256 tiles (default)
 std::atomic<uint64_t> g_token_ctr{0};
 uint64_t g_token_salt = 0;
 cudaEvent_t* g_launch_events = nullptr;  // measurement hook (coda_set_launch_events)
@@ -138,7 +145,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-coda_status_t device_setup(int* sms) {
+coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -166,6 +173,23 @@ coda_status_t device_setup(int* sms) {
                                  kSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm0, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (count / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kPairSmemBytes;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kPairDgrad, &cfg) == cudaSuccess)
+          s.max_pairs = std::min(clusters, count / 2);
+        else
+          ok = false;
+      }
       if (g_encode == nullptr) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -191,6 +215,7 @@ coda_status_t device_setup(int* sms) {
     s.init = true;
   }
   *sms = s.sms;
+  if (max_pairs) *max_pairs = s.max_pairs;
   return s.status;
 }
 
@@ -260,9 +285,10 @@ coda_status_t fwd_impl(bool fused, const coda_bf16* x, const coda_bf16* W0, cons
   if (workspace == nullptr || workspace_bytes < fwd_ws_bytes(M, d, fused))
     return CODA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
-  int sms = 0;
-  st = device_setup(&sms);
+  int sms = 0, max_pairs = 0;
+  st = device_setup(&sms, &max_pairs);
   if (st != CODA_OK) return st;
+  const bool pair = g_mma_mode.load() == 1;
 
   FwdWorkspace ws;
   ws.act = reinterpret_cast<__nv_bfloat16*>(workspace);
@@ -289,8 +315,12 @@ coda_status_t fwd_impl(bool fused, const coda_bf16* x, const coda_bf16* W0, cons
   p0.h_out = reinterpret_cast<__nv_bfloat16*>(h_out);
   p0.hg_out = fused ? ws.act : nullptr;
   p0.part = ws.part;
-  cudaError_t e = launch(kGemm0, std::min(sms, mt * nt0), kThreads, kSmemBytes, stream, false, mA0,
-                         mB0, Mi, di, di, kGroupM, p0, tmo);
+  const int mtp = static_cast<int>(cdiv(M, kPairBM));
+  cudaError_t e =
+      pair ? launch(kPairGemm0, 2 * std::min(max_pairs, mtp * nt0), kThreads, kPairSmemBytes,
+                    stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, tmo)
+           : launch(kGemm0, std::min(sms, mt * nt0), kThreads, kSmemBytes, stream, false, mA0,
+                    mB0, Mi, di, di, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -311,8 +341,10 @@ coda_status_t fwd_impl(bool fused, const coda_bf16* x, const coda_bf16* W0, cons
   EpiRowScale::Params p1;
   p1.r = fused ? r_out : nullptr;
   p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
-  e = launch(kGemm1, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false, mA1, mB1, Mi,
-             N1i, di, kGroupM, p1, tmo);
+  e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
+                    stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
+           : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false, mA1, mB1,
+                    Mi, N1i, di, kGroupM, p1, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -337,8 +369,9 @@ size_t coda_fwd_unfused_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
 
 size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
-  const int64_t mt = cdiv(M, kBM), nt = cdiv(d, kBN);
-  return align256(static_cast<size_t>(nt) * M * 4) + align256(static_cast<size_t>(mt) * nt * 8);
+  // one flag per (128-row slab, column tile); CTA-pair tiles cover 2 * ceil(M/256) slabs
+  const int64_t slabs = 2 * cdiv(M, kPairBM), nt = cdiv(d, kBN);
+  return align256(static_cast<size_t>(nt) * M * 4) + align256(static_cast<size_t>(slabs) * nt * 8);
 }
 
 coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
@@ -372,18 +405,21 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   if (workspace == nullptr || workspace_bytes < coda_bwd_dgrad_workspace_bytes(M, d, N1))
     return CODA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
-  int sms = 0;
-  st = device_setup(&sms);
+  int sms = 0, max_pairs = 0;
+  st = device_setup(&sms, &max_pairs);
   if (st != CODA_OK) return st;
+  const bool pair = g_mma_mode.load() == 1;
 
-  const int mt = static_cast<int>(cdiv(M, kBM));
+  // Row-major tile order; every column tile of a row block must be in flight
+  // at once (at most one wave per row block), see EpiRmsNormBackward.
   const int nt = static_cast<int>(cdiv(d, kBN));
-  const int grid = std::min(sms, mt * nt);
-  if (nt > grid) return CODA_ERR_UNSUPPORTED_SHAPE;  // a row block must fit in one wave
+  const int mt = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
+  const int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
+  if (nt > units) return CODA_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap mA, mB;
-  bool ok = tmap_2d(&mA, dy, N1, M, kBK, kBM);   // dy [M, N1]       K-major (K = N1)
-  ok &= tmap_2d(&mB, W1, N1, d, kBK, kBN);       // W1 [d(N), N1(K)] K-major
+  bool ok = tmap_2d(&mA, dy, N1, M, kBK, kBM);                  // dy [M, N1] K-major (K = N1)
+  ok &= tmap_2d(&mB, W1, N1, d, kBK, pair ? 128 : kBN);         // W1 [d(N), N1(K)] K-major
   if (!ok) return CODA_ERR_LAUNCH;
 
   EpiRmsNormBackward::Params p;
@@ -397,9 +433,13 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
   if (tok == 0) tok = 1;
   p.token = tok;
-  cudaError_t e = launch(kDgrad, grid, kThreads, kSmemBytes, stream, true, mA, mB,
-                         static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
-                         g_timeout_ns.load());
+  cudaError_t e =
+      pair ? launch(kPairDgrad, 2 * units, kThreads, kPairSmemBytes, stream, true, mA, mB,
+                    static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
+                    g_timeout_ns.load())
+           : launch(kDgrad, units, kThreads, kSmemBytes, stream, true, mA, mB,
+                    static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
+                    g_timeout_ns.load());
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -439,6 +479,14 @@ void coda_set_launch_events(cudaEvent_t* events, int n) {
   g_launch_events = (n > 0) ? events : nullptr;
   g_launch_events_n = (n > 0) ? n : 0;
 }
+
+coda_status_t coda_set_mma_mode(int mode) {
+  if (mode != 0 && mode != 1) return CODA_ERR_INVALID_ARG;
+  g_mma_mode.store(mode);
+  return CODA_OK;
+}
+
+int coda_get_mma_mode(void) { return g_mma_mode.load(); }
 
 void coda_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1 : ns); }
 

@@ -1,0 +1,234 @@
+// gemm_pair.cuh -- the GEMM-epilogue kernel on a CTA pair (tcgen05 .cta_group::2).
+//
+// Same contract and epilogue policies as gemm_epilogue_kernel (gemm.cuh), but a
+// cluster of two CTAs on two SMs computes one 256 x 256 output tile:
+//   - CTA r (r = 0, 1) loads rows [128 r, 128 r + 128) of the A tile and half
+//     of the B tile (N columns [128 r, 128 r + 128)) into its own shared memory;
+//   - one thread of CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+//     K = 16), which reads both CTAs' operands and writes each CTA's 128
+//     accumulator rows into that CTA's tensor memory;
+//   - each CTA's epilogue drains its own 128 x 256 accumulator.
+// Each SM therefore streams 32 KB per 64-deep K step instead of 48 KB, which
+// leaves room for a 6-stage ring and halves the B traffic from L2.
+//
+// Barriers: the TMA of both CTAs completes on CTA 0's `full` barrier (CTA 0
+// arms it with both CTAs' bytes); the MMA commit is multicast to the `empty`,
+// `tfull` and `drain` barriers of both CTAs; each CTA's epilogue releases an
+// accumulator by one arrive on CTA 0's `tempty` barrier (count 2).
+#pragma once
+
+#include "gemm.cuh"
+
+namespace coda {
+
+constexpr int kPairBM = 256;                         // tile rows per CTA pair
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairAStageBytes = 128 * kBK * 2;  // 16 KB: this CTA's 128 rows
+constexpr uint32_t kPairBStageBytes = 128 * kBK * 2;  // 16 KB: this CTA's half of B
+constexpr uint32_t kPairStageBytes = kPairAStageBytes + kPairBStageBytes;
+constexpr uint32_t kPairSmemA = 0;
+constexpr uint32_t kPairSmemB = kPairStages * kPairAStageBytes;
+constexpr uint32_t kPairSmemBar = kPairSmemB + kPairStages * kPairBStageBytes;
+constexpr uint32_t kPairSmemBytes = kPairSmemBar + 256 + 1024;
+
+static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
+
+template <class Epi, bool kBMNMajor>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
+                              int group_m, const typename Epi::Params ep, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const uint32_t sA = base + kPairSmemA;
+  const uint32_t sB = base + kPairSmemB;
+  const uint32_t bar0 = base + kPairSmemBar;
+  // full[S] | empty[S] | tfull[2] | tempty[2] | drain
+  const uint32_t bar_full = bar0;
+  const uint32_t bar_empty = bar0 + 8u * kPairStages;
+  const uint32_t bar_tfull = bar0 + 16u * kPairStages;
+  const uint32_t bar_tempty = bar_tfull + 16u;
+  const uint32_t bar_drain = bar_tempty + 16u;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPairSmemBar + 128);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kPairSmemBar + 132);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int mt = (M + kPairBM - 1) / kPairBM;
+  const int nt = (N + kBN - 1) / kBN;
+  const int nk = (K + kBK - 1) / kBK;
+  const int num_tiles = mt * nt;
+  const TileMap tmap{mt, nt, group_m};
+  const WaitCtl wc{timeout_ns, &g_coda_status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(bar_full + 8u * s, 1);
+      mbar_init(bar_empty + 8u * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8u * b, 1);
+      mbar_init(bar_tempty + 8u * b, 2);
+    }
+    mbar_init(bar_drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued_mask = 0, last_par = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < num_tiles; t += npairs) {
+        int mb, nb;
+        tmap.coords(t, mb, nb);
+        const int arow = mb * kPairBM + static_cast<int>(rank) * 128;
+        const int bcol = nb * kBN + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_local = bar_full + 8u * s;
+          const uint32_t full_leader = mapa_shared(full_local, 0);
+          if (leader) mbar_arrive_expect_tx(full_local, 2u * kPairStageBytes);
+          const uint32_t a_dst = sA + s * kPairAStageBytes;
+          const uint32_t b_dst = sB + s * kPairBStageBytes;
+          tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, arow);
+          if constexpr (kBMNMajor) {
+            tma_load_2d_pair(b_dst, &tmB, full_leader, bcol, kb * kBK);
+            tma_load_2d_pair(b_dst + kBChunkBytes, &tmB, full_leader, bcol + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(b_dst, &tmB, full_leader, kb * kBK, bcol);
+          }
+          issued_mask |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+          if (++s == kPairStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // Let every issued copy (of both CTAs) land before the pair can exit.
+        for (int i = 0; i < kPairStages; ++i)
+          if (issued_mask & (1u << i)) {
+            const uint32_t p = (last_par >> i) & 1u;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar_full + 8u * i, p) && globaltimer_ns() - t0 < timeout_ns) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (CTA 0 only)
+    if (lane == 0) {
+      if (leader) {
+        constexpr uint32_t idesc = idesc_bf16_f32(kPairBM, kBN, false, kBMNMajor);
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = pair; ok && t < num_tiles; t += npairs, ++it) {
+          const uint32_t b = it & 1u;
+          const uint32_t aph = (it >> 1) & 1u;
+          if (!bounded_wait(bar_tempty + 8u * b, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * kBN;
+          for (int kb = 0; kb < nk; ++kb) {
+            if (!bounded_wait(bar_full + 8u * s, ph, wc, kSiteMmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = sA + s * kPairAStageBytes;
+            const uint32_t b0 = sB + s * kPairBStageBytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+              const uint64_t bd = kBMNMajor ? sdesc_sw128(b0 + k * 2048, kBChunkBytes, 1024)
+                                            : sdesc_sw128(b0 + k * 32, 16, 1024);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            umma_commit_pair_mc(bar_empty + 8u * s, 0x3);
+            if (++s == kPairStages) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair_mc(bar_tfull + 8u * b, 0x3);
+        }
+        // Always signal `drain` in both CTAs once every MMA issued here is done.
+        umma_commit_pair_mc(bar_drain, 0x3);
+      }
+      // Both CTAs: no TMEM release while MMAs may still write it.
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar_drain, 0)) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+          record_failure(wc, kSiteDrain);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    uint32_t it = 0;
+    for (int t = pair; t < num_tiles; t += npairs, ++it) {
+      const uint32_t b = it & 1u;
+      const uint32_t aph = (it >> 1) & 1u;
+      int mb, nb;
+      tmap.coords(t, mb, nb);
+      const bool ok = bounded_wait(bar_tfull + 8u * b, aph, wc, kSiteEpiTmemFull);
+      if (!epi_all(ok)) break;
+      tc_fence_after();
+      TileCtx c;
+      c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
+      c.mb = mb * 2 + static_cast<int>(rank);  // this CTA's 128-row slab
+      c.nb = nb;
+      c.row = row;
+      c.M = M;
+      c.N = N;
+      c.nt = nt;
+      Epi::apply(ep, wc, c);
+      tc_fence_before();
+      named_bar_sync(1, kEpiThreads);
+      if (threadIdx.x == kEpiFirstThread) mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * b, 0));
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace coda

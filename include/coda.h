@@ -131,6 +131,15 @@ CODA_API coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, 
  * Returns CODA_ERR_LAUNCH if the stream itself reports a CUDA error. */
 CODA_API coda_status_t coda_get_device_status(cudaStream_t stream, uint32_t* detail);
 
+/* Tile shape of the tensor-core GEMMs used by every following call:
+ *   0  one CTA per 128 x 256 output tile (tcgen05 .cta_group::1)
+ *   1  a pair of CTAs on two SMs per 256 x 256 tile (tcgen05 .cta_group::2);
+ *      each SM loads half of B, which halves operand traffic per SM (default).
+ * Results are identical up to the fp32 summation order inside the tensor
+ * cores.  Returns CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
+CODA_API coda_status_t coda_set_mma_mode(int mode);
+CODA_API int coda_get_mma_mode(void);
+
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records
  * CODA_ERR_DEVICE_TIMEOUT and lets its kernel finish without hanging. */

@@ -37,6 +37,15 @@ def B():
     return binding
 
 
+@pytest.fixture(params=[0, 1], ids=["cta1", "cta2"])
+def mode(request, B):
+    """Run the test with single-CTA tiles (0) and with CTA-pair tiles (1)."""
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(request.param)
+    yield request.param
+    B.coda_set_mma_mode(old)
+
+
 def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
@@ -92,20 +101,20 @@ def run_case(B, M, d, N1, eps, seed=0, rows=None, bwd=True, unfused=False):
     (1, 8, 8),           # smallest legal shape
     (129, 64, 264),      # one row past a tile; d < one column tile
 ])
-def test_forward_and_dgrad_small(B, M, d, N1):
+def test_forward_and_dgrad_small(B, mode, M, d, N1):
     run_case(B, M, d, N1, 1e-5)
 
 
-def test_unfused_sequence_matches_oracle(B):
+def test_unfused_sequence_matches_oracle(B, mode):
     run_case(B, 300, 328, 776, 1e-5, bwd=False, unfused=True)
 
 
-def test_eps_zero_and_large(B):
+def test_eps_zero_and_large(B, mode):
     run_case(B, 256, 256, 512, 0.0)
     run_case(B, 256, 256, 512, 0.5)
 
 
-def test_zero_row(B):
+def test_zero_row(B, mode):
     """A row with x = z = 0 has h = 0, r = 1/sqrt(eps) and y = 0; its gradient
     is r * gamma * (dy @ W1^T) (the h-term vanishes), checked with the oracle."""
     dev = torch.device("cuda:0")
@@ -140,7 +149,7 @@ def test_empty_batch_is_noop(B):
     assert dh.shape == (0, d)
 
 
-def test_repeat_calls_are_bitwise_deterministic(B):
+def test_repeat_calls_are_bitwise_deterministic(B, mode):
     dev = torch.device("cuda:0")
     M, d, N1 = 640, 512, 1280
     t = synth.make_forward_inputs(M, d, N1, seed=5)
@@ -176,6 +185,13 @@ def test_bad_arguments_on_gpu(B):
     assert B.coda_get_device_status() == (B.CODA_OK, 0)
 
 
+def test_mma_mode_setting(B):
+    old = B.coda_get_mma_mode()
+    with pytest.raises(B.CodaError):
+        B.coda_set_mma_mode(7)
+    assert B.coda_get_mma_mode() == old
+
+
 def test_watchdog_reports_timeout_and_context_survives(B):
     assert B.coda_get_device_status()[0] == B.CODA_OK
     assert B.coda_watchdog_selftest(20_000_000) == B.CODA_OK  # 20 ms per wait
@@ -187,7 +203,7 @@ def test_watchdog_reports_timeout_and_context_survives(B):
 
 # ----------------------------------------------------------------------------- Llama-shaped, full size
 @pytest.mark.parametrize("name", ["llama1b", "llama7b", "llama70b"])
-def test_llama_shapes_sampled_rows(B, name):
+def test_llama_shapes_sampled_rows(B, mode, name):
     w = synth.WORKLOADS[name]
     rows = synth.sample_rows(w.M, 512, seed=1)
     # llama7b also runs the data-gradient workload: saved h, r from this
