@@ -45,7 +45,8 @@ from gemm_epilogue_fusion_gemm0_gb300 import synth  # noqa: E402
 METRIC = "fused GEMM-Res-RMSNorm-GEMM TFLOP/s (fwd, bwd-dgrad); % of GB300 BF16 peak"
 WORKLOAD = synth.WORKLOADS["llama7b"]
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = ["csrc/coda.cu", "csrc/gemm.cuh", "csrc/epilogues.cuh", "csrc/ptx.cuh"]
+KERNEL_SOURCES = ["csrc/coda.cu", "csrc/gemm.cuh", "csrc/gemm_pair.cuh", "csrc/epilogues.cuh",
+                  "csrc/ptx.cuh"]
 
 
 def log(*a):
