@@ -16,4 +16,7 @@ from .coda_oracle import (  # noqa: F401
     forward,
     backward_dgrad,
     normwise_rel_err,
+    silu,
+    swiglu,
+    forward_swiglu,
 )

@@ -123,6 +123,30 @@ def backward_dgrad(dy, W1, h, r, gamma) -> BackwardResult:
     return BackwardResult(dh=dh, s=s, dh2=dh2)
 
 
+def silu(t) -> np.ndarray:
+    """silu(t) = t * sigmoid(t) = t / (1 + exp(-t))."""
+    t = _f64(t)
+    with np.errstate(over="ignore"):
+        return t / (1.0 + np.exp(-t))
+
+
+def swiglu(y) -> np.ndarray:
+    """Gated activation on a [gate | up] pre-activation (CODA blog, section
+    "五类 Epilogue 原语", SwiGLU gating; the pairing is the one of section
+    "成对激活的寄存器级融合"): with y = [g | u] split into two equal column
+    halves, a[:, j] = silu(g[:, j]) * u[:, j]."""
+    y = _f64(y)
+    half = y.shape[1] // 2
+    return silu(y[:, :half]) * y[:, half:]
+
+
+def forward_swiglu(x, W0, z, gamma, W1, eps: float):
+    """The chain followed by the gated activation: returns (ForwardResult, a)
+    with a = swiglu(RMSNorm(x @ W0 + z, gamma) @ W1), W1 = [W_gate | W_up]."""
+    f = forward(x, W0, z, gamma, W1, eps)
+    return f, swiglu(f.y)
+
+
 def normwise_rel_err(got, ref) -> float:
     """||got - ref||_F / ||ref||_F in float64 (the parity metric)."""
     got = _f64(got)

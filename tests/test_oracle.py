@@ -299,3 +299,67 @@ def test_planted_mistake_is_caught(name, monkeypatch):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake {name} was not caught by any pin"
+
+
+# ----------------------------------------------------------------------------
+# SwiGLU extension (gated activation on the [gate | up] output of the chain)
+# ----------------------------------------------------------------------------
+
+def pin_swiglu_bruteforce(seed=8):
+    rng = np.random.default_rng(seed)
+    for (M, d, N1) in [(3, 5, 4), (4, 9, 10), (2, 16, 32)]:
+        x, W0, z, gamma, W1, _, eps = _rand_case(rng, M, d, N1, eps=1e-5)
+        f, a = O.forward_swiglu(x, W0, z, gamma, W1, eps)
+        _, _, y = _brute_forward(x.tolist(), W0.tolist(), z.tolist(), gamma.tolist(), W1.tolist(), eps)
+        half = N1 // 2
+        ref = np.zeros((M, half))
+        for m in range(M):
+            for j in range(half):
+                g, u = y[m][j], y[m][half + j]
+                ref[m, j] = g / (1.0 + math.exp(-g)) * u
+        np.testing.assert_allclose(a, ref, rtol=1e-11, atol=1e-13)
+
+
+def pin_swiglu_library(seed=9):
+    rng = np.random.default_rng(seed)
+    y = rng.standard_normal((7, 12)) * 3.0
+    ref = (torch.nn.functional.silu(torch.tensor(y[:, :6])) * torch.tensor(y[:, 6:])).numpy()
+    np.testing.assert_allclose(O.swiglu(y), ref, rtol=1e-13, atol=1e-15)
+
+
+def pin_swiglu_closed_forms():
+    # silu(0) = 0; silu(t) -> t for t >> 0, -> 0 for t << 0; up = 1 gives silu(gate)
+    y = np.array([[0.0, 50.0, -50.0, 1.0, 2.0, 3.0, 4.0, 1.0]])
+    a = O.swiglu(y)
+    assert a[0, 0] == 0.0
+    np.testing.assert_allclose(a[0, 1], 50.0 * 3.0, rtol=1e-15)  # gate 50, up 3
+    assert abs(a[0, 2]) < 1e-18
+    np.testing.assert_allclose(a[0, 3], 1.0 / (1.0 + math.exp(-1.0)), rtol=1e-15)
+    # the gate is the first half and the up projection the second half
+    assert O.swiglu(np.array([[1.0, 0.0]]))[0, 0] == 0.0
+
+
+SWIGLU_PINS = [pin_swiglu_bruteforce, pin_swiglu_library, pin_swiglu_closed_forms]
+
+
+@pytest.mark.parametrize("pin", SWIGLU_PINS, ids=lambda p: p.__name__)
+def test_swiglu_pin(pin):
+    pin()
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("gate_up_swapped", lambda y: O.silu(np.asarray(y, float)[:, np.asarray(y).shape[1] // 2:])
+     * np.asarray(y, float)[:, :np.asarray(y).shape[1] // 2]),
+    ("interleaved_pairs", lambda y: O.silu(np.asarray(y, float)[:, 0::2]) * np.asarray(y, float)[:, 1::2]),
+    ("sigmoid_not_silu", lambda y: 1.0 / (1.0 + np.exp(-np.asarray(y, float)[:, :np.asarray(y).shape[1] // 2]))
+     * np.asarray(y, float)[:, np.asarray(y).shape[1] // 2:]),
+])
+def test_swiglu_planted_mistake_is_caught(name, fn, monkeypatch):
+    monkeypatch.setattr(O, "swiglu", fn)
+    failed = []
+    for pin in SWIGLU_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name} was not caught"
