@@ -19,4 +19,6 @@ from .coda_oracle import (  # noqa: F401
     silu,
     swiglu,
     forward_swiglu,
+    backward_swiglu,
+    backward_rmsnorm_given_s,
 )

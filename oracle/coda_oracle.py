@@ -147,6 +147,42 @@ def forward_swiglu(x, W0, z, gamma, W1, eps: float):
     return f, swiglu(f.y)
 
 
+def backward_swiglu(dout, W2, y):
+    """Backward of out = swiglu(y) @ W2 to the pre-activation y = [g | u].
+
+    Steps:
+      1. da = dout @ W2^T                        (W2 stored [in = N1/2, out])
+      2. dg = da * u * silu'(g),  du = da * silu(g)
+         with silu'(t) = sig(t) * (1 + t * (1 - sig(t))), sig the logistic
+      3. dy = [dg | du]
+    Also returns s = sum_n dy[:, n] * y[:, n], the row statistic of the RMSNorm
+    backward, formed where dy and y meet (CODA blog, section
+    "反向传播的 GEMM-Epilogue 结构": s = sum_cols(grad_y * y))."""
+    dout = _f64(dout)
+    y = _f64(y)
+    half = y.shape[1] // 2
+    g, u = y[:, :half], y[:, half:]
+    da = dout @ _f64(W2).T
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    dg = da * u * sig * (1.0 + g * (1.0 - sig))
+    du = da * g * sig
+    dy = np.concatenate([dg, du], axis=1)
+    s = np.sum(dy * y, axis=1)
+    return dy, s
+
+
+def backward_rmsnorm_given_s(dh2, h, r, gamma, s):
+    """RMSNorm-branch backward with the row statistic supplied from outside:
+    dh = r * gamma * dh2 - (r^2 * s / d) * h.  Equal to backward_dgrad's dh when
+    s = sum_j dh2_j * h2_j (the identity r * sum(g * h) = s)."""
+    dh2 = _f64(dh2)
+    h = _f64(h)
+    r = _f64(r)
+    d = h.shape[1]
+    return r[:, None] * _f64(gamma)[None, :] * dh2 - ((r ** 2) * _f64(s) / d)[:, None] * h
+
+
 def normwise_rel_err(got, ref) -> float:
     """||got - ref||_F / ||ref||_F in float64 (the parity metric)."""
     got = _f64(got)

@@ -363,3 +363,108 @@ def test_swiglu_planted_mistake_is_caught(name, fn, monkeypatch):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake {name} was not caught"
+
+
+# ----------------------------------------------------------------------------
+# SwiGLU backward and the statistic formed upstream
+# ----------------------------------------------------------------------------
+
+def _swiglu_case(rng, M=4, half=5, dout_w=6):
+    y = rng.standard_normal((M, 2 * half)) * 2.0
+    W2 = rng.standard_normal((half, dout_w)) / math.sqrt(half)
+    dout = rng.standard_normal((M, dout_w)) * 0.3
+    return y, W2, dout
+
+
+def pin_swiglu_bwd_autograd(seed=10):
+    """torch autograd of out = (silu(g) * u) @ W2 in fp64."""
+    rng = np.random.default_rng(seed)
+    for shape in [(4, 5, 6), (3, 16, 8)]:
+        y, W2, dout = _swiglu_case(rng, *shape)
+        ty = torch.tensor(y, requires_grad=True)
+        half = y.shape[1] // 2
+        out = (torch.nn.functional.silu(ty[:, :half]) * ty[:, half:]) @ torch.tensor(W2)
+        out.backward(torch.tensor(dout))
+        dy, s = O.backward_swiglu(dout, W2, y)
+        np.testing.assert_allclose(dy, ty.grad.numpy(), rtol=1e-11, atol=1e-13)
+
+
+def pin_swiglu_bwd_finite_differences(seed=11):
+    rng = np.random.default_rng(seed)
+    y, W2, dout = _swiglu_case(rng, 3, 4, 5)
+    dy, _ = O.backward_swiglu(dout, W2, y)
+    half = y.shape[1] // 2
+
+    def loss(yy):
+        return float(np.sum(dout * ((yy[:, :half] / (1 + np.exp(-yy[:, :half]))) * yy[:, half:] @ W2)))
+
+    fd = np.zeros_like(y)
+    for i in range(y.shape[0]):
+        for j in range(y.shape[1]):
+            yp, ym = y.copy(), y.copy()
+            yp[i, j] += 1e-6
+            ym[i, j] -= 1e-6
+            fd[i, j] = (loss(yp) - loss(ym)) / 2e-6
+    np.testing.assert_allclose(dy, fd, rtol=1e-6, atol=1e-9)
+
+
+def pin_statistic_upstream_equals_definition(seed=12):
+    """s formed upstream (sum dy * y) equals sum_j dh2_j h2_j of the definition,
+    and the given-s RMSNorm backward equals backward_dgrad."""
+    rng = np.random.default_rng(seed)
+    M, d, N1, dw = 5, 12, 10, 7
+    x, W0, z, gamma, W1, _, eps = _rand_case(rng, M, d, N1, eps=1e-5)
+    f = O.forward(x, W0, z, gamma, W1, eps)
+    W2 = rng.standard_normal((N1 // 2, dw)) / math.sqrt(N1 // 2)
+    dout = rng.standard_normal((M, dw)) * 0.2
+    dy, s = O.backward_swiglu(dout, W2, f.y)
+    b = O.backward_dgrad(dy, W1, f.h, f.r, gamma)
+    np.testing.assert_allclose(s, b.s, rtol=1e-10, atol=1e-13)
+    dh = O.backward_rmsnorm_given_s(b.dh2, f.h, f.r, gamma, s)
+    np.testing.assert_allclose(dh, b.dh, rtol=1e-9, atol=1e-13)
+
+
+SWIGLU_BWD_PINS = [pin_swiglu_bwd_autograd, pin_swiglu_bwd_finite_differences,
+                   pin_statistic_upstream_equals_definition]
+
+
+@pytest.mark.parametrize("pin", SWIGLU_BWD_PINS, ids=lambda p: p.__name__)
+def test_swiglu_bwd_pin(pin):
+    pin()
+
+
+def _swiglu_bwd_mutant(kind):
+    def bwd(dout, W2, y):
+        y = np.asarray(y, float)
+        half = y.shape[1] // 2
+        g, u = y[:, :half], y[:, half:]
+        da = np.asarray(dout, float) @ np.asarray(W2, float).T
+        sig = 1.0 / (1.0 + np.exp(-g))
+        dsilu = sig if kind == "dsilu_is_sigmoid" else sig * (1.0 + g * (1.0 - sig))
+        dg = da * u * dsilu
+        du = da * g * sig
+        dy = np.concatenate([du, dg] if kind == "halves_swapped" else [dg, du], axis=1)
+        return dy, np.sum(dy * y, axis=1)
+    return bwd
+
+
+@pytest.mark.parametrize("kind", ["dsilu_is_sigmoid", "halves_swapped"])
+def test_swiglu_bwd_planted_mistake_is_caught(kind, monkeypatch):
+    monkeypatch.setattr(O, "backward_swiglu", _swiglu_bwd_mutant(kind))
+    failed = []
+    for pin in SWIGLU_BWD_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed
+
+
+def test_given_s_planted_mistake_is_caught(monkeypatch):
+    # r^3 instead of r^2 in the given-s form
+    monkeypatch.setattr(O, "backward_rmsnorm_given_s",
+                        lambda dh2, h, r, gamma, s: np.asarray(r)[:, None] * np.asarray(gamma)[None, :]
+                        * np.asarray(dh2) - ((np.asarray(r) ** 3) * np.asarray(s) / np.shape(h)[1])[:, None]
+                        * np.asarray(h))
+    with pytest.raises(AssertionError):
+        pin_statistic_upstream_equals_definition()
