@@ -328,6 +328,56 @@ def run_coda(args):
     flops_step = w.fwd_flops + w.bwd_flops
     value = world * K * flops_step / (ms * 1e-3) / 1e12
 
+    # ---- widened path (not part of `value`): forward with the SwiGLU epilogue
+    a_sw = torch.empty((M, N1 // 2), dtype=torch.bfloat16, device=dev)
+    extras = {}
+    for _ in range(3):
+        B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw,
+                          ws=ws_f, stream=stream)
+    KS = max(3, min(K, 50))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    s0.record(stream)
+    for _ in range(KS):
+        B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw,
+                          ws=ws_f, stream=stream)
+    s1.record(stream)
+    barrier()
+    sw_ms = s0.elapsed_time(s1) / KS
+    extras["fwd_swiglu"] = {"ms": sw_ms, "tflops": w.fwd_flops / (sw_ms * 1e-3) / 1e12,
+                            "calls": KS, "gpu_launches": 3 * KS,
+                            "note": "coda_fwd_swiglu: GEMM1 epilogue applies r and silu(gate)*up"}
+    # backward through the gated activation and the down projection (Dout = d),
+    # statistic formed upstream, tile-local RMSNorm-branch data gradient
+    y_pre = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+    B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw, y=y_pre,
+                      ws=ws_f, stream=stream)
+    W2 = (torch.randn((N1 // 2, d), device=dev) / (N1 // 2) ** 0.5).to(torch.bfloat16)
+    dout = (torch.randn((M, d), device=dev) * 0.1).to(torch.bfloat16)
+    dy_b = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+    s_b = torch.empty((M,), dtype=torch.float32, device=dev)
+    ws_s = B.workspace(B.coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, d), dev)
+    for _ in range(3):
+        B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b, dh=dh,
+                                ws=ws_s, stream=stream)
+    barrier()
+    s0.record(stream)
+    for _ in range(KS):
+        B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b, dh=dh,
+                                ws=ws_s, stream=stream)
+    s1.record(stream)
+    barrier()
+    sb_ms = s0.elapsed_time(s1) / KS
+    sb_flops = 2 * M * d * (N1 // 2) + w.bwd_flops
+    extras["bwd_swiglu_dgrad"] = {
+        "ms": sb_ms, "tflops": sb_flops / (sb_ms * 1e-3) / 1e12, "calls": KS,
+        "gpu_launches": 3 * KS, "Dout": d,
+        "note": "coda_bwd_swiglu_dgrad: dout@W2^T with SwiGLU-bwd + partial s epilogue, "
+                "row sum, dy@W1^T with tile-local RMSNorm bwd"}
+    st, detail = B.coda_get_device_status()
+    if st != B.CODA_OK:
+        raise RuntimeError(f"device status after extras: {B.status_string(st)} {detail:#x}")
+
     # ---- end to end through the same C-ABI calls with pinned host buffers
     host_in = {k: v.pin_memory() for k, v in t.items() if k != "_rng"}
     host_dy = dy_cpu.pin_memory()
@@ -411,6 +461,7 @@ def run_coda(args):
                 "d2h_bytes_per_step": d2h, "steps": KE},
         "gpu_launches": 4 * K,
         "cpu_baseline": cpu,
+        "extras": extras,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

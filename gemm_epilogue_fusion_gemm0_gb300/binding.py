@@ -54,6 +54,11 @@ EXPORTS = {
     "coda_set_launch_events": (None, [_vp, ctypes.c_int]),
     "coda_bwd_dgrad_noalloc": (_st, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "coda_set_mma_mode": (_st, [ctypes.c_int]),
+    "coda_bwd_swiglu_dgrad_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "coda_bwd_swiglu_dgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp,
+                                    _vp, _vp, _vp, _sz, _vp]),
+    "coda_fwd_swiglu": (_st, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                              _sz, _vp]),
     "coda_get_mma_mode": (ctypes.c_int, []),
 }
 
@@ -150,6 +155,32 @@ def coda_fwd_unfused(x, W0, z, gamma, W1, eps, h=None, r=None, y=None, ws=None, 
                        W1, eps, h, r, y, ws, stream)
 
 
+def coda_fwd_swiglu(x, W0, z, gamma, W1, eps, h=None, r=None, a=None, y=None, want_y=False,
+                    ws=None, stream=None):
+    """Fused forward with the SwiGLU gated activation; W1 = [W_gate | W_up].
+    Returns (h, r, a) or (h, r, a, y) with want_y=True (pre-activation)."""
+    M, d = x.shape
+    N1 = W1.shape[1]
+    dev = x.device
+    bf = torch.bfloat16
+    h = torch.empty((M, d), dtype=bf, device=dev) if h is None else h
+    r = torch.empty((M,), dtype=torch.float32, device=dev) if r is None else r
+    a = torch.empty((M, N1 // 2), dtype=bf, device=dev) if a is None else a
+    if want_y and y is None:
+        y = torch.empty((M, N1), dtype=bf, device=dev)
+    if ws is None:
+        ws = workspace(coda_fwd_workspace_bytes(M, d, N1), dev)
+    st = _lib.coda_fwd_swiglu(
+        _dev(x, bf, (M, d), "x"), _dev(W0, bf, (d, d), "W0"), _dev(z, bf, (M, d), "z"),
+        _dev(gamma, bf, (d,), "gamma"), _dev(W1, bf, (d, N1), "W1"), float(eps), M, d, N1,
+        _dev(h, bf, (M, d), "h"), _dev(r, torch.float32, (M,), "r"),
+        None if y is None else _dev(y, bf, (M, N1), "y"), _dev(a, bf, (M, N1 // 2), "a"),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream),
+    )
+    _check(st, "coda_fwd_swiglu")
+    return (h, r, a, y) if y is not None else (h, r, a)
+
+
 def coda_bwd_dgrad(dy, W1, h, r, gamma, dh=None, ws=None, stream=None):
     """Fused RMSNorm-branch data gradient; returns dh."""
     M, N1 = dy.shape
@@ -167,6 +198,36 @@ def coda_bwd_dgrad(dy, W1, h, r, gamma, dh=None, ws=None, stream=None):
     )
     _check(st, "coda_bwd_dgrad")
     return dh
+
+
+def coda_bwd_swiglu_dgrad_workspace_bytes(M: int, d: int, N1: int, Dout: int) -> int:
+    return int(_lib.coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout))
+
+
+def coda_bwd_swiglu_dgrad(dout, W2, y, W1, h, r, gamma, dy=None, s=None, dh=None, ws=None,
+                          stream=None):
+    """SwiGLU backward (statistic formed upstream) + tile-local RMSNorm-branch
+    data gradient; returns (dy, s, dh)."""
+    M, Dout = dout.shape
+    half = W2.shape[0]
+    N1 = 2 * half
+    d = W1.shape[0]
+    dev = dout.device
+    bf = torch.bfloat16
+    dy = torch.empty((M, N1), dtype=bf, device=dev) if dy is None else dy
+    s = torch.empty((M,), dtype=torch.float32, device=dev) if s is None else s
+    dh = torch.empty((M, d), dtype=bf, device=dev) if dh is None else dh
+    if ws is None:
+        ws = workspace(coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout), dev)
+    st = _lib.coda_bwd_swiglu_dgrad(
+        _dev(dout, bf, (M, Dout), "dout"), _dev(W2, bf, (half, Dout), "W2"),
+        _dev(y, bf, (M, N1), "y"), _dev(W1, bf, (d, N1), "W1"), _dev(h, bf, (M, d), "h"),
+        _dev(r, torch.float32, (M,), "r"), _dev(gamma, bf, (d,), "gamma"), M, d, N1, Dout,
+        _dev(dy, bf, (M, N1), "dy"), _dev(s, torch.float32, (M,), "s"), _dev(dh, bf, (M, d), "dh"),
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream),
+    )
+    _check(st, "coda_bwd_swiglu_dgrad")
+    return dy, s, dh
 
 
 def coda_get_device_status(stream=None) -> tuple[int, int]:

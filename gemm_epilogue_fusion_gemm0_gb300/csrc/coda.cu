@@ -40,6 +40,16 @@ __global__ void rowreduce_rsqrt_kernel(const float* __restrict__ part, int nt, i
   r[m] = rsqrtf(s / static_cast<float>(d) + eps);
 }
 
+// Auxiliary reduction of the backward statistic: s[m] = sum_t spart[t][m]
+// (fixed summation order over tiles).
+__global__ void rowsum_kernel(const float* __restrict__ part, int nt, int M, float* __restrict__ s) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  float acc = 0.f;
+  for (int t = 0; t < nt; ++t) acc += __ldg(part + static_cast<size_t>(t) * M + m);
+  s[m] = acc;
+}
+
 // Standalone RMSNorm of the unfused reference sequence: reads h, writes
 // hn = bf16(r * h * gamma) and r.  One block of 256 threads per row.
 __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const __nv_bfloat16* __restrict__ h,
@@ -105,6 +115,12 @@ static auto* const kDgrad = &gemm_epilogue_kernel<EpiRmsNormBackward, false>;
 static auto* const kPairGemm0 = &gemm_pair_epilogue_kernel<EpiResidualGammaSumsq, true>;
 static auto* const kPairGemm1 = &gemm_pair_epilogue_kernel<EpiRowScale, true>;
 static auto* const kPairDgrad = &gemm_pair_epilogue_kernel<EpiRmsNormBackward, false>;
+static auto* const kGemm1Swiglu = &gemm_epilogue_kernel<EpiRowScaleSwiGLU, true>;
+static auto* const kPairGemm1Swiglu = &gemm_pair_epilogue_kernel<EpiRowScaleSwiGLU, true>;
+static auto* const kSwigluBwd = &gemm_epilogue_kernel<EpiSwiGLUBackward, false>;
+static auto* const kPairSwigluBwd = &gemm_pair_epilogue_kernel<EpiSwiGLUBackward, false>;
+static auto* const kDgradGivenS = &gemm_epilogue_kernel<EpiRmsNormBackwardGivenS, false>;
+static auto* const kPairDgradGivenS = &gemm_pair_epilogue_kernel<EpiRmsNormBackwardGivenS, false>;
 
 }  // namespace coda
 
@@ -178,6 +194,18 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
       ok &= cudaFuncSetAttribute(kPairGemm1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) == cudaSuccess;
       if (ok) {
         cudaLaunchConfig_t cfg = {};
@@ -269,19 +297,26 @@ size_t fwd_ws_bytes(int64_t M, int64_t d, bool fused) {
   return act + part;
 }
 
-coda_status_t fwd_impl(bool fused, const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
+enum class FwdKind { kFused, kUnfused, kFusedSwiGLU };
+
+coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
                        const coda_bf16* gamma, const coda_bf16* W1, float eps, int64_t M, int64_t d,
                        int64_t N1, coda_bf16* h_out, float* r_out, coda_bf16* y_out,
-                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                       coda_bf16* a_out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  const bool fused = kind != FwdKind::kUnfused;
+  const bool swiglu = kind == FwdKind::kFusedSwiGLU;
   coda_status_t st = check_common(M, d, N1);
   if (st != CODA_OK) return st;
+  if (swiglu && N1 % 16 != 0) return CODA_ERR_UNSUPPORTED_SHAPE;  // N1/2 rows of 16 bytes
   if (M == 0) return CODA_OK;
-  if (!x || !W0 || !z || !gamma || !W1 || !h_out || !r_out || !y_out)
+  if (!x || !W0 || !z || !gamma || !W1 || !h_out || !r_out || (swiglu ? !a_out : !y_out))
     return CODA_ERR_INVALID_ARG;
   if (!std::isfinite(eps) || eps < 0.f) return CODA_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, W0, z, gamma, W1, h_out, r_out, y_out};
+  const void* ptrs[] = {x, W0, z, gamma, W1, h_out, r_out, swiglu ? a_out : y_out};
   for (const void* p : ptrs)
     if (!aligned16(p)) return CODA_ERR_MISALIGNED;
+  if (swiglu && !aligned16(y_out)) return CODA_ERR_MISALIGNED;  // optional, may be null
   if (workspace == nullptr || workspace_bytes < fwd_ws_bytes(M, d, fused))
     return CODA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
@@ -305,7 +340,8 @@ coda_status_t fwd_impl(bool fused, const coda_bf16* x, const coda_bf16* W0, cons
 
   const int mt = static_cast<int>(cdiv(M, kBM));
   const int nt0 = static_cast<int>(cdiv(d, kBN));
-  const int nt1 = static_cast<int>(cdiv(N1, kBN));
+  const int nt1 = swiglu ? EpiRowScaleSwiGLU::num_col_tiles(static_cast<int>(N1))
+                        : static_cast<int>(cdiv(N1, kBN));
   const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
   const uint64_t tmo = g_timeout_ns.load();
 
@@ -338,13 +374,24 @@ coda_status_t fwd_impl(bool fused, const coda_bf16* x, const coda_bf16* W0, cons
     return CODA_ERR_LAUNCH;
   }
   after_launch(1, stream);
-  EpiRowScale::Params p1;
-  p1.r = fused ? r_out : nullptr;
-  p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
-  e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
-                    stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
-           : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false, mA1, mB1,
-                    Mi, N1i, di, kGroupM, p1, tmo);
+  if (swiglu) {
+    EpiRowScaleSwiGLU::Params ps;
+    ps.r = r_out;
+    ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
+    ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
+    e = pair ? launch(kPairGemm1Swiglu, 2 * std::min(max_pairs, mtp * nt1), kThreads,
+                      kPairSmemBytes, stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, tmo)
+             : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false,
+                      mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
+  } else {
+    EpiRowScale::Params p1;
+    p1.r = fused ? r_out : nullptr;
+    p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
+    e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
+                      stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
+             : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false, mA1,
+                      mB1, Mi, N1i, di, kGroupM, p1, tmo);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -378,8 +425,17 @@ coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16*
                        const coda_bf16* gamma, const coda_bf16* W1, float eps, int64_t M, int64_t d,
                        int64_t N1, coda_bf16* h_out, float* r_out, coda_bf16* y_out,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  return fwd_impl(true, x, W0, z, gamma, W1, eps, M, d, N1, h_out, r_out, y_out, workspace,
-                  workspace_bytes, stream);
+  return fwd_impl(FwdKind::kFused, x, W0, z, gamma, W1, eps, M, d, N1, h_out, r_out, y_out,
+                  nullptr, workspace, workspace_bytes, stream);
+}
+
+coda_status_t coda_fwd_swiglu(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
+                              const coda_bf16* gamma, const coda_bf16* W1, float eps, int64_t M,
+                              int64_t d, int64_t N1, coda_bf16* h_out, float* r_out,
+                              coda_bf16* y_out, coda_bf16* a_out, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  return fwd_impl(FwdKind::kFusedSwiGLU, x, W0, z, gamma, W1, eps, M, d, N1, h_out, r_out, y_out,
+                  a_out, workspace, workspace_bytes, stream);
 }
 
 coda_status_t coda_fwd_unfused(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
@@ -387,8 +443,8 @@ coda_status_t coda_fwd_unfused(const coda_bf16* x, const coda_bf16* W0, const co
                                int64_t d, int64_t N1, coda_bf16* h_out, float* r_out,
                                coda_bf16* y_out, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream) {
-  return fwd_impl(false, x, W0, z, gamma, W1, eps, M, d, N1, h_out, r_out, y_out, workspace,
-                  workspace_bytes, stream);
+  return fwd_impl(FwdKind::kUnfused, x, W0, z, gamma, W1, eps, M, d, N1, h_out, r_out, y_out,
+                  nullptr, workspace, workspace_bytes, stream);
 }
 
 coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const coda_bf16* h,
@@ -445,6 +501,96 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
     return CODA_ERR_LAUNCH;
   }
   after_launch(0, stream);
+  return CODA_OK;
+}
+
+size_t coda_bwd_swiglu_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1, int64_t Dout) {
+  if (check_common(M, d, N1) != CODA_OK || Dout <= 0 || M == 0) return 0;
+  return align256(static_cast<size_t>(cdiv(N1 / 2, kBN)) * M * 4);
+}
+
+coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, const coda_bf16* y,
+                                    const coda_bf16* W1, const coda_bf16* h, const float* r,
+                                    const coda_bf16* gamma, int64_t M, int64_t d, int64_t N1,
+                                    int64_t Dout, coda_bf16* dy_out, float* s_out,
+                                    coda_bf16* dh_out, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+  coda_status_t st = check_common(M, d, N1);
+  if (st != CODA_OK) return st;
+  if (Dout <= 0) return CODA_ERR_INVALID_ARG;
+  if (N1 % 16 != 0 || Dout % 8 != 0 || Dout > (int64_t(1) << 31) - 256)
+    return CODA_ERR_UNSUPPORTED_SHAPE;
+  if (M == 0) return CODA_OK;
+  if (!dout || !W2 || !y || !W1 || !h || !r || !gamma || !dy_out || !s_out || !dh_out)
+    return CODA_ERR_INVALID_ARG;
+  const void* ptrs[] = {dout, W2, y, W1, h, r, gamma, dy_out, s_out, dh_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CODA_ERR_MISALIGNED;
+  if (workspace == nullptr ||
+      workspace_bytes < coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout))
+    return CODA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
+  int sms = 0, max_pairs = 0;
+  st = device_setup(&sms, &max_pairs);
+  if (st != CODA_OK) return st;
+  const bool pair = g_mma_mode.load() == 1;
+  const int64_t half = N1 / 2;
+  const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
+  const int halfi = static_cast<int>(half), Douti = static_cast<int>(Dout);
+  const uint64_t tmo = g_timeout_ns.load();
+
+  CUtensorMap mA0, mB0, mA1, mB1;
+  const uint32_t bbox = pair ? 128 : kBN;
+  bool ok = tmap_2d(&mA0, dout, Dout, M, kBK, kBM);   // dout [M, Dout]       K-major (K = Dout)
+  ok &= tmap_2d(&mB0, W2, Dout, half, kBK, bbox);     // W2 [half(N), Dout(K)] K-major
+  ok &= tmap_2d(&mA1, dy_out, N1, M, kBK, kBM);       // dy [M, N1]           K-major (K = N1)
+  ok &= tmap_2d(&mB1, W1, N1, d, kBK, bbox);          // W1 [d(N), N1(K)]      K-major
+  if (!ok) return CODA_ERR_LAUNCH;
+
+  const int nts = static_cast<int>(cdiv(half, kBN));
+  const int ntd = static_cast<int>(cdiv(d, kBN));
+  const int mt = static_cast<int>(cdiv(M, kBM));
+  const int mtp = static_cast<int>(cdiv(M, kPairBM));
+
+  // 1. down-projection data gradient with the SwiGLU backward + partial s
+  EpiSwiGLUBackward::Params p0;
+  p0.y = reinterpret_cast<const __nv_bfloat16*>(y);
+  p0.dy_out = reinterpret_cast<__nv_bfloat16*>(dy_out);
+  p0.spart = reinterpret_cast<float*>(workspace);
+  cudaError_t e =
+      pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads, kPairSmemBytes,
+                    stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM, p0, tmo)
+           : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, kSmemBytes, stream, false, mA0,
+                    mB0, Mi, halfi, Douti, kGroupM, p0, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(0, stream);
+  // 2. light auxiliary reduction of the statistic
+  e = launch(rowsum_kernel, static_cast<int>(cdiv(M, 256)), 256, 0, stream, false,
+             static_cast<const float*>(p0.spart), nts, Mi, s_out);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(1, stream);
+  // 3. RMSNorm-branch data gradient, tile-local with s given
+  EpiRmsNormBackwardGivenS::Params p1;
+  p1.h = reinterpret_cast<const __nv_bfloat16*>(h);
+  p1.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  p1.r = r;
+  p1.s = s_out;
+  p1.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
+  e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads, kPairSmemBytes,
+                    stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, tmo)
+           : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kSmemBytes, stream, false,
+                    mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(2, stream);
   return CODA_OK;
 }
 

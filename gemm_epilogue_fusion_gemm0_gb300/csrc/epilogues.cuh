@@ -20,6 +20,14 @@ struct Chunk8 {
   uint32_t w[4];
 };
 
+// Column mapping of a policy: how many 256-column accumulator tiles cover the
+// output, and where the producer fetches the j-th 64-column chunk (j = 0..3)
+// of an MN-major B tile.  The default is the plain contiguous tiling.
+struct EpiDefaultCols {
+  static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N + kBN - 1) / kBN; }
+  static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
+};
+
 __device__ __forceinline__ Chunk8 ldg8(const __nv_bfloat16* p) {
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
   return Chunk8{{v.x, v.y, v.z, v.w}};
@@ -39,7 +47,7 @@ __device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
 // With hg_out == nullptr and part == nullptr it is the plain residual-add
 // epilogue of the unfused reference sequence.
 // ---------------------------------------------------------------------------
-struct EpiResidualGammaSumsq {
+struct EpiResidualGammaSumsq : EpiDefaultCols {
   struct Params {
     const __nv_bfloat16* z;
     const __nv_bfloat16* gamma;
@@ -92,7 +100,7 @@ struct EpiResidualGammaSumsq {
 // second GEMM.  With r == nullptr it is the plain store of the unfused
 // reference sequence.
 // ---------------------------------------------------------------------------
-struct EpiRowScale {
+struct EpiRowScale : EpiDefaultCols {
   struct Params {
     const float* r;  // [M], may be null (scale 1)
     __nv_bfloat16* y_out;
@@ -140,7 +148,7 @@ struct EpiRowScale {
 // row-major order with at most gridDim.x column tiles per row; then every wait
 // depends only on tiles with smaller index and cannot deadlock.
 // ---------------------------------------------------------------------------
-struct EpiRmsNormBackward {
+struct EpiRmsNormBackward : EpiDefaultCols {
   struct Params {
     const __nv_bfloat16* h;
     const __nv_bfloat16* gamma;
@@ -203,6 +211,190 @@ struct EpiRmsNormBackward {
     }
     const float coef = rr * rr * rr * q / static_cast<float>(c.N);
 
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            const Chunk8 hh = ldg8(p.h + rowoff + n);
+            const Chunk8 gg = ldg8(p.gamma + n);
+            uint32_t dw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
+                               coef * bf16lo(hh.w[e]);
+              const float d1 = rr * bf16hi(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
+                               coef * bf16hi(hh.w[e]);
+              dw[e] = pack_bf16x2(d0, d1);
+            }
+            stg8(p.dh_out + rowoff + n, dw);
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// GEMM1 epilogue with the gated activation (CODA blog, SwiGLU gating among the
+// section "五类 Epilogue 原语", and the pairing idea of section
+// "成对激活的寄存器级融合").  W1 = [W_gate | W_up] ([d, N1], the usual layout);
+// output tile nb covers gated columns [128 nb, 128 nb + 128): its B tile holds
+// the 128 gate columns in accumulator columns 0..127 and the matching 128 up
+// columns in 128..255.  Each thread owns a whole accumulator row in TMEM, so
+// the pair (gate_j, up_j) is column j and j + 128 of the same thread; no
+// weight interleaving and no shuffles are needed.
+//   g = r[m] * acc[:, j], u = r[m] * acc[:, j + 128]
+//   a[m, 128 nb + j] = silu(g) * u            -> a_out [M, N1/2] bf16
+//   optionally y_out = [g | u] at their [gate | up] positions ([M, N1] bf16)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float silu_f(float t) { return t / (1.0f + __expf(-t)); }
+
+struct EpiRowScaleSwiGLU {
+  struct Params {
+    const float* r;         // [M]
+    __nv_bfloat16* y_out;   // [M, N1] pre-activation, may be null
+    __nv_bfloat16* a_out;   // [M, N1 / 2]
+  };
+
+  static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N / 2 + 127) / 128; }
+  static __device__ __forceinline__ int b_col(int nb, int j, int N) {
+    return (j < 2 ? 0 : N / 2) + nb * 128 + 64 * (j & 1);
+  }
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const int half = c.N / 2;
+    const float rr = row_ok ? __ldg(p.r + m) : 0.f;
+    const size_t a_row = static_cast<size_t>(row_ok ? m : 0) * half;
+    const size_t y_row = static_cast<size_t>(row_ok ? m : 0) * c.N;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t g[32], u[32];
+      tmem_ld32(c.taddr + ch * 32, g);
+      tmem_ld32(c.taddr + 128 + ch * 32, u);
+      tmem_ld_wait(g);
+      tmem_ld_wait(u);
+      const int o0 = c.nb * 128 + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int o = o0 + q * 8;
+          if (o < half) {
+            uint32_t aw[4], gw[4], uw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float g0 = rr * __uint_as_float(g[q * 8 + 2 * e]);
+              const float g1 = rr * __uint_as_float(g[q * 8 + 2 * e + 1]);
+              const float u0 = rr * __uint_as_float(u[q * 8 + 2 * e]);
+              const float u1 = rr * __uint_as_float(u[q * 8 + 2 * e + 1]);
+              aw[e] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+              gw[e] = pack_bf16x2(g0, g1);
+              uw[e] = pack_bf16x2(u0, u1);
+            }
+            stg8(p.a_out + a_row + o, aw);
+            if (p.y_out != nullptr) {
+              stg8(p.y_out + y_row + o, gw);
+              stg8(p.y_out + y_row + half + o, uw);
+            }
+          }
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// SwiGLU backward epilogue with the row statistic formed upstream (CODA blog,
+// section "反向传播的 GEMM-Epilogue 结构": s = sum_cols(grad_y * y) can be
+// accumulated in the epilogue of the GEMM where grad_y and y meet).
+// The GEMM is the down-projection data gradient: acc = da = dout @ W2^T, one
+// 256-column tile of the N1/2 gated columns.  With the saved pre-activation
+// y = [g | u] (bf16, [M, N1]) loaded as a rank-2 tile:
+//   dg = da * u * silu'(g),  du = da * silu(g)      -> dy_out = [dg | du] bf16
+//   spart[nb][m] = sum over the tile of dg * g + du * u   (fp32)
+// ---------------------------------------------------------------------------
+struct EpiSwiGLUBackward : EpiDefaultCols {
+  struct Params {
+    const __nv_bfloat16* y;  // [M, 2 * half] saved pre-activation [g | u]
+    __nv_bfloat16* dy_out;   // [M, 2 * half]
+    float* spart;            // [nt][M]
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const int half = c.N;  // the GEMM's output width is the gated width
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * (2 * static_cast<size_t>(half));
+    float ss = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kBN / 32; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld_wait(v);
+      const int j0 = c.nb * kBN + ch * 32;
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = j0 + q * 8;
+          if (j < half) {
+            const Chunk8 gg = ldg8(p.y + rowoff + j);
+            const Chunk8 uu = ldg8(p.y + rowoff + half + j);
+            uint32_t dgw[4], duw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float dgv[2], duv[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const float da = __uint_as_float(v[q * 8 + 2 * e + k]);
+                const float g = k ? bf16hi(gg.w[e]) : bf16lo(gg.w[e]);
+                const float u = k ? bf16hi(uu.w[e]) : bf16lo(uu.w[e]);
+                const float sig = 1.0f / (1.0f + __expf(-g));
+                dgv[k] = da * u * sig * (1.0f + g * (1.0f - sig));
+                duv[k] = da * g * sig;
+                ss = fmaf(dgv[k], g, ss);
+                ss = fmaf(duv[k], u, ss);
+              }
+              dgw[e] = pack_bf16x2(dgv[0], dgv[1]);
+              duw[e] = pack_bf16x2(duv[0], duv[1]);
+            }
+            stg8(p.dy_out + rowoff + j, dgw);
+            stg8(p.dy_out + rowoff + half + j, duw);
+          }
+        }
+      }
+    }
+    if (row_ok) p.spart[static_cast<size_t>(c.nb) * c.M + m] = ss;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Data-gradient epilogue with the statistic given (formed upstream):
+//   grad_h = r * gamma * acc - (r^2 * s / d) * h,  acc = grad_h2 = grad_y @ W1^T.
+// Purely tile-local: no cross-tile exchange, any tile order.
+// ---------------------------------------------------------------------------
+struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
+  struct Params {
+    const __nv_bfloat16* h;
+    const __nv_bfloat16* gamma;
+    const float* r;
+    const float* s;
+    __nv_bfloat16* dh_out;
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const float rr = row_ok ? __ldg(p.r + m) : 0.f;
+    const float coef = row_ok ? rr * rr * __ldg(p.s + m) / static_cast<float>(c.N) : 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < kBN / 32; ++ch) {
       uint32_t v[32];

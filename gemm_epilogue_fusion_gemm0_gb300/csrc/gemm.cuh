@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int mt = (M + kBM - 1) / kBM;
-  const int nt = (N + kBN - 1) / kBN;
+  const int nt = Epi::num_col_tiles(N);
   const int nk = (K + kBK - 1) / kBK;
   const int num_tiles = mt * nt;
   const TileMap tmap{mt, nt, group_m};
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kBMNMajor) {
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j)
-              tma_load_2d(b_dst + j * kBChunkBytes, &tmB, full, nb * kBN + 64 * j, kb * kBK);
+              tma_load_2d(b_dst + j * kBChunkBytes, &tmB, full, Epi::b_col(nb, j, N), kb * kBK);
           } else {
             tma_load_2d(b_dst, &tmB, full, kb * kBK, nb * kBN);
           }

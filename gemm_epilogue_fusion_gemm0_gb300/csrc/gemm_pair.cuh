@@ -62,7 +62,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
   const int mt = (M + kPairBM - 1) / kPairBM;
-  const int nt = (N + kBN - 1) / kBN;
+  const int nt = Epi::num_col_tiles(N);
   const int nk = (K + kBK - 1) / kBK;
   const int num_tiles = mt * nt;
   const TileMap tmap{mt, nt, group_m};
@@ -103,7 +103,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int mb, nb;
         tmap.coords(t, mb, nb);
         const int arow = mb * kPairBM + static_cast<int>(rank) * 128;
-        const int bcol = nb * kBN + static_cast<int>(rank) * 128;
+        const int bcol = nb * kBN + static_cast<int>(rank) * 128;  // K-major B rows
         for (int kb = 0; kb < nk; ++kb) {
           if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
@@ -116,8 +116,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t b_dst = sB + s * kPairBStageBytes;
           tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, arow);
           if constexpr (kBMNMajor) {
-            tma_load_2d_pair(b_dst, &tmB, full_leader, bcol, kb * kBK);
-            tma_load_2d_pair(b_dst + kBChunkBytes, &tmB, full_leader, bcol + 64, kb * kBK);
+            const int j0 = 2 * static_cast<int>(rank);  // this CTA's two 64-column chunks
+            tma_load_2d_pair(b_dst, &tmB, full_leader, Epi::b_col(nb, j0, N), kb * kBK);
+            tma_load_2d_pair(b_dst + kBChunkBytes, &tmB, full_leader, Epi::b_col(nb, j0 + 1, N),
+                             kb * kBK);
           } else {
             tma_load_2d_pair(b_dst, &tmB, full_leader, kb * kBK, bcol);
           }

@@ -83,6 +83,16 @@ def make_grad_output(rng_or_seed, M: int, N1: int) -> torch.Tensor:
     return to_bf16(_normal(rng, (M, N1), 1e-2))
 
 
+def make_down_proj_backward(rng, M: int, N1: int, Dout: int) -> dict:
+    """bf16 CPU tensors for the backward through the gated activation and the
+    down projection: W2 [N1/2, Dout] ~ N(0, 2/N1) and dout [M, Dout] ~ N(0, 1e-2),
+    drawn in that order from `rng` (continue the forward generator)."""
+    half = N1 // 2
+    W2 = to_bf16(_normal(rng, (half, Dout), 1.0 / half))
+    dout = to_bf16(_normal(rng, (M, Dout), 1e-2))
+    return {"W2": W2, "dout": dout}
+
+
 def sample_rows(M: int, n: int, seed: int = 1) -> np.ndarray:
     """Sorted seeded sample of n distinct row indices in [0, M), always
     containing the first row, both sides of the first 128-row tile boundary

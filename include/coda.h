@@ -100,6 +100,28 @@ CODA_API coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const c
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Forward of the chain with the SwiGLU gated activation fused into GEMM1's
+ * epilogue ("CODA：将 Transformer 块重写为 GEMM-Epilogue 程序以消除显存瓶颈",
+ * blog.hotdry.top: SwiGLU gating is one of the section "五类 Epilogue 原语",
+ * and section "成对激活的寄存器级融合" fuses the gate/up pair in the epilogue):
+ *   steps 1 and 2 as coda_fwd, then GEMM1 with W1 = [W_gate | W_up] ([d, N1],
+ *   the usual concatenated layout; no interleaving needed) and epilogue
+ *   g = r * (hg @ W_gate),  u = r * (hg @ W_up),  a = silu(g) * u.
+ * One accumulator tile holds 128 gate columns and the matching 128 up columns,
+ * so each thread, which owns a whole tile row in tensor memory, has both
+ * members of every pair; the gated output is the only [M, N1/2] tensor written.
+ *   a_out  [M, N1/2] bf16 out   (required)
+ *   y_out  [M, N1]   bf16 out   pre-activation [g | u]; may be NULL
+ * Other arguments and the workspace as coda_fwd.  N1 must be a multiple of 16.
+ */
+CODA_API coda_status_t coda_fwd_swiglu(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
+                                       const coda_bf16* gamma, const coda_bf16* W1, float eps,
+                                       int64_t M, int64_t d, int64_t N1,
+                                       coda_bf16* h_out, float* r_out, coda_bf16* y_out,
+                                       coda_bf16* a_out, void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
+
+/*
  * Data gradient through the RMSNorm branch, as one GEMM-epilogue program:
  *   grad_h2 = grad_y @ W1^T  accumulated in tensor memory, then in the epilogue
  *   q[m]    = sum_j grad_h2[m,j] * gamma[j] * h[m,j]  (so s = r * q equals
@@ -123,6 +145,35 @@ CODA_API coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, 
                              int64_t M, int64_t d, int64_t N1,
                              coda_bf16* dh_out, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream);
+
+/*
+ * Backward of a = silu(g) * u, out = a @ W2, through to grad_h, with the
+ * RMSNorm row statistic formed where grad_y and y meet ("CODA：将 Transformer
+ * 块重写为 GEMM-Epilogue 程序以消除显存瓶颈", blog.hotdry.top, section
+ * "反向传播的 GEMM-Epilogue 结构": s = sum_cols(grad_y * y) accumulated in the
+ * epilogue of the GEMM that produces grad_y).  Three launches:
+ *   1. da = dout @ W2^T, epilogue: with the saved pre-activation y = [g | u],
+ *      dg = da * u * silu'(g), du = da * silu(g) -> dy_out = [dg | du], and
+ *      per-tile partial sums of dy * y;
+ *   2. s[m] = sum of the partials (light auxiliary reduction) -> s_out;
+ *   3. grad_h2 = dy @ W1^T, epilogue: grad_h = r * gamma * grad_h2
+ *      - (r^2 * s / d) * h, purely tile-local (no cross-tile exchange).
+ *   dout   [M, Dout]  bf16 in     W2    [N1/2, Dout] bf16 in (down projection, [in, out])
+ *   y      [M, N1]    bf16 in     (pre-activation [g | u] saved by coda_fwd_swiglu)
+ *   W1     [d, N1]    bf16 in     h [M, d] bf16, r [M] fp32, gamma [d] bf16 in
+ *   dy_out [M, N1]    bf16 out    s_out [M] fp32 out     dh_out [M, d] bf16 out
+ *   workspace: at least coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout).
+ * N1 must be a multiple of 16 and Dout of 8.  Conventions as coda_bwd_dgrad.
+ */
+CODA_API size_t coda_bwd_swiglu_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1,
+                                                      int64_t Dout);
+CODA_API coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2,
+                                             const coda_bf16* y, const coda_bf16* W1,
+                                             const coda_bf16* h, const float* r,
+                                             const coda_bf16* gamma, int64_t M, int64_t d,
+                                             int64_t N1, int64_t Dout, coda_bf16* dy_out,
+                                             float* s_out, coda_bf16* dh_out, void* workspace,
+                                             size_t workspace_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, then reports and clears the library's device-side
  * status word: CODA_OK, or CODA_ERR_DEVICE_TIMEOUT if a bounded wait in any

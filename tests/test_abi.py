@@ -93,6 +93,19 @@ def test_argument_validation_before_any_launch(lib):
     assert _bwd(lib, wsb=8) == E["CODA_ERR_WORKSPACE_TOO_SMALL"]
 
 
+def test_swiglu_argument_validation(lib):
+    E = {v: k for k, v in lib.STATUS_NAMES.items()}
+    raw = lib.raw()
+
+    def call(N1=512, y=0, a=FAKE):
+        return raw.coda_fwd_swiglu(FAKE, FAKE, FAKE, FAKE, FAKE, 1e-5, 128, 256, N1, FAKE, FAKE,
+                                   y, a, FAKE, 1 << 30, None)
+
+    assert call(N1=520) == E["CODA_ERR_UNSUPPORTED_SHAPE"]  # N1/2 rows must be 16-byte multiples
+    assert call(a=0) == E["CODA_ERR_INVALID_ARG"]
+    assert call(y=FAKE + 2) == E["CODA_ERR_MISALIGNED"]
+
+
 def test_no_device_is_reported_without_gpu(lib):
     import torch
 

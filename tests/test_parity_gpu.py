@@ -209,3 +209,72 @@ def test_llama_shapes_sampled_rows(B, mode, name):
     # llama7b also runs the data-gradient workload: saved h, r from this
     # forward and dy drawn after the forward inputs from the same generator.
     run_case(B, w.M, w.d, w.N1, w.eps, seed=0, rows=rows, bwd=(name == "llama7b"))
+
+
+# ----------------------------------------------------------------------------- SwiGLU forward
+def run_swiglu(B, M, d, N1, eps, seed=0, rows=None):
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=seed)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    h, r, a, y = B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, want_y=True)
+    _, _, a2 = B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps)  # no y
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    assert torch.equal(a, a2)
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    idx = torch.as_tensor(sel)
+    f, a_ref = oracle.forward_swiglu(f64(t["x"][idx]), f64(t["W0"]), f64(t["z"][idx]),
+                                     f64(t["gamma"]), f64(t["W1"]), eps)
+    return {"a": check("a", f64(a.cpu()[idx]), a_ref, TOL_HY),
+            "y": check("y", f64(y.cpu()[idx]), f.y, TOL_HY),
+            "h": check("h", f64(h.cpu()[idx]), f.h, TOL_HY),
+            "r": check_r(f64(r.cpu()[idx]), f.r)}
+
+
+@pytest.mark.parametrize("M,d,N1", [
+    (128, 256, 512),    # tiny
+    (300, 328, 784),    # ragged: N1/2 = 392 is not a multiple of the 128-column gated tile
+    (640, 512, 1536),   # several tiles
+])
+def test_swiglu_forward_small(B, mode, M, d, N1):
+    run_swiglu(B, M, d, N1, 1e-5)
+
+
+def test_swiglu_forward_llama7b_sampled_rows(B, mode):
+    w = synth.WORKLOADS["llama7b"]
+    run_swiglu(B, w.M, w.d, w.N1, w.eps, rows=synth.sample_rows(w.M, 256, seed=2))
+
+
+# ----------------------------------------------------------------------------- SwiGLU backward, s upstream
+def run_swiglu_bwd(B, M, d, N1, Dout, eps, seed=0, rows=None):
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=seed)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    h, r, _, y = B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, want_y=True)
+    bw = synth.make_down_proj_backward(t["_rng"], M, N1, Dout)
+    dy, s, dh = B.coda_bwd_swiglu_dgrad(bw["dout"].to(dev), bw["W2"].to(dev), y, g["W1"], h, r,
+                                        g["gamma"])
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    idx = torch.as_tensor(sel)
+    yG, hG, rG = f64(y.cpu()[idx]), f64(h.cpu()[idx]), f64(r.cpu()[idx])
+    dy_ref, s_ref = oracle.backward_swiglu(f64(bw["dout"][idx]), f64(bw["W2"]), yG)
+    dh_ref = oracle.backward_dgrad(dy_ref, f64(t["W1"]), hG, rG, f64(t["gamma"])).dh
+    return {"dy": check("dy", f64(dy.cpu()[idx]), dy_ref, TOL_HY),
+            "s": check("s", f64(s.cpu()[idx])[:, None], s_ref[:, None], TOL_HY),
+            "dh": check("dh", f64(dh.cpu()[idx]), dh_ref, TOL_DH)}
+
+
+@pytest.mark.parametrize("M,d,N1,Dout", [
+    (128, 256, 512, 256),     # tiny
+    (300, 328, 784, 264),     # ragged in every dimension
+    (640, 512, 1536, 512),    # several tiles
+])
+def test_swiglu_backward_small(B, mode, M, d, N1, Dout):
+    run_swiglu_bwd(B, M, d, N1, Dout, 1e-5)
+
+
+def test_swiglu_backward_llama7b_sampled_rows(B, mode):
+    w = synth.WORKLOADS["llama7b"]
+    run_swiglu_bwd(B, w.M, w.d, w.N1, w.d, w.eps, rows=synth.sample_rows(w.M, 256, seed=3))
