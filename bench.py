@@ -61,6 +61,20 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (identity on one rank)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: int, flops_per_unit: float, max_ms: float) -> float:
+    """Whole-job TFLOP/s: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank * flops_per_unit / (max_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -321,12 +335,9 @@ def run_coda(args):
     fwd_ms = statistics.fmean(evs[i][0].elapsed_time(evs[i][3]) for i in range(K))
     bwd_ms = per["dgrad_rmsnorm_bwd"]
 
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     flops_step = w.fwd_flops + w.bwd_flops
-    value = world * K * flops_step / (ms * 1e-3) / 1e12
+    value = job_throughput(world, K, flops_step, ms)
 
     # ---- widened path (not part of `value`): forward with the SwiGLU epilogue
     a_sw = torch.empty((M, N1 // 2), dtype=torch.bfloat16, device=dev)
@@ -360,18 +371,30 @@ def run_coda(args):
     for _ in range(3):
         B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b, dh=dh,
                                 ws=ws_s, stream=stream)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KS)]
+    for ev in sev:
+        for e in ev:
+            e.record(stream)
     barrier()
     s0.record(stream)
-    for _ in range(KS):
+    for i in range(KS):
+        sev[i][0].record(stream)
+        B.coda_set_launch_events(sev[i][1:4])
         B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b, dh=dh,
                                 ws=ws_s, stream=stream)
     s1.record(stream)
     barrier()
+    B.coda_set_launch_events(None)
     sb_ms = s0.elapsed_time(s1) / KS
+    sb_k = [statistics.fmean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(KS))
+            for j in range(3)]
     sb_flops = 2 * M * d * (N1 // 2) + w.bwd_flops
     extras["bwd_swiglu_dgrad"] = {
         "ms": sb_ms, "tflops": sb_flops / (sb_ms * 1e-3) / 1e12, "calls": KS,
         "gpu_launches": 3 * KS, "Dout": d,
+        "kernels_ms": {"swiglu_bwd_gemm": sb_k[0], "rowsum_s": sb_k[1], "dgrad_given_s": sb_k[2]},
+        "kernels_tflops": {"swiglu_bwd_gemm": 2 * M * d * (N1 // 2) / (sb_k[0] * 1e-3) / 1e12,
+                           "dgrad_given_s": w.bwd_flops / (sb_k[2] * 1e-3) / 1e12},
         "note": "coda_bwd_swiglu_dgrad: dout@W2^T with SwiGLU-bwd + partial s epilogue, "
                 "row sum, dy@W1^T with tile-local RMSNorm bwd"}
     st, detail = B.coda_get_device_status()
@@ -409,11 +432,8 @@ def run_coda(args):
     e1.record(stream)
     barrier()
     ems = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ems], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ems = float(tt.item())
-    e2e_value = world * KE * flops_step / (ems * 1e-3) / 1e12
+    ems = max_over_ranks(ems, world, dev)
+    e2e_value = job_throughput(world, KE, flops_step, ems)
 
     if rank != 0:
         if world > 1:
