@@ -293,7 +293,7 @@ struct FwdWorkspace {
 
 size_t fwd_ws_bytes(int64_t M, int64_t d, bool fused) {
   const size_t act = align256(static_cast<size_t>(M) * d * 2);
-  const size_t part = fused ? align256(static_cast<size_t>(cdiv(d, kBN)) * M * 4) : 0;
+  const size_t part = fused ? align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4) : 0;
   return act + part;
 }
 
@@ -364,7 +364,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   after_launch(0, stream);
   if (fused) {
     e = launch(rowreduce_rsqrt_kernel, static_cast<int>(cdiv(M, 256)), 256, 0, stream, false,
-               static_cast<const float*>(ws.part), nt0, Mi, di, eps, r_out);
+               static_cast<const float*>(ws.part), 2 * nt0, Mi, di, eps, r_out);
   } else {
     e = launch(rmsnorm_rows_kernel, Mi, 256, 0, stream, false,
                static_cast<const __nv_bfloat16*>(p0.h_out), p0.gamma, eps, Mi, di, ws.act, r_out);
@@ -418,7 +418,8 @@ size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
   // one flag per (128-row slab, column tile); CTA-pair tiles cover 2 * ceil(M/256) slabs
   const int64_t slabs = 2 * cdiv(M, kPairBM), nt = cdiv(d, kBN);
-  return align256(static_cast<size_t>(nt) * M * 4) + align256(static_cast<size_t>(slabs) * nt * 8);
+  return align256(static_cast<size_t>(2 * nt) * M * 4) +
+         align256(static_cast<size_t>(slabs) * nt * 8);
 }
 
 coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
@@ -485,7 +486,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
   p.qpart = reinterpret_cast<float*>(workspace);
   p.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
-                                        align256(static_cast<size_t>(nt) * M * 4));
+                                        align256(static_cast<size_t>(2 * nt) * M * 4));
   uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
   if (tok == 0) tok = 1;
   p.token = tok;
@@ -506,7 +507,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
 
 size_t coda_bwd_swiglu_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1, int64_t Dout) {
   if (check_common(M, d, N1) != CODA_OK || Dout <= 0 || M == 0) return 0;
-  return align256(static_cast<size_t>(cdiv(N1 / 2, kBN)) * M * 4);
+  return align256(static_cast<size_t>(2 * cdiv(N1 / 2, kBN)) * M * 4);
 }
 
 coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, const coda_bf16* y,
@@ -569,7 +570,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   after_launch(0, stream);
   // 2. light auxiliary reduction of the statistic
   e = launch(rowsum_kernel, static_cast<int>(cdiv(M, 256)), 256, 0, stream, false,
-             static_cast<const float*>(p0.spart), nts, Mi, s_out);
+             static_cast<const float*>(p0.spart), 2 * nts, Mi, s_out);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -678,12 +679,12 @@ coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t stream) {
 // workspace live instead in the fixed array below, which every GPU that
 // loads this library holds until the process exits.
 // ---------------------------------------------------------------------------
-constexpr size_t kNoAllocPartials = CODA_NOALLOC_MAX_PARTIALS;  // fp32 per-(row, column tile)
+constexpr size_t kNoAllocPartials = 2 * CODA_NOALLOC_MAX_PARTIALS;  // fp32, two per (row, column tile)
 constexpr size_t kNoAllocFlags = CODA_NOALLOC_MAX_TILES;        // u64 per output tile
 constexpr size_t kNoAllocFlagOffset = kNoAllocPartials * sizeof(float);
 constexpr size_t kNoAllocBytes = kNoAllocFlagOffset + kNoAllocFlags * sizeof(uint64_t);
 
-// 2 MiB of partials + 128 KiB of flags.  The flags need no clearing: each
+// 4 MiB of partials + 128 KiB of flags.  The flags need no clearing: each
 // call publishes a fresh 64-bit token, so values left by an earlier call never
 // match (and the array starts zeroed, a value no call ever uses).
 static __device__ __align__(256) unsigned char g_noalloc_dgrad_scratch[kNoAllocBytes];
@@ -729,7 +730,7 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
   for (const void* p : ptrs)
     if (!aligned16(p)) return CODA_ERR_MISALIGNED;
   const int64_t mt64 = cdiv(M, kBM), nt64 = cdiv(d, kBN);
-  if (static_cast<uint64_t>(nt64) * static_cast<uint64_t>(M) > kNoAllocPartials ||
+  if (2 * static_cast<uint64_t>(nt64) * static_cast<uint64_t>(M) > kNoAllocPartials ||
       static_cast<uint64_t>(mt64) * static_cast<uint64_t>(nt64) > kNoAllocFlags)
     return CODA_ERR_UNSUPPORTED_SHAPE;  // larger than the static scratch
   int sms = 0;

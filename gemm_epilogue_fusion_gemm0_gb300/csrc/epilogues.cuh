@@ -1,9 +1,12 @@
 // epilogues.cuh -- the epilogue programs of the chain, one policy class each.
 //
 // Each thread owns one row of the 128 x 256 fp32 accumulator tile (its TMEM
-// lane) and walks it in 32-column chunks (tcgen05.ld 32x32b.x32), so every
-// row reduction below is a plain per-thread sum: no shuffles, no atomics, and
-// a fixed summation order (bit-reproducible results).
+// lane) and one 128-column half of it (TileCtx::half; two epilogue warps share
+// each lane quadrant), walked in 32-column chunks (tcgen05.ld 32x32b.x32).  So
+// every row reduction below is a plain per-thread sum that leaves one partial
+// per (row, half tile): no shuffles, no atomics, and a fixed summation order
+// (bit-reproducible results).  Partials are stored [2 * nt][M], index
+// 2 * nb + half.
 //
 // The primitives used are the method's tile-local ones (CODA blog,
 // blog.hotdry.top, section "五类 Epilogue 原语"): an elementwise map (residual
@@ -28,6 +31,13 @@ struct EpiDefaultCols {
   static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
 };
 
+constexpr int kHalfCols = kBN / 2;        // accumulator columns per epilogue thread
+constexpr int kHalfChunks = kHalfCols / 32;
+
+__device__ __forceinline__ size_t partial_index(const TileCtx& c, int m) {
+  return static_cast<size_t>(2 * c.nb + c.half) * c.M + m;
+}
+
 __device__ __forceinline__ Chunk8 ldg8(const __nv_bfloat16* p) {
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
   return Chunk8{{v.x, v.y, v.z, v.w}};
@@ -43,7 +53,7 @@ __device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
 // tile-local partial sum of squares.
 //   h  = acc + z                (fp32)          -> h_out  bf16
 //   hg = h * gamma              (fp32)          -> hg_out bf16 (GEMM1's A operand)
-//   part[nb][m] = sum over the tile's columns of h^2 (fp32, before rounding)
+//   part[2 nb + half][m] = sum over the half tile's columns of h^2 (fp32, before rounding)
 // With hg_out == nullptr and part == nullptr it is the plain residual-add
 // epilogue of the unfused reference sequence.
 // ---------------------------------------------------------------------------
@@ -53,7 +63,7 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
     const __nv_bfloat16* gamma;
     __nv_bfloat16* h_out;
     __nv_bfloat16* hg_out;  // may be null (unfused sequence)
-    float* part;            // [nt][M], may be null (unfused sequence)
+    float* part;            // [2 * nt][M], may be null (unfused sequence)
   };
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
@@ -63,11 +73,12 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
     const bool fused = p.hg_out != nullptr;
     float ss = 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
       uint32_t v[32];
-      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + ch * 32;
+      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -91,7 +102,7 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
         }
       }
     }
-    if (row_ok && p.part != nullptr) p.part[static_cast<size_t>(c.nb) * c.M + m] = ss;
+    if (row_ok && p.part != nullptr) p.part[partial_index(c, m)] = ss;
   }
 };
 
@@ -112,11 +123,12 @@ struct EpiRowScale : EpiDefaultCols {
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
     const float rr = (row_ok && p.r != nullptr) ? __ldg(p.r + m) : 1.f;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
       uint32_t v[32];
-      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + ch * 32;
+      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -138,10 +150,10 @@ struct EpiRowScale : EpiDefaultCols {
 // ---------------------------------------------------------------------------
 // Data-gradient epilogue (CODA blog, section "反向传播的 GEMM-Epilogue 结构"):
 // acc = grad_h2 = grad_y @ W1^T for this tile.
-//   pass 1: qpart[nb][m] = sum over the tile's columns of acc * gamma * h;
+//   pass 1: qpart[2 nb + half][m] = sum over the half tile of acc * gamma * h;
 //           publish it with a release flag carrying this call's token;
 //   then:   wait until every column tile of this row block has published,
-//           q[m] = sum_nb qpart[nb][m] (fixed order), coef = r^3 q / d;
+//           q[m] = sum of the row's 2 nt partials (fixed order), coef = r^3 q / d;
 //   pass 2: grad_h = r * gamma * acc - coef * h   -> dh_out bf16.
 // q * r = sum_j grad_h2 * h2 is the statistic s of the method.  The flag wait
 // needs every block of the launch resident (cooperative launch) and tiles in
@@ -154,7 +166,7 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     const __nv_bfloat16* gamma;
     const float* r;
     __nv_bfloat16* dh_out;
-    float* qpart;     // [nt][M]
+    float* qpart;     // [2 * nt][M]
     uint64_t* flags;  // [mt][nt]
     uint64_t token;
   };
@@ -167,11 +179,12 @@ struct EpiRmsNormBackward : EpiDefaultCols {
 
     float qp = 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
       uint32_t v[32];
-      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + ch * 32;
+      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -189,7 +202,7 @@ struct EpiRmsNormBackward : EpiDefaultCols {
         }
       }
     }
-    if (row_ok) p.qpart[static_cast<size_t>(c.nb) * c.M + m] = qp;
+    if (row_ok) p.qpart[partial_index(c, m)] = qp;
 
     // Publish this tile's partials, then wait for the whole row block.
     named_bar_sync(1, kEpiThreads);
@@ -206,17 +219,18 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     float q = 0.f;
     float rr = 0.f;
     if (row_ok) {
-      for (int j = 0; j < c.nt; ++j) q += __ldcg(p.qpart + static_cast<size_t>(j) * c.M + m);
+      for (int j = 0; j < 2 * c.nt; ++j) q += __ldcg(p.qpart + static_cast<size_t>(j) * c.M + m);
       rr = __ldg(p.r + m);
     }
     const float coef = rr * rr * rr * q / static_cast<float>(c.N);
 
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
       uint32_t v[32];
-      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + ch * 32;
+      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -276,13 +290,14 @@ struct EpiRowScaleSwiGLU {
     const size_t a_row = static_cast<size_t>(row_ok ? m : 0) * half;
     const size_t y_row = static_cast<size_t>(row_ok ? m : 0) * c.N;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int ch = 0; ch < 2; ++ch) {  // this thread's 64 gated outputs of the tile
+      const int col = c.half * 64 + ch * 32;
       uint32_t g[32], u[32];
-      tmem_ld32(c.taddr + ch * 32, g);
-      tmem_ld32(c.taddr + 128 + ch * 32, u);
+      tmem_ld32(c.taddr + col, g);
+      tmem_ld32(c.taddr + 128 + col, u);
       tmem_ld_wait(g);
       tmem_ld_wait(u);
-      const int o0 = c.nb * 128 + ch * 32;
+      const int o0 = c.nb * 128 + col;
       if (row_ok) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -319,13 +334,13 @@ struct EpiRowScaleSwiGLU {
 // 256-column tile of the N1/2 gated columns.  With the saved pre-activation
 // y = [g | u] (bf16, [M, N1]) loaded as a rank-2 tile:
 //   dg = da * u * silu'(g),  du = da * silu(g)      -> dy_out = [dg | du] bf16
-//   spart[nb][m] = sum over the tile of dg * g + du * u   (fp32)
+//   spart[2 nb + half][m] = sum over the half tile of dg * g + du * u   (fp32)
 // ---------------------------------------------------------------------------
 struct EpiSwiGLUBackward : EpiDefaultCols {
   struct Params {
     const __nv_bfloat16* y;  // [M, 2 * half] saved pre-activation [g | u]
     __nv_bfloat16* dy_out;   // [M, 2 * half]
-    float* spart;            // [nt][M]
+    float* spart;            // [2 * nt][M]
   };
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
@@ -335,11 +350,12 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * (2 * static_cast<size_t>(half));
     float ss = 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
       uint32_t v[32];
-      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int j0 = c.nb * kBN + ch * 32;
+      const int j0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -371,7 +387,7 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
         }
       }
     }
-    if (row_ok) p.spart[static_cast<size_t>(c.nb) * c.M + m] = ss;
+    if (row_ok) p.spart[partial_index(c, m)] = ss;
   }
 };
 
@@ -396,11 +412,12 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
     const float rr = row_ok ? __ldg(p.r + m) : 0.f;
     const float coef = row_ok ? rr * rr * __ldg(p.s + m) / static_cast<float>(c.N) : 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < kBN / 32; ++ch) {
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
       uint32_t v[32];
-      tmem_ld32(c.taddr + ch * 32, v);
+      tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + ch * 32;
+      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {

@@ -10,13 +10,14 @@
 //   i.e. a weight stored [in, out]) or K-major (row-major [N, K], i.e. the
 //   transpose of a weight stored [in, out]).
 //
-// Block = 192 threads, one block per SM, persistent over output tiles:
+// Block = 320 threads, one block per SM, persistent over output tiles:
 //   warp 0      TMA producer: 4-stage ring of A (128x64) + B (64x256) tiles,
 //               128-byte swizzle, completion on mbarriers with expect-tx
 //   warp 1      allocates 512 TMEM columns, one thread issues
 //               tcgen05.mma (M=128, N=256, K=16) into one of two fp32
 //               accumulators (2 x 256 columns), commits stage and tile barriers
-//   warps 2..5  epilogue: drain the accumulator with tcgen05.ld (thread = row),
+//   warps 2..9  epilogue: drain the accumulator with tcgen05.ld (thread = row;
+//               two warps per TMEM lane quadrant, one per 128-column half),
 //               apply Epi, store; while they work the MMA warp fills the other
 //               accumulator, so epilogue and mainloop overlap.
 #pragma once
@@ -31,8 +32,8 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kEpiThreads = 256;
 constexpr int kEpiFirstThread = 64;
 constexpr uint32_t kAStageBytes = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kBStageBytes = kBN * kBK * 2;   // 32 KB
@@ -69,6 +70,7 @@ struct TileCtx {
   uint32_t taddr;  // TMEM address of this thread's lane, column 0 of the tile
   int mb, nb;      // tile coordinates
   int row;         // row inside the tile (0..127) owned by this thread
+  int half;        // which 128-column half of the tile this thread drains (0, 1)
   int M, N;        // problem size (N = output columns)
   int nt;          // number of column tiles
 };
@@ -78,7 +80,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(ok ? 1u : 0u)
@@ -245,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;         // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;  // warps 2..5: columns 0..127, warps 6..9: 128..255
     const int row = quad * 32 + lane;
     uint32_t it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.mb = mb;
       c.nb = nb;
       c.row = row;
+      c.half = half;
       c.M = M;
       c.N = N;
       c.nt = nt;

@@ -199,6 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     uint32_t it = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++it) {
@@ -214,6 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       c.mb = mb * 2 + static_cast<int>(rank);  // this CTA's 128-row slab
       c.nb = nb;
       c.row = row;
+      c.half = half;
       c.M = M;
       c.N = N;
       c.nt = nt;

@@ -67,19 +67,20 @@ typedef enum {
 } coda_status_t;
 
 /* Bytes of device workspace coda_fwd needs: the bf16 GEMM1 operand
- * hg = h * gamma ([M, d]) and the fp32 per-(row, column-tile) partial sums of
- * h^2.  Returns 0 for M == 0. */
+ * hg = h * gamma ([M, d]) and the fp32 partial sums of h^2, two per row and
+ * 256-column tile.  Returns 0 for M == 0. */
 CODA_API size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
-/* Bytes of device workspace coda_bwd_dgrad needs: fp32 per-(row, column-tile)
- * partial row statistics and one 64-bit completion flag per output tile. */
+/* Bytes of device workspace coda_bwd_dgrad needs: fp32 partial row
+ * statistics (two per row and 256-column tile) and one 64-bit completion flag
+ * per 128-row slab and column tile. */
 CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /*
  * Forward of the chain (the method's three steps, see the file header):
  *   1. GEMM0 epilogue: h = x @ W0 + z (fp32), stores h and hg = h * gamma as
- *      bf16, and writes per-(row, 256-column tile) partial sums of h^2
- *      (fp32, taken before rounding h).
+ *      bf16, and writes partial sums of h^2 (fp32, taken before rounding h;
+ *      two per row and 256-column tile).
  *   2. auxiliary row reduction: r[m] = 1 / sqrt(sum of partials / d + eps).
  *   3. GEMM1 epilogue: y = r[m] * (hg @ W1), stored bf16.
  * No normalised [M, d] tensor is ever written.
@@ -246,8 +247,8 @@ CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t 
  * reserved in advance.  It computes exactly what coda_bwd_dgrad computes, with
  * the same kernel, but takes only inputs and outputs: the per-tile partial row
  * statistics and the completion flags live in a fixed array inside the
- * library (CODA_NOALLOC_MAX_PARTIALS floats + CODA_NOALLOC_MAX_TILES 64-bit
- * flags, about 2.1 MiB), which every GPU that loads the library holds until
+ * library (2 * CODA_NOALLOC_MAX_PARTIALS floats + CODA_NOALLOC_MAX_TILES 64-bit
+ * flags, about 4.1 MiB), which every GPU that loads the library holds until
  * the process exits.  It allocates nothing and calls no allocating routine.
  *
  *  - Size limit: ceil(d/256) * M <= CODA_NOALLOC_MAX_PARTIALS and

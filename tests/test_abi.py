@@ -47,15 +47,15 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # hg [M,d] bf16 + partial sums [ceil(d/256), M] fp32, each rounded up to 256 B
+    # hg [M,d] bf16 + partial sums [2 * ceil(d/256), M] fp32, each rounded up to 256 B
     M, d, N1 = 8192, 4096, 28672
-    assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 16 * M * 4
+    assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 32 * M * 4
     assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == M * d * 2
-    # qpart [16, M] fp32 + flags [2 * ceil(M/256) * 16] u64 (one per 128-row slab and column tile)
-    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 16 * M * 4 + 64 * 16 * 8
-    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 1280 + 256  # 4 slabs x 1 tile
+    # qpart [2 * 16, M] fp32 + flags [2 * ceil(M/256) * 16] u64 (one per 128-row slab and column tile)
+    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 32 * M * 4 + 64 * 16 * 8
+    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 2560 + 256  # 4 slabs x 1 tile
     assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
-    assert lib.coda_fwd_workspace_bytes(300, 328, 776) == 196864 + 2560  # ragged: rounded up
+    assert lib.coda_fwd_workspace_bytes(300, 328, 776) == 196864 + 4864  # ragged: rounded up
     assert lib.coda_fwd_workspace_bytes(10, 12, 16) == 0  # d % 8 != 0: unsupported
 
 
