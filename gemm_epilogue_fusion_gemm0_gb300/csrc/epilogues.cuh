@@ -31,6 +31,24 @@ struct EpiDefaultCols {
   static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
 };
 
+// Loads the four 8-element groups [n0 + 8q, n0 + 8q + 8) of row `rowp` (q = 0..3);
+// groups at or past `limit` (or all of them when !ok) read as zeros.  Issued for
+// the next 32-column chunk before the current one is processed, so global-load
+// latency overlaps the epilogue arithmetic.
+__device__ __forceinline__ void ldg_chunk(const __nv_bfloat16* rowp, int n0, int limit, bool ok,
+                                          Chunk8 (&out)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int n = n0 + q * 8;
+    if (ok && n < limit) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(rowp + n));
+      out[q] = Chunk8{{v.x, v.y, v.z, v.w}};
+    } else {
+      out[q] = Chunk8{{0u, 0u, 0u, 0u}};
+    }
+  }
+}
+
 constexpr int kHalfCols = kBN / 2;        // accumulator columns per epilogue thread
 constexpr int kHalfChunks = kHalfCols / 32;
 
@@ -71,34 +89,48 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
     const bool fused = p.hg_out != nullptr;
+    const int nbase = c.nb * kBN + c.half * kHalfCols;
     float ss = 0.f;
-#pragma unroll 1
+    Chunk8 zc[4], gc[4];
+    ldg_chunk(p.z + rowoff, nbase, c.N, row_ok, zc);
+    ldg_chunk(p.gamma, nbase, c.N, row_ok, gc);
+#pragma unroll
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
+      Chunk8 zn[4], gn[4];
+      if (ch + 1 < kHalfChunks) {
+        ldg_chunk(p.z + rowoff, n0 + 32, c.N, row_ok, zn);
+        ldg_chunk(p.gamma, n0 + 32, c.N, row_ok, gn);
+      }
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int n = n0 + g * 8;
           if (n < c.N) {
-            const Chunk8 zz = ldg8(p.z + rowoff + n);
-            const Chunk8 gg = ldg8(p.gamma + n);
             uint32_t hw[4], hgw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zz.w[e]);
-              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zz.w[e]);
+              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zc[g].w[e]);
+              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zc[g].w[e]);
               ss = fmaf(h0, h0, ss);
               ss = fmaf(h1, h1, ss);
               hw[e] = pack_bf16x2(h0, h1);
-              hgw[e] = pack_bf16x2(h0 * bf16lo(gg.w[e]), h1 * bf16hi(gg.w[e]));
+              hgw[e] = pack_bf16x2(h0 * bf16lo(gc[g].w[e]), h1 * bf16hi(gc[g].w[e]));
             }
             stg8(p.h_out + rowoff + n, hw);
             if (fused) stg8(p.hg_out + rowoff + n, hgw);
           }
+        }
+      }
+      if (ch + 1 < kHalfChunks) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          zc[q] = zn[q];
+          gc[q] = gn[q];
         }
       }
     }
@@ -348,21 +380,30 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
     const bool row_ok = m < c.M;
     const int half = c.N;  // the GEMM's output width is the gated width
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * (2 * static_cast<size_t>(half));
+    const __nv_bfloat16* grow = p.y + rowoff;
+    const __nv_bfloat16* urow = p.y + rowoff + half;
+    const int jbase = c.nb * kBN + c.half * kHalfCols;
     float ss = 0.f;
-#pragma unroll 1
+    Chunk8 gc[4], uc[4];
+    ldg_chunk(grow, jbase, half, row_ok, gc);
+    ldg_chunk(urow, jbase, half, row_ok, uc);
+#pragma unroll
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int j0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
+      Chunk8 gn[4], un[4];
+      if (ch + 1 < kHalfChunks) {
+        ldg_chunk(grow, j0 + 32, half, row_ok, gn);
+        ldg_chunk(urow, j0 + 32, half, row_ok, un);
+      }
       tmem_ld_wait(v);
-      const int j0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int j = j0 + q * 8;
           if (j < half) {
-            const Chunk8 gg = ldg8(p.y + rowoff + j);
-            const Chunk8 uu = ldg8(p.y + rowoff + half + j);
             uint32_t dgw[4], duw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -370,9 +411,9 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
                 const float da = __uint_as_float(v[q * 8 + 2 * e + k]);
-                const float g = k ? bf16hi(gg.w[e]) : bf16lo(gg.w[e]);
-                const float u = k ? bf16hi(uu.w[e]) : bf16lo(uu.w[e]);
-                const float sig = 1.0f / (1.0f + __expf(-g));
+                const float g = k ? bf16hi(gc[q].w[e]) : bf16lo(gc[q].w[e]);
+                const float u = k ? bf16hi(uc[q].w[e]) : bf16lo(uc[q].w[e]);
+                const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
                 dgv[k] = da * u * sig * (1.0f + g * (1.0f - sig));
                 duv[k] = da * g * sig;
                 ss = fmaf(dgv[k], g, ss);
@@ -384,6 +425,13 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
             stg8(p.dy_out + rowoff + j, dgw);
             stg8(p.dy_out + rowoff + half + j, duw);
           }
+        }
+      }
+      if (ch + 1 < kHalfChunks) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          gc[q] = gn[q];
+          uc[q] = un[q];
         }
       }
     }
@@ -411,31 +459,45 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
     const float rr = row_ok ? __ldg(p.r + m) : 0.f;
     const float coef = row_ok ? rr * rr * __ldg(p.s + m) / static_cast<float>(c.N) : 0.f;
-#pragma unroll 1
+    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    Chunk8 hc[4], gc[4];
+    ldg_chunk(p.h + rowoff, nbase, c.N, row_ok, hc);
+    ldg_chunk(p.gamma, nbase, c.N, row_ok, gc);
+#pragma unroll
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
+      Chunk8 hn[4], gn[4];
+      if (ch + 1 < kHalfChunks) {
+        ldg_chunk(p.h + rowoff, n0 + 32, c.N, row_ok, hn);
+        ldg_chunk(p.gamma, n0 + 32, c.N, row_ok, gn);
+      }
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int n = n0 + g * 8;
           if (n < c.N) {
-            const Chunk8 hh = ldg8(p.h + rowoff + n);
-            const Chunk8 gg = ldg8(p.gamma + n);
             uint32_t dw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
-                               coef * bf16lo(hh.w[e]);
-              const float d1 = rr * bf16hi(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
-                               coef * bf16hi(hh.w[e]);
+              const float d0 = rr * bf16lo(gc[g].w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
+                               coef * bf16lo(hc[g].w[e]);
+              const float d1 = rr * bf16hi(gc[g].w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
+                               coef * bf16hi(hc[g].w[e]);
               dw[e] = pack_bf16x2(d0, d1);
             }
             stg8(p.dh_out + rowoff + n, dw);
           }
+        }
+      }
+      if (ch + 1 < kHalfChunks) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hc[q] = hn[q];
+          gc[q] = gn[q];
         }
       }
     }
