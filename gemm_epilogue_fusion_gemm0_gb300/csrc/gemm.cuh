@@ -43,7 +43,12 @@ constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr uint32_t kSmemA = 0;
 constexpr uint32_t kSmemB = kStages * kAStageBytes;
 constexpr uint32_t kSmemBar = kSmemB + kStages * kBStageBytes;
+// barriers: full[S] | empty[S] | tfull[2] | tempty[2] | drain, then the TMEM
+// address holder and the abort flag right after them
+constexpr uint32_t kBarBytes = 8u * (2 * kStages + 5);
 constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;  // barriers + 1 KB alignment slack
+
+static_assert(kBarBytes + 8 <= 256, "barrier area overflows its reserved 256 bytes");
 
 static_assert(kBK * 2 == 128, "one K tile row must be exactly one 128-byte swizzle row");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
@@ -107,8 +112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bar0 + 16u * kStages;
   const uint32_t bar_tempty = bar_tfull + 16u;
   const uint32_t bar_drain = bar_tempty + 16u;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kSmemBar + 128);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + 132);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kSmemBar + kBarBytes);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + kBarBytes + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

@@ -29,7 +29,12 @@ constexpr uint32_t kPairStageBytes = kPairAStageBytes + kPairBStageBytes;
 constexpr uint32_t kPairSmemA = 0;
 constexpr uint32_t kPairSmemB = kPairStages * kPairAStageBytes;
 constexpr uint32_t kPairSmemBar = kPairSmemB + kPairStages * kPairBStageBytes;
+// barriers: full[S] | empty[S] | tfull[2] | tempty[2] | drain, then the TMEM
+// address holder and the abort flag right after them
+constexpr uint32_t kPairBarBytes = 8u * (2 * kPairStages + 5);
 constexpr uint32_t kPairSmemBytes = kPairSmemBar + 256 + 1024;
+
+static_assert(kPairBarBytes + 8 <= 256, "barrier area overflows its reserved 256 bytes");
 
 static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
@@ -52,8 +57,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t bar_tfull = bar0 + 16u * kPairStages;
   const uint32_t bar_tempty = bar_tfull + 16u;
   const uint32_t bar_drain = bar_tempty + 16u;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPairSmemBar + 128);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kPairSmemBar + 132);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPairSmemBar + kPairBarBytes);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(smem + kPairSmemBar + kPairBarBytes + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
