@@ -89,48 +89,34 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
     const bool fused = p.hg_out != nullptr;
-    const int nbase = c.nb * kBN + c.half * kHalfCols;
     float ss = 0.f;
-    Chunk8 zc[4], gc[4];
-    ldg_chunk(p.z + rowoff, nbase, c.N, row_ok, zc);
-    ldg_chunk(p.gamma, nbase, c.N, row_ok, gc);
-#pragma unroll
+#pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
-      Chunk8 zn[4], gn[4];
-      if (ch + 1 < kHalfChunks) {
-        ldg_chunk(p.z + rowoff, n0 + 32, c.N, row_ok, zn);
-        ldg_chunk(p.gamma, n0 + 32, c.N, row_ok, gn);
-      }
       tmem_ld_wait(v);
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int n = n0 + g * 8;
           if (n < c.N) {
+            const Chunk8 zz = ldg8(p.z + rowoff + n);
+            const Chunk8 gg = ldg8(p.gamma + n);
             uint32_t hw[4], hgw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zc[g].w[e]);
-              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zc[g].w[e]);
+              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zz.w[e]);
+              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zz.w[e]);
               ss = fmaf(h0, h0, ss);
               ss = fmaf(h1, h1, ss);
               hw[e] = pack_bf16x2(h0, h1);
-              hgw[e] = pack_bf16x2(h0 * bf16lo(gc[g].w[e]), h1 * bf16hi(gc[g].w[e]));
+              hgw[e] = pack_bf16x2(h0 * bf16lo(gg.w[e]), h1 * bf16hi(gg.w[e]));
             }
             stg8(p.h_out + rowoff + n, hw);
             if (fused) stg8(p.hg_out + rowoff + n, hgw);
           }
-        }
-      }
-      if (ch + 1 < kHalfChunks) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          zc[q] = zn[q];
-          gc[q] = gn[q];
         }
       }
     }
