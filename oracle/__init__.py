@@ -9,6 +9,8 @@ library: the two share no code.
 from .coda_oracle import (  # noqa: F401
     ForwardResult,
     BackwardResult,
+    FullBackwardResult,
+    backward_full,
     residual_gemm,
     mean_square,
     inverse_rms,

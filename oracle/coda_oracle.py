@@ -47,6 +47,16 @@ class ForwardResult:
 
 
 @dataclass
+class FullBackwardResult:
+    dh: np.ndarray      # [M, d]  total gradient at h (RMSNorm branch + upstream residual); = dz
+    dx: np.ndarray      # [M, d]
+    dgamma: np.ndarray  # [d]
+    dW0: np.ndarray     # [d, d]
+    dW1: np.ndarray     # [d, N1]
+    h2: np.ndarray      # [M, d]  normalised activation RMSNorm(h, gamma)
+
+
+@dataclass
 class BackwardResult:
     dh: np.ndarray   # [M, d]  gradient w.r.t. h through the RMSNorm branch
     s: np.ndarray    # [M]     row statistic sum_j grad_h2 * h2
@@ -121,6 +131,30 @@ def backward_dgrad(dy, W1, h, r, gamma) -> BackwardResult:
     dh = r[:, None] * g - ((r ** 3) / d * gh)[:, None] * h
     s = np.sum(dh2 * rmsnorm(h, gamma, r), axis=1)
     return BackwardResult(dh=dh, s=s, dh2=dh2)
+
+
+def backward_full(dy, x, W0, W1, h, r, gamma, dh_res=None) -> FullBackwardResult:
+    """All gradients of the chain h = x @ W0 + z, y = RMSNorm(h, gamma) @ W1,
+    given dy, the saved h and r, and optionally the gradient dh_res that
+    reaches h through the residual stream.
+
+    Steps:
+      1. dh2, dh (RMSNorm branch) from backward_dgrad
+      2. dh_tot = dh + dh_res                       (= dz, since h = ... + z)
+      3. h2 = RMSNorm(h, gamma);  dgamma = sum_m dh2 * (r * h)  (dh2/dgamma_j = r h_j)
+      4. dW1 = h2^T dy
+      5. dx = dh_tot @ W0^T,  dW0 = x^T dh_tot
+    """
+    b = backward_dgrad(dy, W1, h, r, gamma)
+    dh_tot = b.dh if dh_res is None else b.dh + _f64(dh_res)
+    h = _f64(h)
+    r = _f64(r)
+    h2 = rmsnorm(h, gamma, r)
+    dgamma = np.sum(b.dh2 * (r[:, None] * h), axis=0)
+    dW1 = h2.T @ _f64(dy)
+    dx = dh_tot @ _f64(W0).T
+    dW0 = _f64(x).T @ dh_tot
+    return FullBackwardResult(dh=dh_tot, dx=dx, dgamma=dgamma, dW0=dW0, dW1=dW1, h2=h2)
 
 
 def silu(t) -> np.ndarray:

@@ -468,3 +468,95 @@ def test_given_s_planted_mistake_is_caught(monkeypatch):
                         * np.asarray(h))
     with pytest.raises(AssertionError):
         pin_statistic_upstream_equals_definition()
+
+
+# ----------------------------------------------------------------------------
+# Full backward of the chain (all parameter and input gradients)
+# ----------------------------------------------------------------------------
+
+def pin_full_backward_autograd(seed=13):
+    """torch autograd (fp64) of L = sum(dy * y) + sum(dh_res * h) through
+    h = x @ W0 + z, y = rms_norm(h, gamma) @ W1."""
+    rng = np.random.default_rng(seed)
+    for (M, d, N1) in [(5, 8, 6), (3, 16, 12)]:
+        x, W0, z, gamma, W1, dy, eps = _rand_case(rng, M, d, N1, eps=1e-5)
+        dh_res = 0.2 * rng.standard_normal((M, d))
+        T = {k: torch.tensor(v, requires_grad=True) for k, v in
+             dict(x=x, W0=W0, z=z, gamma=gamma, W1=W1).items()}
+        th = T["x"] @ T["W0"] + T["z"]
+        ty = torch.nn.functional.rms_norm(th, (d,), weight=T["gamma"], eps=eps) @ T["W1"]
+        loss = torch.sum(torch.tensor(dy) * ty) + torch.sum(torch.tensor(dh_res) * th)
+        loss.backward()
+        f = O.forward(x, W0, z, gamma, W1, eps)
+        b = O.backward_full(dy, x, W0, W1, f.h, f.r, gamma, dh_res)
+        np.testing.assert_allclose(b.dh, T["z"].grad.numpy(), rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(b.dx, T["x"].grad.numpy(), rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(b.dW0, T["W0"].grad.numpy(), rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(b.dW1, T["W1"].grad.numpy(), rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(b.dgamma, T["gamma"].grad.numpy(), rtol=1e-9, atol=1e-12)
+
+
+def pin_full_backward_finite_differences(seed=14):
+    """Central differences of L = sum(dy * y) in gamma and W0 (no upstream term)."""
+    rng = np.random.default_rng(seed)
+    M, d, N1 = 3, 5, 4
+    x, W0, z, gamma, W1, dy, eps = _rand_case(rng, M, d, N1, eps=1e-3)
+
+    def loss(W0_, gamma_):
+        f = O.forward(x, W0_, z, gamma_, W1, eps)
+        return float(np.sum(dy * f.y))
+
+    f = O.forward(x, W0, z, gamma, W1, eps)
+    b = O.backward_full(dy, x, W0, W1, f.h, f.r, gamma)
+    step = 1e-6
+    for j in range(d):
+        gp, gm = gamma.copy(), gamma.copy()
+        gp[j] += step
+        gm[j] -= step
+        fd = (loss(W0, gp) - loss(W0, gm)) / (2 * step)
+        np.testing.assert_allclose(b.dgamma[j], fd, rtol=1e-5, atol=1e-8)
+    for (i, j) in [(0, 0), (2, 3), (4, 1)]:
+        wp, wm = W0.copy(), W0.copy()
+        wp[i, j] += step
+        wm[i, j] -= step
+        fd = (loss(wp, gamma) - loss(wm, gamma)) / (2 * step)
+        np.testing.assert_allclose(b.dW0[i, j], fd, rtol=1e-5, atol=1e-8)
+
+
+FULL_BWD_PINS = [pin_full_backward_autograd, pin_full_backward_finite_differences]
+
+
+@pytest.mark.parametrize("pin", FULL_BWD_PINS, ids=lambda p: p.__name__)
+def test_full_backward_pin(pin):
+    pin()
+
+
+def _full_bwd_mutant(kind):
+    orig = O.backward_full
+
+    def bwd(dy, x, W0, W1, h, r, gamma, dh_res=None):
+        res = orig(dy, x, W0, W1, h, r, gamma, dh_res)
+        if kind == "dgamma_without_r":
+            bd = O.backward_dgrad(dy, W1, h, r, gamma)
+            res.dgamma = np.sum(bd.dh2 * np.asarray(h, float), axis=0)
+        elif kind == "dW1_from_h_not_h2":
+            res.dW1 = np.asarray(h, float).T @ np.asarray(dy, float)
+        elif kind == "dx_without_residual_grad" and dh_res is not None:
+            res.dx = (res.dh - np.asarray(dh_res, float)) @ np.asarray(W0, float).T
+        elif kind == "dW0_transposed":
+            res.dW0 = res.dW0.T
+        return res
+    return bwd
+
+
+@pytest.mark.parametrize("kind", ["dgamma_without_r", "dW1_from_h_not_h2", "dx_without_residual_grad",
+                                  "dW0_transposed"])
+def test_full_backward_planted_mistake_is_caught(kind, monkeypatch):
+    monkeypatch.setattr(O, "backward_full", _full_bwd_mutant(kind))
+    failed = []
+    for pin in FULL_BWD_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, kind
