@@ -397,6 +397,44 @@ def run_coda(args):
                            "dgrad_given_s": w.bwd_flops / (sb_k[2] * 1e-3) / 1e12},
         "note": "coda_bwd_swiglu_dgrad: dout@W2^T with SwiGLU-bwd + partial s epilogue, "
                 "row sum, dy@W1^T with tile-local RMSNorm bwd"}
+    # all gradients of the chain (training step backward): coda_bwd, 5 launches
+    dh_res = (torch.randn((M, d), device=dev) * 0.1).to(torch.bfloat16)
+    fb_out = {"dh": dh, "dx": torch.empty((M, d), dtype=torch.bfloat16, device=dev),
+              "dgamma": torch.empty((d,), dtype=torch.float32, device=dev),
+              "dW0": torch.empty((d, d), dtype=torch.float32, device=dev),
+              "dW1": torch.empty((d, N1), dtype=torch.float32, device=dev)}
+    ws_fb = B.workspace(B.coda_bwd_workspace_bytes(M, d, N1), dev)
+    B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+               stream=stream)
+    for _ in range(3):
+        B.coda_bwd(dy, g["x"], g["W0"], g["W1"], h, r, g["gamma"], dh_res, out=fb_out, ws=ws_fb,
+                   stream=stream)
+    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KS)]
+    for ev in fev:
+        for e in ev:
+            e.record(stream)
+    barrier()
+    s0.record(stream)
+    for i in range(KS):
+        fev[i][0].record(stream)
+        B.coda_set_launch_events(fev[i][1:6])
+        B.coda_bwd(dy, g["x"], g["W0"], g["W1"], h, r, g["gamma"], dh_res, out=fb_out, ws=ws_fb,
+                   stream=stream)
+    s1.record(stream)
+    barrier()
+    B.coda_set_launch_events(None)
+    fb_ms = s0.elapsed_time(s1) / KS
+    fb_k = [statistics.fmean(fev[i][j].elapsed_time(fev[i][j + 1]) for i in range(KS))
+            for j in range(5)]
+    fb_fl = [2 * M * N1 * d, 0, 2 * d * N1 * M, 2 * M * d * d, 2 * d * d * M]
+    fb_names = ["dgrad_rmsnorm_bwd_dgamma_h2", "colsum_dgamma", "dW1_h2T_dy", "dx_dh_W0T",
+                "dW0_xT_dh"]
+    extras["bwd_full"] = {
+        "ms": fb_ms, "tflops": sum(fb_fl) / (fb_ms * 1e-3) / 1e12, "calls": KS,
+        "gpu_launches": 5 * KS,
+        "kernels_ms": dict(zip(fb_names, fb_k)),
+        "kernels_tflops": {n: f / (k * 1e-3) / 1e12 for n, f, k in zip(fb_names, fb_fl, fb_k) if f},
+        "note": "coda_bwd: all gradients (dh incl. residual grad, dx, dgamma, dW0, dW1)"}
     st, detail = B.coda_get_device_status()
     if st != B.CODA_OK:
         raise RuntimeError(f"device status after extras: {B.status_string(st)} {detail:#x}")

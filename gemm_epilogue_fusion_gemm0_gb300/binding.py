@@ -54,6 +54,9 @@ EXPORTS = {
     "coda_set_launch_events": (None, [_vp, ctypes.c_int]),
     "coda_bwd_dgrad_noalloc": (_st, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "coda_set_mma_mode": (_st, [ctypes.c_int]),
+    "coda_bwd_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "coda_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
+                       _vp, _sz, _vp]),
     "coda_bwd_swiglu_dgrad_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
     "coda_bwd_swiglu_dgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp,
                                     _vp, _vp, _vp, _sz, _vp]),
@@ -228,6 +231,37 @@ def coda_bwd_swiglu_dgrad(dout, W2, y, W1, h, r, gamma, dy=None, s=None, dh=None
     )
     _check(st, "coda_bwd_swiglu_dgrad")
     return dy, s, dh
+
+
+def coda_bwd_workspace_bytes(M: int, d: int, N1: int) -> int:
+    return int(_lib.coda_bwd_workspace_bytes(M, d, N1))
+
+
+def coda_bwd(dy, x, W0, W1, h, r, gamma, dh_res=None, out=None, ws=None, stream=None):
+    """All gradients of the chain; returns dict dh (= dz), dx, dgamma, dW0, dW1."""
+    M, N1 = dy.shape
+    d = W1.shape[0]
+    dev = dy.device
+    bf, f32 = torch.bfloat16, torch.float32
+    o = dict(out or {})
+    o.setdefault("dh", torch.empty((M, d), dtype=bf, device=dev))
+    o.setdefault("dx", torch.empty((M, d), dtype=bf, device=dev))
+    o.setdefault("dgamma", torch.empty((d,), dtype=f32, device=dev))
+    o.setdefault("dW0", torch.empty((d, d), dtype=f32, device=dev))
+    o.setdefault("dW1", torch.empty((d, N1), dtype=f32, device=dev))
+    if ws is None:
+        ws = workspace(coda_bwd_workspace_bytes(M, d, N1), dev)
+    st = _lib.coda_bwd(
+        _dev(dy, bf, (M, N1), "dy"), _dev(x, bf, (M, d), "x"), _dev(W0, bf, (d, d), "W0"),
+        _dev(W1, bf, (d, N1), "W1"), _dev(h, bf, (M, d), "h"), _dev(r, f32, (M,), "r"),
+        _dev(gamma, bf, (d,), "gamma"), None if dh_res is None else _dev(dh_res, bf, (M, d), "dh_res"),
+        M, d, N1, _dev(o["dh"], bf, (M, d), "dh"), _dev(o["dx"], bf, (M, d), "dx"),
+        _dev(o["dgamma"], f32, (d,), "dgamma"), _dev(o["dW0"], f32, (d, d), "dW0"),
+        _dev(o["dW1"], f32, (d, N1), "dW1"), ws.data_ptr(), ws.numel() * ws.element_size(),
+        _stream_ptr(stream),
+    )
+    _check(st, "coda_bwd")
+    return o
 
 
 def coda_get_device_status(stream=None) -> tuple[int, int]:

@@ -50,6 +50,16 @@ __global__ void rowsum_kernel(const float* __restrict__ part, int nt, int M, flo
   s[m] = acc;
 }
 
+// dgamma[j] = sum_i gpart[i][j] over the per-warp column partials (fixed order).
+__global__ void colsum_kernel(const float* __restrict__ part, int nrows, int d,
+                              float* __restrict__ out) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= d) return;
+  float acc = 0.f;
+  for (int i = 0; i < nrows; ++i) acc += __ldg(part + static_cast<size_t>(i) * d + j);
+  out[j] = acc;
+}
+
 // Standalone RMSNorm of the unfused reference sequence: reads h, writes
 // hn = bf16(r * h * gamma) and r.  One block of 256 threads per row.
 __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const __nv_bfloat16* __restrict__ h,
@@ -118,6 +128,10 @@ static auto* const kPairDgrad = &gemm_pair_epilogue_kernel<EpiRmsNormBackward, f
 static auto* const kGemm1Swiglu = &gemm_epilogue_kernel<EpiRowScaleSwiGLU, true>;
 static auto* const kPairGemm1Swiglu = &gemm_pair_epilogue_kernel<EpiRowScaleSwiGLU, true>;
 static auto* const kSwigluBwd = &gemm_epilogue_kernel<EpiSwiGLUBackward, false>;
+static auto* const kWgrad = &gemm_epilogue_kernel<EpiStoreF32, true, true>;
+static auto* const kPairWgrad = &gemm_pair_epilogue_kernel<EpiStoreF32, true, true>;
+static auto* const kXgrad = &gemm_epilogue_kernel<EpiRowScale, false>;
+static auto* const kPairXgrad = &gemm_pair_epilogue_kernel<EpiRowScale, false>;
 static auto* const kPairSwigluBwd = &gemm_pair_epilogue_kernel<EpiSwiGLUBackward, false>;
 static auto* const kDgradGivenS = &gemm_epilogue_kernel<EpiRmsNormBackwardGivenS, false>;
 static auto* const kPairDgradGivenS = &gemm_pair_epilogue_kernel<EpiRmsNormBackwardGivenS, false>;
@@ -201,6 +215,14 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
                                  kPairSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -345,7 +367,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
   const uint64_t tmo = g_timeout_ns.load();
 
-  EpiResidualGammaSumsq::Params p0;
+  EpiResidualGammaSumsq::Params p0 = {};
   p0.z = reinterpret_cast<const __nv_bfloat16*>(z);
   p0.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p0.h_out = reinterpret_cast<__nv_bfloat16*>(h_out);
@@ -375,7 +397,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   }
   after_launch(1, stream);
   if (swiglu) {
-    EpiRowScaleSwiGLU::Params ps;
+    EpiRowScaleSwiGLU::Params ps = {};
     ps.r = r_out;
     ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
@@ -384,7 +406,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
              : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false,
                       mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
   } else {
-    EpiRowScale::Params p1;
+    EpiRowScale::Params p1 = {};
     p1.r = fused ? r_out : nullptr;
     p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
@@ -479,7 +501,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   ok &= tmap_2d(&mB, W1, N1, d, kBK, pair ? 128 : kBN);         // W1 [d(N), N1(K)] K-major
   if (!ok) return CODA_ERR_LAUNCH;
 
-  EpiRmsNormBackward::Params p;
+  EpiRmsNormBackward::Params p = {};
   p.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p.r = r;
@@ -502,6 +524,138 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
     return CODA_ERR_LAUNCH;
   }
   after_launch(0, stream);
+  return CODA_OK;
+}
+
+size_t coda_bwd_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
+  if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
+  const int64_t slabs = std::max(2 * cdiv(M, kPairBM), cdiv(M, kBM));
+  return coda_bwd_dgrad_workspace_bytes(M, d, N1) + align256(static_cast<size_t>(M) * d * 2) +
+         align256(static_cast<size_t>(4 * slabs) * d * 4);
+}
+
+coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16* W0,
+                       const coda_bf16* W1, const coda_bf16* h, const float* r,
+                       const coda_bf16* gamma, const coda_bf16* dh_res, int64_t M, int64_t d,
+                       int64_t N1, coda_bf16* dh_out, coda_bf16* dx_out, float* dgamma_out,
+                       float* dW0_out, float* dW1_out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  coda_status_t st = check_common(M, d, N1);
+  if (st != CODA_OK) return st;
+  if (M == 0) return CODA_OK;
+  if (!dy || !x || !W0 || !W1 || !h || !r || !gamma || !dh_out || !dx_out || !dgamma_out ||
+      !dW0_out || !dW1_out)
+    return CODA_ERR_INVALID_ARG;
+  const void* ptrs[] = {dy, x, W0, W1, h, r, gamma, dh_out, dx_out, dgamma_out, dW0_out, dW1_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CODA_ERR_MISALIGNED;
+  if (dh_res != nullptr && !aligned16(dh_res)) return CODA_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < coda_bwd_workspace_bytes(M, d, N1))
+    return CODA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
+  int sms = 0, max_pairs = 0;
+  st = device_setup(&sms, &max_pairs);
+  if (st != CODA_OK) return st;
+  const bool pair = g_mma_mode.load() == 1;
+  const uint64_t tmo = g_timeout_ns.load();
+  const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
+
+  const int nt = static_cast<int>(cdiv(d, kBN));
+  const int mt = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
+  const int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
+  if (nt > units) return CODA_ERR_UNSUPPORTED_SHAPE;
+  const int slabs = pair ? 2 * mt : mt;
+
+  char* ws = static_cast<char*>(workspace);
+  float* qpart = reinterpret_cast<float*>(ws);
+  uint64_t* flags =
+      reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(2 * nt) * M * 4));
+  char* rest = ws + coda_bwd_dgrad_workspace_bytes(M, d, N1);
+  __nv_bfloat16* h2 = reinterpret_cast<__nv_bfloat16*>(rest);
+  float* gpart = reinterpret_cast<float*>(rest + align256(static_cast<size_t>(M) * d * 2));
+
+  const uint32_t bbox = pair ? 128 : kBN;
+  CUtensorMap mDy, mW1, mH2, mDyMN, mDh, mW0, mX, mDhMN;
+  bool ok = tmap_2d(&mDy, dy, N1, M, kBK, kBM);     // dy [M, N1] K-major (dgrad)
+  ok &= tmap_2d(&mW1, W1, N1, d, kBK, bbox);        // W1 [d(N), N1(K)] K-major
+  ok &= tmap_2d(&mH2, h2, d, M, 64, kBK);           // h2^T: [M(K), d(M)] MN-major A
+  ok &= tmap_2d(&mDyMN, dy, N1, M, 64, kBK);        // dy: [M(K), N1(N)] MN-major B
+  ok &= tmap_2d(&mDh, dh_out, d, M, kBK, kBM);      // dh [M, d] K-major A
+  ok &= tmap_2d(&mW0, W0, d, d, kBK, bbox);         // W0 [d_in(N), d_out(K)] K-major B
+  ok &= tmap_2d(&mX, x, d, M, 64, kBK);             // x^T: [M(K), d(M)] MN-major A
+  ok &= tmap_2d(&mDhMN, dh_out, d, M, 64, kBK);     // dh: [M(K), d(N)] MN-major B
+  if (!ok) return CODA_ERR_LAUNCH;
+
+  // 1. dgrad + RMSNorm backward + residual gradient + h2 + dgamma partials
+  EpiRmsNormBackward::Params p = {};
+  p.h = reinterpret_cast<const __nv_bfloat16*>(h);
+  p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  p.r = r;
+  p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
+  p.qpart = qpart;
+  p.flags = flags;
+  uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
+  p.token = tok == 0 ? 1 : tok;
+  p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
+  p.h2_out = h2;
+  p.gpart = gpart;
+  cudaError_t e = pair ? launch(kPairDgrad, 2 * units, kThreads, kPairSmemBytes, stream, true,
+                                mDy, mW1, Mi, di, N1i, 1, p, tmo)
+                       : launch(kDgrad, units, kThreads, kSmemBytes, stream, true, mDy, mW1, Mi,
+                                di, N1i, 1, p, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(0, stream);
+  // 2. dgamma = column sums of the partials
+  e = launch(colsum_kernel, static_cast<int>(cdiv(d, 256)), 256, 0, stream, false,
+             static_cast<const float*>(gpart), 4 * slabs, di, dgamma_out);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(1, stream);
+  // 3. dW1 = h2^T dy   (K = tokens)
+  EpiStoreF32::Params pw1 = {};
+  pw1.out = dW1_out;
+  const int mtw = static_cast<int>(cdiv(d, pair ? kPairBM : kBM));
+  const int ntw1 = static_cast<int>(cdiv(N1, kBN));
+  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, kPairSmemBytes,
+                    stream, false, mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, tmo)
+           : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kSmemBytes, stream, false, mH2,
+                    mDyMN, di, N1i, Mi, kGroupM, pw1, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(2, stream);
+  // 4. dx = dh W0^T
+  EpiRowScale::Params px = {};
+  px.r = nullptr;
+  px.y_out = reinterpret_cast<__nv_bfloat16*>(dx_out);
+  const int mtx = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
+  e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, kPairSmemBytes,
+                    stream, false, mDh, mW0, Mi, di, di, kPairGroupM, px, tmo)
+           : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kSmemBytes, stream, false, mDh,
+                    mW0, Mi, di, di, kGroupM, px, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(3, stream);
+  // 5. dW0 = x^T dh   (K = tokens)
+  EpiStoreF32::Params pw0 = {};
+  pw0.out = dW0_out;
+  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, kPairSmemBytes,
+                    stream, false, mX, mDhMN, di, di, Mi, kPairGroupM, pw0, tmo)
+           : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kSmemBytes, stream, false, mX,
+                    mDhMN, di, di, Mi, kGroupM, pw0, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(4, stream);
   return CODA_OK;
 }
 
@@ -554,7 +708,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   const int mtp = static_cast<int>(cdiv(M, kPairBM));
 
   // 1. down-projection data gradient with the SwiGLU backward + partial s
-  EpiSwiGLUBackward::Params p0;
+  EpiSwiGLUBackward::Params p0 = {};
   p0.y = reinterpret_cast<const __nv_bfloat16*>(y);
   p0.dy_out = reinterpret_cast<__nv_bfloat16*>(dy_out);
   p0.spart = reinterpret_cast<float*>(workspace);
@@ -577,7 +731,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   }
   after_launch(1, stream);
   // 3. RMSNorm-branch data gradient, tile-local with s given
-  EpiRmsNormBackwardGivenS::Params p1;
+  EpiRmsNormBackwardGivenS::Params p1 = {};
   p1.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p1.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p1.r = r;
@@ -750,7 +904,7 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
   ok &= tmap_2d(&mB, W1, N1, d, kBK, kBN);
   if (!ok) return CODA_ERR_LAUNCH;
 
-  EpiRmsNormBackward::Params p;
+  EpiRmsNormBackward::Params p = {};
   p.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p.r = r;

@@ -125,6 +125,38 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
 };
 
 // ---------------------------------------------------------------------------
+// Plain fp32 store (weight gradients): out[m, n] = acc.
+// ---------------------------------------------------------------------------
+struct EpiStoreF32 : EpiDefaultCols {
+  struct Params {
+    float* out;  // [M, N] row-major
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+#pragma unroll 1
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
+      uint32_t v[32];
+      tmem_ld32(c.taddr + col, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + col;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const int n = n0 + g * 4;
+          if (n < c.N)
+            *reinterpret_cast<uint4*>(p.out + rowoff + n) =
+                make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
 // GEMM1 epilogue (step 3): y = r[m] * acc, the row scale applied after the
 // second GEMM.  With r == nullptr it is the plain store of the unfused
 // reference sequence.
@@ -187,6 +219,10 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     float* qpart;     // [2 * nt][M]
     uint64_t* flags;  // [mt][nt]
     uint64_t token;
+    // Optional extras of the full backward (all null for the plain dgrad):
+    const __nv_bfloat16* dh_res;  // [M, d] gradient reaching h through the residual; added to dh
+    __nv_bfloat16* h2_out;        // [M, d] normalised activation r * h * gamma (dW1's operand)
+    float* gpart;                 // [4 * slabs][d] per-warp column partials of dgamma
   };
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
@@ -241,6 +277,7 @@ struct EpiRmsNormBackward : EpiDefaultCols {
       rr = __ldg(p.r + m);
     }
     const float coef = rr * rr * rr * q / static_cast<float>(c.N);
+    const bool extras = p.gpart != nullptr;
 
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
@@ -249,6 +286,9 @@ struct EpiRmsNormBackward : EpiDefaultCols {
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
       const int n0 = c.nb * kBN + col;
+      float t[32];  // r * h * grad_h2: this row's contribution to dgamma
+#pragma unroll
+      for (int i = 0; i < 32; ++i) t[i] = 0.f;
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -256,18 +296,43 @@ struct EpiRmsNormBackward : EpiDefaultCols {
           if (n < c.N) {
             const Chunk8 hh = ldg8(p.h + rowoff + n);
             const Chunk8 gg = ldg8(p.gamma + n);
-            uint32_t dw[4];
+            Chunk8 rs = {{0u, 0u, 0u, 0u}};
+            if (p.dh_res != nullptr) rs = ldg8(p.dh_res + rowoff + n);
+            uint32_t dw[4], h2w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
-                               coef * bf16lo(hh.w[e]);
-              const float d1 = rr * bf16hi(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
-                               coef * bf16hi(hh.w[e]);
+              const float a0 = __uint_as_float(v[g * 8 + 2 * e]);
+              const float a1 = __uint_as_float(v[g * 8 + 2 * e + 1]);
+              const float h0 = bf16lo(hh.w[e]), h1 = bf16hi(hh.w[e]);
+              const float g0 = bf16lo(gg.w[e]), g1 = bf16hi(gg.w[e]);
+              const float d0 = rr * g0 * a0 - coef * h0 + bf16lo(rs.w[e]);
+              const float d1 = rr * g1 * a1 - coef * h1 + bf16hi(rs.w[e]);
               dw[e] = pack_bf16x2(d0, d1);
+              h2w[e] = pack_bf16x2(rr * h0 * g0, rr * h1 * g1);
+              t[g * 8 + 2 * e] = rr * h0 * a0;
+              t[g * 8 + 2 * e + 1] = rr * h1 * a1;
             }
             stg8(p.dh_out + rowoff + n, dw);
+            if (p.h2_out != nullptr) stg8(p.h2_out + rowoff + n, h2w);
           }
         }
+      }
+      if (extras) {
+        // Column sums over the warp's 32 rows: butterfly reduction; lane k ends
+        // with the sum for column n0 + k.
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int j = 0; j < o; ++j) {
+            const float send = upper ? t[j] : t[j + o];
+            const float keep = upper ? t[j + o] : t[j];
+            t[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        const int slab_warp = c.mb * 4 + (c.row >> 5);
+        if (n0 + lane < c.N) p.gpart[static_cast<size_t>(slab_warp) * c.N + n0 + lane] = t[0];
       }
     }
   }

@@ -6,9 +6,11 @@
 // epilogue that works on the output tile while it is still on chip).
 //
 //   C[M, N] = A[M, K] @ B[K, N], bf16 operands, fp32 accumulation in TMEM.
-//   A is K-major (row-major [M, K]).  B is either MN-major (row-major [K, N],
-//   i.e. a weight stored [in, out]) or K-major (row-major [N, K], i.e. the
-//   transpose of a weight stored [in, out]).
+//   A is K-major (row-major [M, K], activations) or MN-major (row-major
+//   [K, M], i.e. the transpose of an activation: weight gradients, K = tokens).
+//   B is MN-major (row-major [K, N], i.e. a weight stored [in, out], or an
+//   activation gradient) or K-major (row-major [N, K], i.e. the transpose of
+//   a weight stored [in, out]).
 //
 // Block = 320 threads, one block per SM, persistent over output tiles:
 //   warp 0      TMA producer: 4-stage ring of A (128x64) + B (64x256) tiles,
@@ -93,7 +95,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
   return r != 0;
 }
 
-template <class Epi, bool kBMNMajor>
+template <class Epi, bool kBMNMajor, bool kAMNMajor = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int group_m,
@@ -168,7 +170,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, kStageBytes);
           const uint32_t a_dst = sA + s * kAStageBytes;
           const uint32_t b_dst = sB + s * kBStageBytes;
-          tma_load_2d(a_dst, &tmA, full, kb * kBK, mb * kBM);
+          if constexpr (kAMNMajor) {
+            tma_load_2d(a_dst, &tmA, full, mb * kBM, kb * kBK);
+            tma_load_2d(a_dst + kBChunkBytes, &tmA, full, mb * kBM + 64, kb * kBK);
+          } else {
+            tma_load_2d(a_dst, &tmA, full, kb * kBK, mb * kBM);
+          }
           if constexpr (kBMNMajor) {
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j)
@@ -200,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false, kBMNMajor);
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, kAMNMajor, kBMNMajor);
       int s = 0;
       uint32_t ph = 0;
       uint32_t it = 0;
@@ -224,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = sB + s * kBStageBytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t ad = kAMNMajor ? sdesc_sw128(a0 + k * 2048, kBChunkBytes, 1024)
+                                          : sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = kBMNMajor ? sdesc_sw128(b0 + k * 2048, kBChunkBytes, 1024)
                                           : sdesc_sw128(b0 + k * 32, 16, 1024);
             umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);

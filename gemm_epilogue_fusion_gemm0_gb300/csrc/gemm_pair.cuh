@@ -38,7 +38,7 @@ static_assert(kPairBarBytes + 8 <= 256, "barrier area overflows its reserved 256
 
 static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
-template <class Epi, bool kBMNMajor>
+template <class Epi, bool kBMNMajor, bool kAMNMajor = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
@@ -120,7 +120,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (leader) mbar_arrive_expect_tx(full_local, 2u * kPairStageBytes);
           const uint32_t a_dst = sA + s * kPairAStageBytes;
           const uint32_t b_dst = sB + s * kPairBStageBytes;
-          tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, arow);
+          if constexpr (kAMNMajor) {
+            tma_load_2d_pair(a_dst, &tmA, full_leader, arow, kb * kBK);
+            tma_load_2d_pair(a_dst + kBChunkBytes, &tmA, full_leader, arow + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, arow);
+          }
           if constexpr (kBMNMajor) {
             const int j0 = 2 * static_cast<int>(rank);  // this CTA's two 64-column chunks
             tma_load_2d_pair(b_dst, &tmB, full_leader, Epi::b_col(nb, j0, N), kb * kBK);
@@ -152,7 +157,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (CTA 0 only)
     if (lane == 0) {
       if (leader) {
-        constexpr uint32_t idesc = idesc_bf16_f32(kPairBM, kBN, false, kBMNMajor);
+        constexpr uint32_t idesc = idesc_bf16_f32(kPairBM, kBN, kAMNMajor, kBMNMajor);
         int s = 0;
         uint32_t ph = 0;
         uint32_t it = 0;
@@ -176,7 +181,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t b0 = sB + s * kPairBStageBytes;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = sdesc_sw128(a0 + k * 32, 16, 1024);
+              const uint64_t ad = kAMNMajor ? sdesc_sw128(a0 + k * 2048, kBChunkBytes, 1024)
+                                            : sdesc_sw128(a0 + k * 32, 16, 1024);
               const uint64_t bd = kBMNMajor ? sdesc_sw128(b0 + k * 2048, kBChunkBytes, 1024)
                                             : sdesc_sw128(b0 + k * 32, 16, 1024);
               umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);

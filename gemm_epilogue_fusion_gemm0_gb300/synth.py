@@ -83,6 +83,12 @@ def make_grad_output(rng_or_seed, M: int, N1: int) -> torch.Tensor:
     return to_bf16(_normal(rng, (M, N1), 1e-2))
 
 
+def make_residual_grad(rng, M: int, d: int) -> torch.Tensor:
+    """bf16 CPU tensor dh_res [M, d] ~ N(0, 1e-2): the gradient reaching h
+    through the residual stream; drawn after dy from the same generator."""
+    return to_bf16(_normal(rng, (M, d), 1e-2))
+
+
 def make_down_proj_backward(rng, M: int, N1: int, Dout: int) -> dict:
     """bf16 CPU tensors for the backward through the gated activation and the
     down projection: W2 [N1/2, Dout] ~ N(0, 2/N1) and dout [M, Dout] ~ N(0, 1e-2),

@@ -176,6 +176,38 @@ CODA_API coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_b
                                              float* s_out, coda_bf16* dh_out, void* workspace,
                                              size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * All gradients of the chain h = x @ W0 + z, y = RMSNorm(h, gamma) @ W1 for
+ * one training step, as GEMM-epilogue programs ("CODA：将 Transformer 块重写为
+ * GEMM-Epilogue 程序以消除显存瓶颈", blog.hotdry.top, section
+ * "反向传播的 GEMM-Epilogue 结构": with a GEMM + tile-local-epilogue forward the
+ * backward keeps the same structure, the linear maps staying GEMMs).  Five
+ * launches on `stream`:
+ *   1. grad_h2 = dy @ W1^T; epilogue: the RMSNorm backward of coda_bwd_dgrad,
+ *      plus dh_res (the gradient that reaches h through the residual stream,
+ *      may be NULL), plus h2 = r * h * gamma (stored to the workspace) and
+ *      per-warp column partials of dgamma = sum_m grad_h2 * r * h;
+ *   2. dgamma = column sums of the partials (light auxiliary reduction);
+ *   3. dW1 = h2^T dy          (K = M tokens; operands read transposed by TMA);
+ *   4. dx  = dh @ W0^T;
+ *   5. dW0 = x^T dh           (K = M tokens).
+ *   dy [M, N1] bf16, x [M, d] bf16, W0 [d, d] bf16, W1 [d, N1] bf16,
+ *   h [M, d] bf16 and r [M] fp32 (saved by coda_fwd), gamma [d] bf16,
+ *   dh_res [M, d] bf16 or NULL                                   (inputs)
+ *   dh_out [M, d] bf16 (= dz), dx_out [M, d] bf16, dgamma_out [d] fp32,
+ *   dW0_out [d, d] fp32, dW1_out [d, N1] fp32                    (outputs)
+ *   workspace: at least coda_bwd_workspace_bytes(M, d, N1) bytes.
+ * Launch 1 is cooperative, as in coda_bwd_dgrad.  Conventions as coda_fwd.
+ */
+CODA_API size_t coda_bwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
+CODA_API coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16* W0,
+                                const coda_bf16* W1, const coda_bf16* h, const float* r,
+                                const coda_bf16* gamma, const coda_bf16* dh_res,
+                                int64_t M, int64_t d, int64_t N1,
+                                coda_bf16* dh_out, coda_bf16* dx_out, float* dgamma_out,
+                                float* dW0_out, float* dW1_out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then reports and clears the library's device-side
  * status word: CODA_OK, or CODA_ERR_DEVICE_TIMEOUT if a bounded wait in any
  * kernel of this library ran out since the last call.  If `detail` is not

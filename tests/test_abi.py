@@ -106,6 +106,25 @@ def test_swiglu_argument_validation(lib):
     assert call(y=FAKE + 2) == E["CODA_ERR_MISALIGNED"]
 
 
+def test_full_backward_workspace_and_validation(lib):
+    E = {v: k for k, v in lib.STATUS_NAMES.items()}
+    M, d, N1 = 8192, 4096, 28672
+    # dgrad workspace + h2 [M, d] bf16 + dgamma partials [4 * 64 slabs, d] fp32
+    assert lib.coda_bwd_workspace_bytes(M, d, N1) == (
+        lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) + M * d * 2 + 4 * 64 * d * 4)
+    raw = lib.raw()
+
+    def call(res=0, M=128, wsb=1 << 30, dgamma=FAKE):
+        return raw.coda_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, res, M, 256, 512, FAKE, FAKE,
+                            dgamma, FAKE, FAKE, FAKE, wsb, None)
+
+    assert call(M=-1) == E["CODA_ERR_INVALID_ARG"]
+    assert call(M=0) == E["CODA_OK"]
+    assert call(dgamma=0) == E["CODA_ERR_INVALID_ARG"]
+    assert call(res=FAKE + 4) == E["CODA_ERR_MISALIGNED"]
+    assert call(wsb=64) == E["CODA_ERR_WORKSPACE_TOO_SMALL"]
+
+
 def test_no_device_is_reported_without_gpu(lib):
     import torch
 

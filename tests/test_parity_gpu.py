@@ -278,3 +278,42 @@ def test_swiglu_backward_small(B, mode, M, d, N1, Dout):
 def test_swiglu_backward_llama7b_sampled_rows(B, mode):
     w = synth.WORKLOADS["llama7b"]
     run_swiglu_bwd(B, w.M, w.d, w.N1, w.d, w.eps, rows=synth.sample_rows(w.M, 256, seed=3))
+
+
+# ----------------------------------------------------------------------------- full backward
+def run_full_bwd(B, M, d, N1, eps, seed=0, with_res=True):
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=seed)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    h, r, _ = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps)
+    dy = synth.make_grad_output(t["_rng"], M, N1)
+    res = synth.make_residual_grad(t["_rng"], M, d) if with_res else None
+    o = B.coda_bwd(dy.to(dev), g["x"], g["W0"], g["W1"], h, r, g["gamma"],
+                   None if res is None else res.to(dev))
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    ref = oracle.backward_full(f64(dy), f64(t["x"]), f64(t["W0"]), f64(t["W1"]), f64(h.cpu()),
+                               f64(r.cpu()), f64(t["gamma"]), None if res is None else f64(res))
+    return {"dh": check("dh", f64(o["dh"].cpu()), ref.dh, TOL_DH),
+            "dx": check("dx", f64(o["dx"].cpu()), ref.dx, TOL_DH),
+            "dgamma": check("dgamma", f64(o["dgamma"].cpu())[None, :], ref.dgamma[None, :], TOL_HY),
+            "dW0": check("dW0", f64(o["dW0"].cpu()), ref.dW0, TOL_HY),
+            "dW1": check("dW1", f64(o["dW1"].cpu()), ref.dW1, TOL_HY)}
+
+
+@pytest.mark.parametrize("M,d,N1", [
+    (128, 256, 512),     # tiny
+    (300, 328, 776),     # ragged in every dimension (K = tokens is ragged for the weight grads)
+    (640, 512, 1280),    # several tiles
+])
+def test_full_backward_small(B, mode, M, d, N1):
+    run_full_bwd(B, M, d, N1, 1e-5)
+
+
+def test_full_backward_without_residual_gradient(B, mode):
+    run_full_bwd(B, 300, 328, 776, 1e-5, with_res=False)
+
+
+def test_full_backward_llama7b(B, mode):
+    w = synth.WORKLOADS["llama7b"]
+    run_full_bwd(B, w.M, w.d, w.N1, w.eps)
