@@ -358,6 +358,26 @@ def run_coda(args):
     extras["fwd_swiglu"] = {"ms": sw_ms, "tflops": w.fwd_flops / (sw_ms * 1e-3) / 1e12,
                             "calls": KS, "gpu_launches": 3 * KS,
                             "note": "coda_fwd_swiglu: GEMM1 epilogue applies r and silu(gate)*up"}
+    # F4: the forward with the row reduction folded into GEMM1's epilogue (2 launches)
+    B.coda_set_fold_rowreduce(1)
+    try:
+        for _ in range(3):
+            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                       stream=stream)
+        barrier()
+        s0.record(stream)
+        for _ in range(KS):
+            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                       stream=stream)
+        s1.record(stream)
+        barrier()
+    finally:
+        B.coda_set_fold_rowreduce(0)
+    fo_ms = s0.elapsed_time(s1) / KS
+    extras["fwd_folded_rowreduce"] = {
+        "ms": fo_ms, "tflops": w.fwd_flops / (fo_ms * 1e-3) / 1e12, "calls": KS,
+        "gpu_launches": 2 * KS, "note": "coda_fwd with r formed in GEMM1's epilogue (F4)"}
+
     # backward through the gated activation and the down projection (Dout = d),
     # statistic formed upstream, tile-local RMSNorm-branch data gradient
     y_pre = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)

@@ -63,6 +63,7 @@ EXPORTS = {
     "coda_fwd_swiglu": (_st, [_vp, _vp, _vp, _vp, _vp, _f32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp,
                               _sz, _vp]),
     "coda_get_mma_mode": (ctypes.c_int, []),
+    "coda_set_fold_rowreduce": (_st, [ctypes.c_int]),
 }
 
 for _name, (_res, _args) in EXPORTS.items():
@@ -274,6 +275,11 @@ def coda_get_device_status(stream=None) -> tuple[int, int]:
 def coda_set_mma_mode(mode: int) -> None:
     """0: single-CTA 128x256 tiles; 1: CTA-pair 256x256 tiles (tcgen05 cta_group::2)."""
     _check(_lib.coda_set_mma_mode(int(mode)), "coda_set_mma_mode")
+
+
+def coda_set_fold_rowreduce(enable: int) -> None:
+    """1: r is formed in GEMM1's epilogue (2 launches); 0: separate reduction (default)."""
+    _check(_lib.coda_set_fold_rowreduce(int(enable)), "coda_set_fold_rowreduce")
 
 
 def coda_get_mma_mode() -> int:

@@ -160,6 +160,7 @@ std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_fold_rowreduce{0};  // 1: r computed in GEMM1's epilogue (no separate launch)
 std::atomic<int> g_mma_mode{1};  // 0: single-CTA 128x256 tiles, 1: CTA-pair 256x256 tiles (default)
 std::atomic<uint64_t> g_token_ctr{0};
 uint64_t g_token_salt = 0;
@@ -384,7 +385,15 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     return CODA_ERR_LAUNCH;
   }
   after_launch(0, stream);
-  if (fused) {
+  int k_launch = 1;
+  FoldedRowReduce fold = {};
+  if (fused && g_fold_rowreduce.load() == 1) {
+    fold.part = ws.part;
+    fold.n_part = 2 * nt0;
+    fold.d = di;
+    fold.eps = eps;
+    fold.r_out = r_out;
+  } else if (fused) {
     e = launch(rowreduce_rsqrt_kernel, static_cast<int>(cdiv(M, 256)), 256, 0, stream, false,
                static_cast<const float*>(ws.part), 2 * nt0, Mi, di, eps, r_out);
   } else {
@@ -395,10 +404,11 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
   }
-  after_launch(1, stream);
+  if (fold.part == nullptr) after_launch(k_launch++, stream);
   if (swiglu) {
     EpiRowScaleSwiGLU::Params ps = {};
     ps.r = r_out;
+    ps.fold = fold;
     ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
     e = pair ? launch(kPairGemm1Swiglu, 2 * std::min(max_pairs, mtp * nt1), kThreads,
@@ -408,6 +418,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   } else {
     EpiRowScale::Params p1 = {};
     p1.r = fused ? r_out : nullptr;
+    p1.fold = fold;
     p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
                       stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
@@ -418,7 +429,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
   }
-  after_launch(2, stream);
+  after_launch(k_launch, stream);
   return CODA_OK;
 }
 
@@ -788,6 +799,12 @@ coda_status_t coda_set_mma_mode(int mode) {
 }
 
 int coda_get_mma_mode(void) { return g_mma_mode.load(); }
+
+coda_status_t coda_set_fold_rowreduce(int enable) {
+  if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
+  g_fold_rowreduce.store(enable);
+  return CODA_OK;
+}
 
 void coda_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1 : ns); }
 

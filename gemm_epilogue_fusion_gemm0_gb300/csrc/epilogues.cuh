@@ -49,6 +49,23 @@ __device__ __forceinline__ void ldg_chunk(const __nv_bfloat16* rowp, int n0, int
   }
 }
 
+// r[m] = rsqrt(sum of the row's h^2 partials / d + eps), summed in the same
+// order and with the same expression as the stand-alone row-reduction kernel,
+// so the folded and the separate forms give bit-identical r.
+struct FoldedRowReduce {
+  const float* part;  // [n_part][M] partial sums of h^2; null: r is read from `r`
+  int n_part;
+  int d;
+  float eps;
+  float* r_out;       // written by the tiles of column block 0
+};
+
+__device__ __forceinline__ float folded_rsqrt(const FoldedRowReduce& f, int m, int M) {
+  float s = 0.f;
+  for (int t = 0; t < f.n_part; ++t) s += __ldcg(f.part + static_cast<size_t>(t) * M + m);
+  return rsqrtf(s / static_cast<float>(f.d) + f.eps);
+}
+
 constexpr int kHalfCols = kBN / 2;        // accumulator columns per epilogue thread
 constexpr int kHalfChunks = kHalfCols / 32;
 
@@ -165,13 +182,20 @@ struct EpiRowScale : EpiDefaultCols {
   struct Params {
     const float* r;  // [M], may be null (scale 1)
     __nv_bfloat16* y_out;
+    FoldedRowReduce fold;  // fold.part != null: r computed here from the partials
   };
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
-    const float rr = (row_ok && p.r != nullptr) ? __ldg(p.r + m) : 1.f;
+    float rr = 1.f;
+    if (row_ok && p.fold.part != nullptr) {
+      rr = folded_rsqrt(p.fold, m, c.M);
+      if (c.nb == 0 && c.half == 0) p.fold.r_out[m] = rr;
+    } else if (row_ok && p.r != nullptr) {
+      rr = __ldg(p.r + m);
+    }
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
@@ -358,6 +382,7 @@ struct EpiRowScaleSwiGLU {
     const float* r;         // [M]
     __nv_bfloat16* y_out;   // [M, N1] pre-activation, may be null
     __nv_bfloat16* a_out;   // [M, N1 / 2]
+    FoldedRowReduce fold;   // fold.part != null: r computed here from the partials
   };
 
   static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N / 2 + 127) / 128; }
@@ -369,7 +394,13 @@ struct EpiRowScaleSwiGLU {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const int half = c.N / 2;
-    const float rr = row_ok ? __ldg(p.r + m) : 0.f;
+    float rr = 0.f;
+    if (row_ok && p.fold.part != nullptr) {
+      rr = folded_rsqrt(p.fold, m, c.M);
+      if (c.nb == 0 && c.half == 0) p.fold.r_out[m] = rr;
+    } else if (row_ok) {
+      rr = __ldg(p.r + m);
+    }
     const size_t a_row = static_cast<size_t>(row_ok ? m : 0) * half;
     const size_t y_row = static_cast<size_t>(row_ok ? m : 0) * c.N;
 #pragma unroll 1

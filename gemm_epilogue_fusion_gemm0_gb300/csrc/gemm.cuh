@@ -52,6 +52,11 @@ constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;  // barriers + 1 KB align
 
 static_assert(kBarBytes + 8 <= 256, "barrier area overflows its reserved 256 bytes");
 
+// Serpentine K order: on odd waves of a block's persistent tile loop the
+// producer walks K backwards, so the next wave starts on the K slices that
+// the previous wave left in L2 (the MMA order follows the producer's).
+constexpr bool kSerpentineK = false;
+
 static_assert(kBK * 2 == 128, "one K tile row must be exactly one 128-byte swizzle row");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
@@ -158,10 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued_mask = 0, last_par = 0;  // per stage: issued?, parity of last issue
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      uint32_t wave = 0;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++wave) {
         int mb, nb;
         tmap.coords(t, mb, nb);
-        for (int kb = 0; kb < nk; ++kb) {
+        const bool reverse = kSerpentineK && (wave & 1u);
+        for (int kbi = 0; kbi < nk; ++kbi) {
+          const int kb = reverse ? nk - 1 - kbi : kbi;
           if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;

@@ -105,12 +105,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued_mask = 0, last_par = 0;
       bool ok = true;
-      for (int t = pair; ok && t < num_tiles; t += npairs) {
+      uint32_t wave = 0;
+      for (int t = pair; ok && t < num_tiles; t += npairs, ++wave) {
         int mb, nb;
         tmap.coords(t, mb, nb);
         const int arow = mb * kPairBM + static_cast<int>(rank) * 128;
         const int bcol = nb * kBN + static_cast<int>(rank) * 128;  // K-major B rows
-        for (int kb = 0; kb < nk; ++kb) {
+        const bool reverse = kSerpentineK && (wave & 1u);
+        for (int kbi = 0; kbi < nk; ++kbi) {
+          const int kb = reverse ? nk - 1 - kbi : kbi;
           if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;

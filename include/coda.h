@@ -224,6 +224,14 @@ CODA_API coda_status_t coda_get_device_status(cudaStream_t stream, uint32_t* det
 CODA_API coda_status_t coda_set_mma_mode(int mode);
 CODA_API int coda_get_mma_mode(void);
 
+/* Forward variant: 1 folds the row reduction (step 2) into GEMM1's epilogue,
+ * which then forms r from the partial sums itself (each tile of column block
+ * 0 also stores it), so coda_fwd and coda_fwd_swiglu launch 2 kernels instead
+ * of 3.  r is bit-identical either way (same summation order and arithmetic).
+ * 0 (the default) keeps the separate light auxiliary reduction.  Returns
+ * CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
+CODA_API coda_status_t coda_set_fold_rowreduce(int enable);
+
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records
  * CODA_ERR_DEVICE_TIMEOUT and lets its kernel finish without hanging. */

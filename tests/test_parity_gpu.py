@@ -317,3 +317,29 @@ def test_full_backward_without_residual_gradient(B, mode):
 def test_full_backward_llama7b(B, mode):
     w = synth.WORKLOADS["llama7b"]
     run_full_bwd(B, w.M, w.d, w.N1, w.eps)
+
+
+# ----------------------------------------------------------------------------- folded row reduction (F4)
+@pytest.mark.parametrize("M,d,N1", [(300, 328, 784), (640, 512, 1536)])
+def test_folded_rowreduce_is_bit_identical(B, mode, M, d, N1):
+    """r formed in GEMM1's epilogue equals the separate reduction bit for bit,
+    so h, r, y and the SwiGLU output are identical; and both match the oracle."""
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=9)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    args = (g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5)
+    try:
+        base = B.coda_fwd(*args)
+        base_sw = B.coda_fwd_swiglu(*args, want_y=True)
+        B.coda_set_fold_rowreduce(1)
+        fold = B.coda_fwd(*args)
+        fold_sw = B.coda_fwd_swiglu(*args, want_y=True)
+    finally:
+        B.coda_set_fold_rowreduce(0)
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    for a, b in zip(base + base_sw, fold + fold_sw):
+        assert torch.equal(a, b)
+    ref = oracle.forward(f64(t["x"]), f64(t["W0"]), f64(t["z"]), f64(t["gamma"]), f64(t["W1"]), 1e-5)
+    check("y", f64(fold[2]), ref.y, TOL_HY)
+    check_r(f64(fold[1]), ref.r)
