@@ -119,17 +119,6 @@ __global__ void watchdog_selftest_kernel(uint64_t timeout_ns) {
   flag_wait(&g_selftest_flag, 1ull, wc, kSiteSelftestFlag);  // nobody sets it
 }
 
-template <class Epi>
-constexpr uint32_t SmemOfSingle = SingleLayout<Epi>::kBytes;
-template <class Epi>
-constexpr uint32_t SmemOfPair = PairLayout<Epi>::kBytes;
-
-template <class K>
-bool set_smem(K kernel, uint32_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(bytes)) == cudaSuccess;
-}
-
 static auto* const kGemm0 = &gemm_epilogue_kernel<EpiResidualGammaSumsq, true>;
 static auto* const kGemm1 = &gemm_epilogue_kernel<EpiRowScale, true>;
 static auto* const kDgrad = &gemm_epilogue_kernel<EpiRmsNormBackward, false>;
@@ -209,27 +198,43 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
       s.status = CODA_ERR_UNSUPPORTED_DEVICE;
     } else {
       bool ok = true;
-      ok &= set_smem(kGemm0, SmemOfSingle<EpiResidualGammaSumsq>);
-      ok &= set_smem(kPairGemm0, SmemOfPair<EpiResidualGammaSumsq>);
-      ok &= set_smem(kGemm1, SmemOfSingle<EpiRowScale>);
-      ok &= set_smem(kPairGemm1, SmemOfPair<EpiRowScale>);
-      ok &= set_smem(kGemm1Swiglu, SmemOfSingle<EpiRowScaleSwiGLU>);
-      ok &= set_smem(kPairGemm1Swiglu, SmemOfPair<EpiRowScaleSwiGLU>);
-      ok &= set_smem(kDgrad, SmemOfSingle<EpiRmsNormBackward>);
-      ok &= set_smem(kPairDgrad, SmemOfPair<EpiRmsNormBackward>);
-      ok &= set_smem(kWgrad, SmemOfSingle<EpiStoreF32>);
-      ok &= set_smem(kPairWgrad, SmemOfPair<EpiStoreF32>);
-      ok &= set_smem(kXgrad, SmemOfSingle<EpiRowScale>);
-      ok &= set_smem(kPairXgrad, SmemOfPair<EpiRowScale>);
-      ok &= set_smem(kSwigluBwd, SmemOfSingle<EpiSwiGLUBackward>);
-      ok &= set_smem(kPairSwigluBwd, SmemOfPair<EpiSwiGLUBackward>);
-      ok &= set_smem(kDgradGivenS, SmemOfSingle<EpiRmsNormBackwardGivenS>);
-      ok &= set_smem(kPairDgradGivenS, SmemOfPair<EpiRmsNormBackwardGivenS>);
+      ok &= cudaFuncSetAttribute(kGemm0, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kGemm1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm0, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
       if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (count / 2));
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = SmemOfPair<EpiRmsNormBackward>;
+        cfg.dynamicSmemBytes = kPairSmemBytes;
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, kPairDgrad, &cfg) == cudaSuccess)
           s.max_pairs = std::min(clusters, count / 2);
@@ -265,16 +270,15 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
   return s.status;
 }
 
-// 2-D bf16 tensor map over a row-major [outer, inner] matrix (128-byte swizzle
-// for MMA operand tiles; 64-byte swizzle for the epilogue's 32 x 32 boxes).
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix, 128-byte swizzle.
 bool tmap_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-             uint32_t box_outer, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+             uint32_t box_outer) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -365,16 +369,16 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   const uint64_t tmo = g_timeout_ns.load();
 
   EpiResidualGammaSumsq::Params p0 = {};
-  if (!tmap_2d(&p0.z_map, z, d, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CODA_ERR_LAUNCH;
+  p0.z = reinterpret_cast<const __nv_bfloat16*>(z);
   p0.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p0.h_out = reinterpret_cast<__nv_bfloat16*>(h_out);
   p0.hg_out = fused ? ws.act : nullptr;
   p0.part = ws.part;
   const int mtp = static_cast<int>(cdiv(M, kPairBM));
   cudaError_t e =
-      pair ? launch(kPairGemm0, 2 * std::min(max_pairs, mtp * nt0), kThreads, SmemOfPair<EpiResidualGammaSumsq>,
+      pair ? launch(kPairGemm0, 2 * std::min(max_pairs, mtp * nt0), kThreads, kPairSmemBytes,
                     stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, tmo)
-           : launch(kGemm0, std::min(sms, mt * nt0), kThreads, SmemOfSingle<EpiResidualGammaSumsq>, stream, false, mA0,
+           : launch(kGemm0, std::min(sms, mt * nt0), kThreads, kSmemBytes, stream, false, mA0,
                     mB0, Mi, di, di, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -408,17 +412,17 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
     e = pair ? launch(kPairGemm1Swiglu, 2 * std::min(max_pairs, mtp * nt1), kThreads,
-                      SmemOfPair<EpiRowScaleSwiGLU>, stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, tmo)
-             : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, SmemOfSingle<EpiRowScaleSwiGLU>, stream, false,
+                      kPairSmemBytes, stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, tmo)
+             : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false,
                       mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
   } else {
     EpiRowScale::Params p1 = {};
     p1.r = fused ? r_out : nullptr;
     p1.fold = fold;
     p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
-    e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, SmemOfPair<EpiRowScale>,
+    e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
                       stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
-             : launch(kGemm1, std::min(sms, mt * nt1), kThreads, SmemOfSingle<EpiRowScale>, stream, false, mA1,
+             : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false, mA1,
                       mB1, Mi, N1i, di, kGroupM, p1, tmo);
   }
   if (e != cudaSuccess) {
@@ -520,10 +524,10 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   if (tok == 0) tok = 1;
   p.token = tok;
   cudaError_t e =
-      pair ? launch(kPairDgrad, 2 * units, kThreads, SmemOfPair<EpiRmsNormBackward>, stream, true, mA, mB,
+      pair ? launch(kPairDgrad, 2 * units, kThreads, kPairSmemBytes, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                     g_timeout_ns.load())
-           : launch(kDgrad, units, kThreads, SmemOfSingle<EpiRmsNormBackward>, stream, true, mA, mB,
+           : launch(kDgrad, units, kThreads, kSmemBytes, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                     g_timeout_ns.load());
   if (e != cudaSuccess) {
@@ -606,9 +610,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
-  cudaError_t e = pair ? launch(kPairDgrad, 2 * units, kThreads, SmemOfPair<EpiRmsNormBackward>, stream, true,
+  cudaError_t e = pair ? launch(kPairDgrad, 2 * units, kThreads, kPairSmemBytes, stream, true,
                                 mDy, mW1, Mi, di, N1i, 1, p, tmo)
-                       : launch(kDgrad, units, kThreads, SmemOfSingle<EpiRmsNormBackward>, stream, true, mDy, mW1, Mi,
+                       : launch(kDgrad, units, kThreads, kSmemBytes, stream, true, mDy, mW1, Mi,
                                 di, N1i, 1, p, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -628,9 +632,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   pw1.out = dW1_out;
   const int mtw = static_cast<int>(cdiv(d, pair ? kPairBM : kBM));
   const int ntw1 = static_cast<int>(cdiv(N1, kBN));
-  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, SmemOfPair<EpiStoreF32>,
+  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, kPairSmemBytes,
                     stream, false, mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, tmo)
-           : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, SmemOfSingle<EpiStoreF32>, stream, false, mH2,
+           : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kSmemBytes, stream, false, mH2,
                     mDyMN, di, N1i, Mi, kGroupM, pw1, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -642,9 +646,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   px.r = nullptr;
   px.y_out = reinterpret_cast<__nv_bfloat16*>(dx_out);
   const int mtx = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
-  e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, SmemOfPair<EpiRowScale>,
+  e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, kPairSmemBytes,
                     stream, false, mDh, mW0, Mi, di, di, kPairGroupM, px, tmo)
-           : launch(kXgrad, std::min(sms, mtx * nt), kThreads, SmemOfSingle<EpiRowScale>, stream, false, mDh,
+           : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kSmemBytes, stream, false, mDh,
                     mW0, Mi, di, di, kGroupM, px, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -654,9 +658,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   // 5. dW0 = x^T dh   (K = tokens)
   EpiStoreF32::Params pw0 = {};
   pw0.out = dW0_out;
-  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, SmemOfPair<EpiStoreF32>,
+  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, kPairSmemBytes,
                     stream, false, mX, mDhMN, di, di, Mi, kPairGroupM, pw0, tmo)
-           : launch(kWgrad, std::min(sms, mtw * nt), kThreads, SmemOfSingle<EpiStoreF32>, stream, false, mX,
+           : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kSmemBytes, stream, false, mX,
                     mDhMN, di, di, Mi, kGroupM, pw0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -716,13 +720,13 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
 
   // 1. down-projection data gradient with the SwiGLU backward + partial s
   EpiSwiGLUBackward::Params p0 = {};
-  if (!tmap_2d(&p0.y_map, y, N1, M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) return CODA_ERR_LAUNCH;
+  p0.y = reinterpret_cast<const __nv_bfloat16*>(y);
   p0.dy_out = reinterpret_cast<__nv_bfloat16*>(dy_out);
   p0.spart = reinterpret_cast<float*>(workspace);
   cudaError_t e =
-      pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads, SmemOfPair<EpiSwiGLUBackward>,
+      pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads, kPairSmemBytes,
                     stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM, p0, tmo)
-           : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, SmemOfSingle<EpiSwiGLUBackward>, stream, false, mA0,
+           : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, kSmemBytes, stream, false, mA0,
                     mB0, Mi, halfi, Douti, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -744,9 +748,9 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   p1.r = r;
   p1.s = s_out;
   p1.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
-  e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads, SmemOfPair<EpiRmsNormBackwardGivenS>,
+  e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads, kPairSmemBytes,
                     stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, tmo)
-           : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, SmemOfSingle<EpiRmsNormBackwardGivenS>, stream, false,
+           : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kSmemBytes, stream, false,
                     mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -927,7 +931,7 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
   uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
   if (tok == 0) tok = 1;
   p.token = tok;
-  cudaError_t e = launch(kDgrad, grid, kThreads, SmemOfSingle<EpiRmsNormBackward>, stream, true, mA, mB,
+  cudaError_t e = launch(kDgrad, grid, kThreads, kSmemBytes, stream, true, mA, mB,
                          static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                          g_timeout_ns.load());
   if (e != cudaSuccess) {

@@ -27,7 +27,6 @@ struct Chunk8 {
 // output, and where the producer fetches the j-th 64-column chunk (j = 0..3)
 // of an MN-major B tile.  The default is the plain contiguous tiling.
 struct EpiDefaultCols {
-  static constexpr uint32_t kEpiSmemPerWarp = 0;  // no epilogue shared memory
   static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N + kBN - 1) / kBN; }
   static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
 };
@@ -67,49 +66,6 @@ __device__ __forceinline__ float folded_rsqrt(const FoldedRowReduce& f, int m, i
   return rsqrtf(s / static_cast<float>(f.d) + f.eps);
 }
 
-// Per-warp TMA stream of the epilogue's rank-2 operand tiles.  Each epilogue
-// warp owns 32 rows x 128 columns of the accumulator tile and walks them in
-// 32-column chunks; for chunk k its lane 0 loads the matching 32 x 32 bf16 box
-// of each operand (64-byte rows, 64-byte swizzle) into buffer k & 1, completing
-// on that buffer's mbarrier, one chunk ahead of the arithmetic.  A thread then
-// reads its own row (4 x 16 bytes) from shared memory: with the 64-byte swizzle
-// the 16-byte group c of row r sits at r * 64 + ((c ^ ((r >> 1) & 3)) * 16),
-// which spreads every 8 consecutive rows over all 32 banks.
-constexpr uint32_t kEpiBox = 32 * 32 * 2;  // one 32 x 32 bf16 box: 2 KB
-
-template <int kOps>
-struct EpiTmaStream {
-  // buffer b of operand o: es.smem + (b * kOps + o) * kEpiBox; barrier b: es.bar + 8 b
-  static __device__ __forceinline__ void issue(const EpiState& es, uint32_t iter,
-                                               const CUtensorMap* const (&maps)[kOps],
-                                               const int (&x)[kOps], int y) {
-    if ((threadIdx.x & 31) == 0) {
-      const uint32_t b = iter & 1u;
-      const uint32_t bar = es.bar + 8u * b;
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, kOps * kEpiBox);
-#pragma unroll
-      for (int o = 0; o < kOps; ++o)
-        tma_load_2d(es.smem + (b * kOps + o) * kEpiBox, maps[o], bar, x[o], y);
-    }
-  }
-  static __device__ __forceinline__ bool wait(const EpiState& es, uint32_t iter,
-                                              const WaitCtl& wc) {
-    return bounded_wait(es.bar + 8u * (iter & 1u), (iter >> 1) & 1u, wc, kSiteEpiOperand);
-  }
-  // this thread's 32 bf16 of operand o in the chunk held by buffer iter & 1
-  static __device__ __forceinline__ void read_row(const EpiState& es, uint32_t iter, int o,
-                                                  Chunk8 (&out)[4]) {
-    const int r = threadIdx.x & 31;
-    const uint32_t row = es.smem + ((iter & 1u) * kOps + o) * kEpiBox + r * 64;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = ld_shared_v4(row + ((c ^ ((r >> 1) & 3)) * 16));
-      out[c] = Chunk8{{v.x, v.y, v.z, v.w}};
-    }
-  }
-};
-
 constexpr int kHalfCols = kBN / 2;        // accumulator columns per epilogue thread
 constexpr int kHalfChunks = kHalfCols / 32;
 
@@ -137,56 +93,39 @@ __device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
 // epilogue of the unfused reference sequence.
 // ---------------------------------------------------------------------------
 struct EpiResidualGammaSumsq : EpiDefaultCols {
-  static constexpr uint32_t kEpiSmemPerWarp = 2 * kEpiBox;  // z chunks, double-buffered
   struct Params {
-    CUtensorMap z_map;  // z [M, d], 32 x 32 boxes, 64-byte swizzle
+    const __nv_bfloat16* z;
     const __nv_bfloat16* gamma;
     __nv_bfloat16* h_out;
     __nv_bfloat16* hg_out;  // may be null (unfused sequence)
     float* part;            // [2 * nt][M], may be null (unfused sequence)
   };
 
-  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
-                                               const TileCtx& c, EpiState& es) {
-    using S = EpiTmaStream<1>;
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
     const bool fused = p.hg_out != nullptr;
-    const int wrow0 = c.mb * kBM + (c.row & ~31);  // first row of this warp's 32
-    const int nbase = c.nb * kBN + c.half * kHalfCols;
-    const CUtensorMap* const maps[1] = {&p.z_map};
     float ss = 0.f;
-    __syncwarp();
-    {
-      const int x[1] = {nbase};
-      S::issue(es, es.iter, maps, x, wrow0);
-    }
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
-      if (ch + 1 < kHalfChunks) {
-        const int x[1] = {n0 + 32};
-        S::issue(es, es.iter + 1, maps, x, wrow0);
-      }
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
-      S::wait(es, es.iter, wc);
       tmem_ld_wait(v);
-      Chunk8 zc[4];
-      S::read_row(es, es.iter, 0, zc);
       if (row_ok) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int n = n0 + g * 8;
           if (n < c.N) {
+            const Chunk8 zz = ldg8(p.z + rowoff + n);
             const Chunk8 gg = ldg8(p.gamma + n);
             uint32_t hw[4], hgw[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zc[g].w[e]);
-              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zc[g].w[e]);
+              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zz.w[e]);
+              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zz.w[e]);
               ss = fmaf(h0, h0, ss);
               ss = fmaf(h1, h1, ss);
               hw[e] = pack_bf16x2(h0, h1);
@@ -197,8 +136,6 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
           }
         }
       }
-      __syncwarp();  // every lane is done with this buffer before it is refilled
-      ++es.iter;
     }
     if (row_ok && p.part != nullptr) p.part[partial_index(c, m)] = ss;
   }
@@ -212,8 +149,7 @@ struct EpiStoreF32 : EpiDefaultCols {
     float* out;  // [M, N] row-major
   };
 
-  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c,
-                                               EpiState&) {
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
@@ -249,8 +185,7 @@ struct EpiRowScale : EpiDefaultCols {
     FoldedRowReduce fold;  // fold.part != null: r computed here from the partials
   };
 
-  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c,
-                                               EpiState&) {
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
@@ -315,7 +250,7 @@ struct EpiRmsNormBackward : EpiDefaultCols {
   };
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
-                                               const TileCtx& c, EpiState&) {
+                                               const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
@@ -450,14 +385,12 @@ struct EpiRowScaleSwiGLU {
     FoldedRowReduce fold;   // fold.part != null: r computed here from the partials
   };
 
-  static constexpr uint32_t kEpiSmemPerWarp = 0;
   static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N / 2 + 127) / 128; }
   static __device__ __forceinline__ int b_col(int nb, int j, int N) {
     return (j < 2 ? 0 : N / 2) + nb * 128 + 64 * (j & 1);
   }
 
-  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c,
-                                               EpiState&) {
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const int half = c.N / 2;
@@ -518,44 +451,36 @@ struct EpiRowScaleSwiGLU {
 //   spart[2 nb + half][m] = sum over the half tile of dg * g + du * u   (fp32)
 // ---------------------------------------------------------------------------
 struct EpiSwiGLUBackward : EpiDefaultCols {
-  static constexpr uint32_t kEpiSmemPerWarp = 2 * 2 * kEpiBox;  // g and u chunks, double-buffered
   struct Params {
-    CUtensorMap y_map;       // y [M, 2 * half], 32 x 32 boxes, 64-byte swizzle
+    const __nv_bfloat16* y;  // [M, 2 * half] saved pre-activation [g | u]
     __nv_bfloat16* dy_out;   // [M, 2 * half]
     float* spart;            // [2 * nt][M]
   };
 
-  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
-                                               const TileCtx& c, EpiState& es) {
-    using S = EpiTmaStream<2>;
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const int half = c.N;  // the GEMM's output width is the gated width
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * (2 * static_cast<size_t>(half));
-    const int wrow0 = c.mb * kBM + (c.row & ~31);
+    const __nv_bfloat16* grow = p.y + rowoff;
+    const __nv_bfloat16* urow = p.y + rowoff + half;
     const int jbase = c.nb * kBN + c.half * kHalfCols;
-    const CUtensorMap* const maps[2] = {&p.y_map, &p.y_map};
     float ss = 0.f;
-    __syncwarp();
-    {
-      const int x[2] = {jbase, half + jbase};
-      S::issue(es, es.iter, maps, x, wrow0);
-    }
-#pragma unroll 1
+    Chunk8 gc[4], uc[4];
+    ldg_chunk(grow, jbase, half, row_ok, gc);
+    ldg_chunk(urow, jbase, half, row_ok, uc);
+#pragma unroll
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int j0 = c.nb * kBN + col;
-      if (ch + 1 < kHalfChunks) {
-        const int x[2] = {j0 + 32, half + j0 + 32};
-        S::issue(es, es.iter + 1, maps, x, wrow0);
-      }
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
-      S::wait(es, es.iter, wc);
+      Chunk8 gn[4], un[4];
+      if (ch + 1 < kHalfChunks) {
+        ldg_chunk(grow, j0 + 32, half, row_ok, gn);
+        ldg_chunk(urow, j0 + 32, half, row_ok, un);
+      }
       tmem_ld_wait(v);
-      Chunk8 gc[4], uc[4];
-      S::read_row(es, es.iter, 0, gc);
-      S::read_row(es, es.iter, 1, uc);
       if (row_ok) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -584,8 +509,13 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
           }
         }
       }
-      __syncwarp();
-      ++es.iter;
+      if (ch + 1 < kHalfChunks) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          gc[q] = gn[q];
+          uc[q] = un[q];
+        }
+      }
     }
     if (row_ok) p.spart[partial_index(c, m)] = ss;
   }
@@ -605,8 +535,7 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
     __nv_bfloat16* dh_out;
   };
 
-  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c,
-                                               EpiState&) {
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
     const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;

@@ -33,49 +33,24 @@ __device__ uint32_t g_coda_status = 0;  // device status word (see WaitSite)
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
+constexpr int kStages = 4;
 constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr int kEpiThreads = 256;
-constexpr int kEpiWarps = 8;
 constexpr int kEpiFirstThread = 64;
 constexpr uint32_t kAStageBytes = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kBStageBytes = kBN * kBK * 2;   // 32 KB
 constexpr uint32_t kBChunkBytes = 64 * kBK * 2;    // one 64-column MN-major chunk: 8 KB
+constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;
-constexpr uint32_t kSmemBudget = 232448;           // 227 KB per block
-constexpr uint32_t kBarArea = 512;                 // barriers, TMEM-address holder, abort flag
+constexpr uint32_t kSmemA = 0;
+constexpr uint32_t kSmemB = kStages * kAStageBytes;
+constexpr uint32_t kSmemBar = kSmemB + kStages * kBStageBytes;
+// barriers: full[S] | empty[S] | tfull[2] | tempty[2] | drain, then the TMEM
+// address holder and the abort flag right after them
+constexpr uint32_t kBarBytes = 8u * (2 * kStages + 5);
+constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;  // barriers + 1 KB alignment slack
 
-// Shared-memory layout of one block, per epilogue policy: the operand ring
-// (as many stages as fit, up to kMaxStages), then the epilogue's own buffers
-// (kEpiPerWarp bytes for each of the 8 epilogue warps), then the barriers:
-//   full[S] | empty[S] | tfull[2] | tempty[2] | drain | epi[2 per epilogue warp]
-// followed by the TMEM-address holder and the abort flag.
-template <uint32_t kAStage, uint32_t kBStage, int kMaxStages, uint32_t kEpiPerWarp>
-struct SmemLayout {
-  static constexpr uint32_t kEpiBytes = kEpiPerWarp * kEpiWarps;
-  static constexpr int kFit =
-      static_cast<int>((kSmemBudget - 1024 - kBarArea - kEpiBytes) / (kAStage + kBStage));
-  static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
-  static constexpr uint32_t kA = 0;
-  static constexpr uint32_t kB = kStages * kAStage;
-  static constexpr uint32_t kEpi = kB + kStages * kBStage;
-  static constexpr uint32_t kBar = kEpi + kEpiBytes;
-  static constexpr int kEpiBars = kEpiPerWarp ? 2 * kEpiWarps : 0;
-  static constexpr uint32_t kBarBytes = 8u * (2 * kStages + 5 + kEpiBars);
-  static constexpr uint32_t kBytes = kBar + kBarArea + 1024;  // + 1 KB alignment slack
-  static_assert(kStages >= 2, "the operand ring needs at least two stages");
-  static_assert(kBarBytes + 8 <= kBarArea, "barrier area overflows its reserved bytes");
-  static_assert(kBytes <= kSmemBudget, "exceeds the 227 KB per-block shared memory limit");
-};
-
-template <class Epi>
-using SingleLayout = SmemLayout<kAStageBytes, kBStageBytes, 4, Epi::kEpiSmemPerWarp>;
-
-// Per-thread epilogue state that persists across the tiles of a block.
-struct EpiState {
-  uint32_t smem;  // shared address of this warp's epilogue buffers
-  uint32_t bar;   // this warp's two epilogue mbarriers (8 bytes apart)
-  uint32_t iter;  // chunks this warp has streamed through its buffers so far
-};
+static_assert(kBarBytes + 8 <= 256, "barrier area overflows its reserved 256 bytes");
 
 // Serpentine K order: on odd waves of a block's persistent tile loop the
 // producer walks K backwards, so the next wave starts on the K slices that
@@ -83,6 +58,7 @@ struct EpiState {
 constexpr bool kSerpentineK = false;
 
 static_assert(kBK * 2 == 128, "one K tile row must be exactly one 128-byte swizzle row");
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
 // Tile order.  Tiles are visited in groups of `group_m` row blocks; inside a
 // group the row block varies fastest, so the blocks working at the same time
@@ -128,27 +104,24 @@ template <class Epi, bool kBMNMajor, bool kAMNMajor = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, int M, int N, int K, int group_m,
-                         const __grid_constant__ typename Epi::Params ep, uint64_t timeout_ns) {
-  using L = SingleLayout<Epi>;
-  constexpr int kStages = L::kStages;
-  constexpr uint32_t kStageBytes = kAStageBytes + kBStageBytes;
+                         const typename Epi::Params ep, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
   uint8_t* smem = smem_raw + (base - raw);
 
-  const uint32_t sA = base + L::kA;
-  const uint32_t sB = base + L::kB;
-  const uint32_t bar0 = base + L::kBar;
+  const uint32_t sA = base + kSmemA;
+  const uint32_t sB = base + kSmemB;
+  const uint32_t bar0 = base + kSmemBar;
+  // barrier layout: full[kStages] | empty[kStages] | tfull[2] | tempty[2] | drain
   const uint32_t bar_full = bar0;
   const uint32_t bar_empty = bar0 + 8u * kStages;
   const uint32_t bar_tfull = bar0 + 16u * kStages;
   const uint32_t bar_tempty = bar_tfull + 16u;
   const uint32_t bar_drain = bar_tempty + 16u;
-  const uint32_t bar_epi = bar_drain + 8u;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kBar + L::kBarBytes);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kSmemBar + kBarBytes);
   volatile uint32_t* abort_flag =
-      reinterpret_cast<volatile uint32_t*>(smem + L::kBar + L::kBarBytes + 4);
+      reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + kBarBytes + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -170,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty + 8u * b, kEpiThreads);
     }
     mbar_init(bar_drain, 1);
-    for (int i = 0; i < L::kEpiBars; ++i) mbar_init(bar_epi + 8u * i, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -300,10 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;         // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;  // warps 2..5: columns 0..127, warps 6..9: 128..255
     const int row = quad * 32 + lane;
-    EpiState es;
-    es.smem = base + L::kEpi + static_cast<uint32_t>(warp - 2) * Epi::kEpiSmemPerWarp;
-    es.bar = bar_epi + static_cast<uint32_t>(warp - 2) * 16u;
-    es.iter = 0;
     uint32_t it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const uint32_t b = it & 1u;
@@ -322,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.M = M;
       c.N = N;
       c.nt = nt;
-      Epi::apply(ep, wc, c, es);
+      Epi::apply(ep, wc, c);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8u * b);
     }

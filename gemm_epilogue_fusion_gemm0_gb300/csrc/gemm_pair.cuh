@@ -22,39 +22,44 @@
 namespace coda {
 
 constexpr int kPairBM = 256;                         // tile rows per CTA pair
+constexpr int kPairStages = 6;
 constexpr uint32_t kPairAStageBytes = 128 * kBK * 2;  // 16 KB: this CTA's 128 rows
 constexpr uint32_t kPairBStageBytes = 128 * kBK * 2;  // 16 KB: this CTA's half of B
 constexpr uint32_t kPairStageBytes = kPairAStageBytes + kPairBStageBytes;
+constexpr uint32_t kPairSmemA = 0;
+constexpr uint32_t kPairSmemB = kPairStages * kPairAStageBytes;
+constexpr uint32_t kPairSmemBar = kPairSmemB + kPairStages * kPairBStageBytes;
+// barriers: full[S] | empty[S] | tfull[2] | tempty[2] | drain, then the TMEM
+// address holder and the abort flag right after them
+constexpr uint32_t kPairBarBytes = 8u * (2 * kPairStages + 5);
+constexpr uint32_t kPairSmemBytes = kPairSmemBar + 256 + 1024;
 
-// Up to 6 stages of 32 KB (fewer when the epilogue needs shared memory).
-template <class Epi>
-using PairLayout = SmemLayout<kPairAStageBytes, kPairBStageBytes, 6, Epi::kEpiSmemPerWarp>;
+static_assert(kPairBarBytes + 8 <= 256, "barrier area overflows its reserved 256 bytes");
+
+static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
 template <class Epi, bool kBMNMajor, bool kAMNMajor = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
-                              int group_m, const __grid_constant__ typename Epi::Params ep,
-                              uint64_t timeout_ns) {
-  using L = PairLayout<Epi>;
-  constexpr int kPairStages = L::kStages;
+                              int group_m, const typename Epi::Params ep, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
 
-  const uint32_t sA = base + L::kA;
-  const uint32_t sB = base + L::kB;
-  const uint32_t bar0 = base + L::kBar;
+  const uint32_t sA = base + kPairSmemA;
+  const uint32_t sB = base + kPairSmemB;
+  const uint32_t bar0 = base + kPairSmemBar;
+  // full[S] | empty[S] | tfull[2] | tempty[2] | drain
   const uint32_t bar_full = bar0;
   const uint32_t bar_empty = bar0 + 8u * kPairStages;
   const uint32_t bar_tfull = bar0 + 16u * kPairStages;
   const uint32_t bar_tempty = bar_tfull + 16u;
   const uint32_t bar_drain = bar_tempty + 16u;
-  const uint32_t bar_epi = bar_drain + 8u;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kBar + L::kBarBytes);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kPairSmemBar + kPairBarBytes);
   volatile uint32_t* abort_flag =
-      reinterpret_cast<volatile uint32_t*>(smem + L::kBar + L::kBarBytes + 4);
+      reinterpret_cast<volatile uint32_t*>(smem + kPairSmemBar + kPairBarBytes + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -80,7 +85,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar_tempty + 8u * b, 2);
     }
     mbar_init(bar_drain, 1);
-    for (int i = 0; i < L::kEpiBars; ++i) mbar_init(bar_epi + 8u * i, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -212,10 +216,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
-    EpiState es;
-    es.smem = base + L::kEpi + static_cast<uint32_t>(warp - 2) * Epi::kEpiSmemPerWarp;
-    es.bar = bar_epi + static_cast<uint32_t>(warp - 2) * 16u;
-    es.iter = 0;
     uint32_t it = 0;
     for (int t = pair; t < num_tiles; t += npairs, ++it) {
       const uint32_t b = it & 1u;
@@ -234,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       c.M = M;
       c.N = N;
       c.nt = nt;
-      Epi::apply(ep, wc, c, es);
+      Epi::apply(ep, wc, c);
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
       if (threadIdx.x == kEpiFirstThread) mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * b, 0));

@@ -69,7 +69,6 @@ enum WaitSite : uint32_t {
   kSiteDrain = 6,
   kSiteSelftestBarrier = 7,
   kSiteSelftestFlag = 8,
-  kSiteEpiOperand = 9,
 };
 
 struct WaitCtl {
@@ -340,25 +339,6 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_m
       " [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
-}
-
-}  // namespace coda
-
-namespace coda {
-
-// Orders this thread's earlier generic-proxy shared-memory accesses before
-// later async-proxy (TMA) accesses of the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
 }
 
 }  // namespace coda
