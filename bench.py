@@ -358,6 +358,49 @@ def run_coda(args):
     extras["fwd_swiglu"] = {"ms": sw_ms, "tflops": w.fwd_flops / (sw_ms * 1e-3) / 1e12,
                             "calls": KS, "gpu_launches": 3 * KS,
                             "note": "coda_fwd_swiglu: GEMM1 epilogue applies r and silu(gate)*up"}
+    # the same forward and data gradient at the other Llama hidden sizes
+    # (device-generated N(0,1) / N(0,1/d) bf16 inputs; timing only)
+    by_w = {}
+    for wn in ("llama1b", "llama70b"):
+        ww = synth.WORKLOADS[wn]
+        Mw, dw, Nw = ww.M, ww.d, ww.N1
+        gw = {"x": torch.randn(Mw, dw, device=dev).to(torch.bfloat16),
+              "z": torch.randn(Mw, dw, device=dev).to(torch.bfloat16),
+              "W0": (torch.randn(dw, dw, device=dev) / dw ** 0.5).to(torch.bfloat16),
+              "W1": (torch.randn(dw, Nw, device=dev) / dw ** 0.5).to(torch.bfloat16),
+              "gamma": (1 + 0.316 * torch.randn(dw, device=dev)).to(torch.bfloat16)}
+        dyw = (0.1 * torch.randn(Mw, Nw, device=dev)).to(torch.bfloat16)
+        outw = B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, stream=stream)
+        wsw = B.workspace(B.coda_fwd_workspace_bytes(Mw, dw, Nw), dev)
+        wsb = B.workspace(B.coda_bwd_dgrad_workspace_bytes(Mw, dw, Nw), dev)
+        dhw = torch.empty((Mw, dw), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, h=outw[0],
+                       r=outw[1], y=outw[2], ws=wsw, stream=stream)
+            B.coda_bwd_dgrad(dyw, gw["W1"], outw[0], outw[1], gw["gamma"], dh=dhw, ws=wsb,
+                             stream=stream)
+        KW = max(3, min(K, 20))
+        barrier()
+        s0.record(stream)
+        for _ in range(KW):
+            B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, h=outw[0],
+                       r=outw[1], y=outw[2], ws=wsw, stream=stream)
+        s1.record(stream)
+        barrier()
+        f_ms = s0.elapsed_time(s1) / KW
+        s0.record(stream)
+        for _ in range(KW):
+            B.coda_bwd_dgrad(dyw, gw["W1"], outw[0], outw[1], gw["gamma"], dh=dhw, ws=wsb,
+                             stream=stream)
+        s1.record(stream)
+        barrier()
+        b_ms = s0.elapsed_time(s1) / KW
+        by_w[wn] = {"shape": [Mw, dw, Nw], "fwd_ms": f_ms,
+                    "fwd_tflops": ww.fwd_flops / (f_ms * 1e-3) / 1e12, "dgrad_ms": b_ms,
+                    "dgrad_tflops": ww.bwd_flops / (b_ms * 1e-3) / 1e12, "calls": KW}
+        del gw, dyw, outw, wsw, wsb, dhw
+    extras["other_llama_shapes"] = by_w
+
     # F4: the forward with the row reduction folded into GEMM1's epilogue (2 launches)
     B.coda_set_fold_rowreduce(1)
     try:
