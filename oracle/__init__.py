@@ -11,6 +11,9 @@ from .coda_oracle import (  # noqa: F401
     BackwardResult,
     FullBackwardResult,
     backward_full,
+    round_e4m3,
+    forward_fp8,
+    E4M3_MAX,
     residual_gemm,
     mean_square,
     inverse_rms,

@@ -217,6 +217,44 @@ def backward_rmsnorm_given_s(dh2, h, r, gamma, s):
     return r[:, None] * _f64(gamma)[None, :] * dh2 - ((r ** 2) * _f64(s) / d)[:, None] * h
 
 
+E4M3_MAX = 448.0
+
+
+def round_e4m3(v) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (ties to even), saturating at +-448.
+
+    E4M3 (the 'fn' variant: no infinities): 1 sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits.  Normal values have |v| >= 2^-6 and spacing
+    2^(e - 3) in the binade [2^e, 2^(e+1)); below 2^-6 the spacing is the
+    subnormal step 2^-9."""
+    v = _f64(v)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)              # subnormal range shares the 2^-9 step
+    step = np.exp2(e - 3.0)
+    q = np.round(a / step) * step        # numpy rounds half to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.sign(v) * q
+
+
+def forward_fp8(x_q, sx, W0_q, sW0, z, gamma, W1_q, sW1, s_hg, eps: float):
+    """The chain with FP8 (E4M3) operands and per-tensor scales; the values of
+    the FP8 tensors are code * scale.
+
+    Steps:
+      1. h  = (x_q sx) @ (W0_q sW0) + z
+      2. r  = 1 / sqrt(mean_j h^2 + eps)
+      3. hq = round_e4m3(h * gamma / s_hg)    (GEMM1's operand, quantised once)
+      4. y  = r * ((hq s_hg) @ (W1_q sW1))
+    Returns (ForwardResult, hq)."""
+    h = (_f64(x_q) * sx) @ (_f64(W0_q) * sW0) + _f64(z)
+    r = inverse_rms(mean_square(h), eps)
+    hq = round_e4m3(h * _f64(gamma)[None, :] / s_hg)
+    y = r[:, None] * ((hq * s_hg) @ (_f64(W1_q) * sW1))
+    return ForwardResult(h=h, r=r, y=y), hq
+
+
 def normwise_rel_err(got, ref) -> float:
     """||got - ref||_F / ||ref||_F in float64 (the parity metric)."""
     got = _f64(got)

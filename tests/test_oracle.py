@@ -560,3 +560,105 @@ def test_full_backward_planted_mistake_is_caught(kind, monkeypatch):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, kind
+
+
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) variant
+# ----------------------------------------------------------------------------
+
+def pin_e4m3_rounding_library(seed=15):
+    """round_e4m3 against torch's float8_e4m3fn conversion on in-range values."""
+    rng = np.random.default_rng(seed)
+    v = np.concatenate([rng.standard_normal(4000) * 50, rng.standard_normal(2000) * 1e-2,
+                        rng.uniform(-448, 448, 2000), [0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -6]])
+    ref = torch.tensor(v, dtype=torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    # float32 first, as torch converts from float32: compare on values exact in float32
+    got = O.round_e4m3(v.astype(np.float32).astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def pin_e4m3_closed_forms():
+    # exact grid points stay; halfway points go to the even mantissa; saturation
+    assert O.round_e4m3(np.array([1.0, 1.125, 448.0, 2.0 ** -9]))[[0, 1, 2, 3]].tolist() == \
+        [1.0, 1.125, 448.0, 2.0 ** -9]
+    assert O.round_e4m3(np.array([1.0625]))[0] == 1.0      # between 1 and 1.125: tie to even 1.0
+    assert O.round_e4m3(np.array([1.1875]))[0] == 1.25     # tie between 1.125 and 1.25 -> 1.25
+    assert O.round_e4m3(np.array([1000.0, -1e6]))[[0, 1]].tolist() == [448.0, -448.0]
+    assert O.round_e4m3(np.array([2.0 ** -10]))[0] == 0.0  # tie between 0 and 2^-9 -> 0
+    assert O.round_e4m3(np.array([3 * 2.0 ** -10]))[0] == 2.0 ** -8  # tie 2^-9/2^-8 -> even
+
+
+def pin_fp8_forward_reduces_to_bf16_definition(seed=16):
+    """With operands exactly representable and s_hg making h * gamma land on the
+    E4M3 grid, forward_fp8 equals the plain forward of the dequantised inputs."""
+    rng = np.random.default_rng(seed)
+    M, d, N1 = 4, 8, 6
+    grid = np.array([-2.0, -1.0, -0.5, 0.0, 0.5, 1.0, 2.0])
+    x_q = rng.choice(grid, (M, d))
+    W0_q = np.zeros((d, d))  # h = z: keeps h * gamma on the grid
+    z = rng.choice(grid, (M, d))
+    gamma = np.ones(d)
+    W1_q = rng.choice(grid, (d, N1))
+    f, hq = O.forward_fp8(x_q, 0.5, W0_q, 0.25, z, gamma, W1_q, 0.125, 1.0, 1e-5)
+    ref = O.forward(x_q * 0.5, W0_q * 0.25, z, gamma, W1_q * 0.125, 1e-5)
+    np.testing.assert_allclose(f.y, ref.y, rtol=1e-14, atol=1e-15)
+    np.testing.assert_array_equal(hq, z)
+
+
+def pin_fp8_forward_bruteforce(seed=17):
+    """Scalar loops over the four steps, with rounding by torch's E4M3 conversion."""
+    rng = np.random.default_rng(seed)
+    M, d, N1 = 3, 5, 4
+    x_q = O.round_e4m3(rng.standard_normal((M, d)) * 20)
+    W0_q = O.round_e4m3(rng.standard_normal((d, d)) * 20)
+    W1_q = O.round_e4m3(rng.standard_normal((d, N1)) * 20)
+    z = rng.standard_normal((M, d))
+    gamma = 1 + 0.3 * rng.standard_normal(d)
+    sx, sW0, sW1, s_hg, eps = 0.05, 0.01, 0.02, 0.03, 1e-5
+    f, _ = O.forward_fp8(x_q, sx, W0_q, sW0, z, gamma, W1_q, sW1, s_hg, eps)
+    for m in range(M):
+        h = [sum(x_q[m][k] * sx * W0_q[k][j] * sW0 for k in range(d)) + z[m][j] for j in range(d)]
+        r = 1.0 / math.sqrt(sum(v * v for v in h) / d + eps)
+        hq = [float(torch.tensor(min(max(h[j] * gamma[j] / s_hg, -448.0), 448.0),
+                                 dtype=torch.float64).to(torch.float8_e4m3fn).to(torch.float64))
+              for j in range(d)]
+        for n in range(N1):
+            y = r * sum(hq[j] * s_hg * W1_q[j][n] * sW1 for j in range(d))
+            assert abs(f.y[m, n] - y) <= 1e-12 * (1 + abs(y))
+
+
+FP8_PINS = [pin_e4m3_rounding_library, pin_e4m3_closed_forms,
+            pin_fp8_forward_reduces_to_bf16_definition, pin_fp8_forward_bruteforce]
+
+
+@pytest.mark.parametrize("pin", FP8_PINS, ids=lambda p: p.__name__)
+def test_fp8_pin(pin):
+    pin()
+
+
+@pytest.mark.parametrize("kind", ["ties_away_from_zero", "three_bits_too_many", "no_saturation"])
+def test_e4m3_planted_mistake_is_caught(kind, monkeypatch):
+    orig = O.round_e4m3
+
+    def mutant(v):
+        v = np.asarray(v, float)
+        a = np.abs(v)
+        e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6.0)
+        if kind == "ties_away_from_zero":
+            step = np.exp2(e - 3.0)
+            q = np.floor(a / step + 0.5) * step
+            return np.sign(v) * np.minimum(q, 448.0)
+        if kind == "three_bits_too_many":
+            step = np.exp2(e - 6.0)
+            return np.sign(v) * np.minimum(np.round(a / step) * step, 448.0)
+        q = orig(np.clip(v, -1e9, 1e9))
+        return np.where(np.abs(v) > 448.0, v, q)
+
+    monkeypatch.setattr(O, "round_e4m3", mutant)
+    failed = []
+    for pin in FP8_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, kind
