@@ -401,6 +401,43 @@ def run_coda(args):
         del gw, dyw, outw, wsw, wsb, dhw
     extras["other_llama_shapes"] = by_w
 
+    # F4: the forward with FP8 (E4M3) GEMM operands
+    t8 = synth.make_fp8_forward_inputs(M, d, N1, seed=rank)
+    f8 = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t8.items()}
+    ws8 = B.workspace(B.coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
+
+    def fwd8():
+        B.coda_fwd_fp8(f8["x_q"], f8["sx"], f8["W0_q"], f8["sW0"], f8["z"], f8["gamma"], f8["W1_q"],
+                       f8["sW1"], f8["s_hg"], eps, h=h, r=r, y=y, ws=ws8, stream=stream)
+
+    for _ in range(3):
+        fwd8()
+    f8ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KS)]
+    for ev in f8ev:
+        for e in ev:
+            e.record(stream)
+    barrier()
+    s0.record(stream)
+    for i in range(KS):
+        f8ev[i][0].record(stream)
+        B.coda_set_launch_events(f8ev[i][1:4])
+        fwd8()
+    s1.record(stream)
+    barrier()
+    B.coda_set_launch_events(None)
+    f8_ms = s0.elapsed_time(s1) / KS
+    f8_k = [statistics.fmean(f8ev[i][j].elapsed_time(f8ev[i][j + 1]) for i in range(KS))
+            for j in range(3)]
+    extras["fwd_fp8"] = {
+        "ms": f8_ms, "tflops": w.fwd_flops / (f8_ms * 1e-3) / 1e12, "calls": KS,
+        "gpu_launches": 3 * KS,
+        "kernels_ms": {"gemm0_fp8": f8_k[0], "rowreduce": f8_k[1], "gemm1_fp8": f8_k[2]},
+        "kernels_tflops": {"gemm0_fp8": 2 * M * d * d / (f8_k[0] * 1e-3) / 1e12,
+                           "gemm1_fp8": 2 * M * d * N1 / (f8_k[2] * 1e-3) / 1e12},
+        "note": "coda_fwd_fp8: E4M3 operands (tcgen05 kind::f8f6f4), per-tensor scales, "
+                "GEMM1 operand quantised in GEMM0's epilogue"}
+    del f8, ws8
+
     # F4: the forward with the row reduction folded into GEMM1's epilogue (2 launches)
     B.coda_set_fold_rowreduce(1)
     try:

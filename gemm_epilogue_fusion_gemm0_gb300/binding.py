@@ -64,6 +64,9 @@ EXPORTS = {
                               _sz, _vp]),
     "coda_get_mma_mode": (ctypes.c_int, []),
     "coda_set_fold_rowreduce": (_st, [ctypes.c_int]),
+    "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
+                           _vp, _vp, _vp, _sz, _vp]),
 }
 
 for _name, (_res, _args) in EXPORTS.items():
@@ -183,6 +186,40 @@ def coda_fwd_swiglu(x, W0, z, gamma, W1, eps, h=None, r=None, a=None, y=None, wa
     )
     _check(st, "coda_fwd_swiglu")
     return (h, r, a, y) if y is not None else (h, r, a)
+
+
+def coda_fwd_fp8_workspace_bytes(M: int, d: int, N1: int) -> int:
+    return int(_lib.coda_fwd_fp8_workspace_bytes(M, d, N1))
+
+
+def coda_fwd_fp8(x_q, sx, W0_q, sW0, z, gamma, W1_q, sW1, s_hg, eps, h=None, r=None, y=None,
+                 ws=None, stream=None):
+    """FP8 forward: x_q, W0_q, W1_q are float8_e4m3fn (or uint8) code tensors with
+    per-tensor scales; returns (h, r, y)."""
+    M, d = x_q.shape
+    N1 = W1_q.shape[1]
+    dev = x_q.device
+    bf = torch.bfloat16
+    h = torch.empty((M, d), dtype=bf, device=dev) if h is None else h
+    r = torch.empty((M,), dtype=torch.float32, device=dev) if r is None else r
+    y = torch.empty((M, N1), dtype=bf, device=dev) if y is None else y
+    if ws is None:
+        ws = workspace(coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
+
+    def code(t, shape, name):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")
+        return _dev(t, t.dtype, shape, name)
+
+    st = _lib.coda_fwd_fp8(
+        code(x_q, (M, d), "x_q"), float(sx), code(W0_q, (d, d), "W0_q"), float(sW0),
+        _dev(z, bf, (M, d), "z"), _dev(gamma, bf, (d,), "gamma"), code(W1_q, (d, N1), "W1_q"),
+        float(sW1), float(s_hg), float(eps), M, d, N1, _dev(h, bf, (M, d), "h"),
+        _dev(r, torch.float32, (M,), "r"), _dev(y, bf, (M, N1), "y"), ws.data_ptr(),
+        ws.numel() * ws.element_size(), _stream_ptr(stream),
+    )
+    _check(st, "coda_fwd_fp8")
+    return h, r, y
 
 
 def coda_bwd_dgrad(dy, W1, h, r, gamma, dh=None, ws=None, stream=None):

@@ -129,6 +129,8 @@ static auto* const kGemm1Swiglu = &gemm_epilogue_kernel<EpiRowScaleSwiGLU, true>
 static auto* const kPairGemm1Swiglu = &gemm_pair_epilogue_kernel<EpiRowScaleSwiGLU, true>;
 static auto* const kSwigluBwd = &gemm_epilogue_kernel<EpiSwiGLUBackward, false>;
 static auto* const kWgrad = &gemm_epilogue_kernel<EpiStoreF32, true, true>;
+static auto* const kPairGemm0F8 = &gemm_pair_epilogue_kernel<EpiResidualGammaSumsqFp8, true, false, true>;
+static auto* const kPairGemm1F8 = &gemm_pair_epilogue_kernel<EpiRowScaleFp8, true, false, true>;
 static auto* const kPairWgrad = &gemm_pair_epilogue_kernel<EpiStoreF32, true, true>;
 static auto* const kXgrad = &gemm_epilogue_kernel<EpiRowScale, false>;
 static auto* const kPairXgrad = &gemm_pair_epilogue_kernel<EpiRowScale, false>;
@@ -218,6 +220,10 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
                                  kSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm0F8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairGemm1F8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairSmemBytes) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -278,6 +284,20 @@ bool tmap_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, 
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D tensor map over a row-major [outer, inner] matrix of 1-byte (FP8) codes,
+// 128-byte swizzle.
+bool tmap_2d_u8(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -535,6 +555,88 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
     return CODA_ERR_LAUNCH;
   }
   after_launch(0, stream);
+  return CODA_OK;
+}
+
+size_t coda_fwd_fp8_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
+  if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
+  return align256(static_cast<size_t>(M) * d) +
+         align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4);
+}
+
+coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, float sW0,
+                           const coda_bf16* z, const coda_bf16* gamma, const uint8_t* W1_q,
+                           float sW1, float s_hg, float eps, int64_t M, int64_t d, int64_t N1,
+                           coda_bf16* h_out, float* r_out, coda_bf16* y_out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  coda_status_t st = check_common(M, d, N1);
+  if (st != CODA_OK) return st;
+  if (d % 16 != 0 || N1 % 16 != 0) return CODA_ERR_UNSUPPORTED_SHAPE;  // 16-byte FP8 rows
+  if (M == 0) return CODA_OK;
+  if (!x_q || !W0_q || !z || !gamma || !W1_q || !h_out || !r_out || !y_out)
+    return CODA_ERR_INVALID_ARG;
+  const float scales[] = {sx, sW0, sW1, s_hg};
+  for (float v : scales)
+    if (!std::isfinite(v) || !(v > 0.f)) return CODA_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return CODA_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_q, W0_q, z, gamma, W1_q, h_out, r_out, y_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CODA_ERR_MISALIGNED;
+  if (workspace == nullptr || workspace_bytes < coda_fwd_fp8_workspace_bytes(M, d, N1))
+    return CODA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
+  int sms = 0, max_pairs = 0;
+  st = device_setup(&sms, &max_pairs);
+  if (st != CODA_OK) return st;
+  const uint64_t tmo = g_timeout_ns.load();
+  const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
+  uint8_t* hq = static_cast<uint8_t*>(workspace);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align256(static_cast<size_t>(M) * d));
+
+  CUtensorMap mA0, mB0, mA1, mB1;
+  bool ok = tmap_2d_u8(&mA0, x_q, d, M, 128, 128);    // x  [M, d] codes, K-major
+  ok &= tmap_2d_u8(&mB0, W0_q, d, d, 128, 128);       // W0 [d(K), d(N)], MN-major
+  ok &= tmap_2d_u8(&mA1, hq, d, M, 128, 128);         // hq [M, d], K-major
+  ok &= tmap_2d_u8(&mB1, W1_q, N1, d, 128, 128);      // W1 [d(K), N1(N)], MN-major
+  if (!ok) return CODA_ERR_LAUNCH;
+
+  const int mtp = static_cast<int>(cdiv(M, kPairBM));
+  const int nt0 = static_cast<int>(cdiv(d, kBN));
+  const int nt1 = static_cast<int>(cdiv(N1, kBN));
+  EpiResidualGammaSumsqFp8::Params p0 = {};
+  p0.z = reinterpret_cast<const __nv_bfloat16*>(z);
+  p0.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
+  p0.h_out = reinterpret_cast<__nv_bfloat16*>(h_out);
+  p0.hq_out = hq;
+  p0.part = part;
+  p0.acc_scale = sx * sW0;
+  p0.inv_s_hg = 1.0f / s_hg;
+  cudaError_t e = launch(kPairGemm0F8, 2 * std::min(max_pairs, mtp * nt0), kThreads,
+                         kPairSmemBytes, stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(0, stream);
+  e = launch(rowreduce_rsqrt_kernel, static_cast<int>(cdiv(M, 256)), 256, 0, stream, false,
+             static_cast<const float*>(part), 2 * nt0, Mi, di, eps, r_out);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(1, stream);
+  EpiRowScaleFp8::Params p1 = {};
+  p1.r = r_out;
+  p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
+  p1.scale = s_hg * sW1;
+  e = launch(kPairGemm1F8, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes, stream,
+             false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return CODA_ERR_LAUNCH;
+  }
+  after_launch(2, stream);
   return CODA_OK;
 }
 

@@ -15,6 +15,8 @@
 // (per-tile sums of squares / of grad_h2 * gamma * h).
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "gemm.cuh"
 
 namespace coda {
@@ -580,6 +582,109 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
         for (int q = 0; q < 4; ++q) {
           hc[q] = hn[q];
           gc[q] = gn[q];
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// FP8 forward (E4M3 operands with per-tensor scales).
+// GEMM0: h = acc * (sx * sW0) + z, partial sums of h^2 as in the bf16 path, and
+//        GEMM1's operand quantised once: hq = e4m3_satfinite(h * gamma / s_hg).
+// GEMM1: y = r * (s_hg * sW1) * acc.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
+  struct Params {
+    const __nv_bfloat16* z;
+    const __nv_bfloat16* gamma;
+    __nv_bfloat16* h_out;
+    uint8_t* hq_out;   // [M, d] E4M3 codes of h * gamma / s_hg
+    float* part;       // [2 * nt][M]
+    float acc_scale;   // sx * sW0
+    float inv_s_hg;    // 1 / s_hg
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    float ss = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
+      uint32_t v[32];
+      tmem_ld32(c.taddr + col, v);
+      tmem_ld_wait(v);
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            const Chunk8 zz = ldg8(p.z + rowoff + n);
+            const Chunk8 gg = ldg8(p.gamma + n);
+            uint32_t hw[4];
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) * p.acc_scale + bf16lo(zz.w[e]);
+              const float h1 =
+                  __uint_as_float(v[g * 8 + 2 * e + 1]) * p.acc_scale + bf16hi(zz.w[e]);
+              ss = fmaf(h0, h0, ss);
+              ss = fmaf(h1, h1, ss);
+              hw[e] = pack_bf16x2(h0, h1);
+              q[2 * e] = h0 * bf16lo(gg.w[e]) * p.inv_s_hg;
+              q[2 * e + 1] = h1 * bf16hi(gg.w[e]) * p.inv_s_hg;
+            }
+            stg8(p.h_out + rowoff + n, hw);
+            *reinterpret_cast<uint2*>(p.hq_out + rowoff + n) =
+                make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]), pack_e4m3x4(q[4], q[5], q[6], q[7]));
+          }
+        }
+      }
+    }
+    if (row_ok) p.part[partial_index(c, m)] = ss;
+  }
+};
+
+struct EpiRowScaleFp8 : EpiDefaultCols {
+  struct Params {
+    const float* r;  // [M]
+    __nv_bfloat16* y_out;
+    float scale;     // s_hg * sW1
+  };
+
+  static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
+    const int m = c.mb * kBM + c.row;
+    const bool row_ok = m < c.M;
+    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const float rr = row_ok ? __ldg(p.r + m) * p.scale : 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kHalfChunks; ++ch) {
+      const int col = c.half * kHalfCols + ch * 32;
+      uint32_t v[32];
+      tmem_ld32(c.taddr + col, v);
+      tmem_ld_wait(v);
+      const int n0 = c.nb * kBN + col;
+      if (row_ok) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 8;
+          if (n < c.N) {
+            uint32_t yw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              yw[e] = pack_bf16x2(rr * __uint_as_float(v[g * 8 + 2 * e]),
+                                  rr * __uint_as_float(v[g * 8 + 2 * e + 1]));
+            stg8(p.y_out + rowoff + n, yw);
+          }
         }
       }
     }

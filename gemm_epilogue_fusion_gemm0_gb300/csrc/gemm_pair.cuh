@@ -38,7 +38,10 @@ static_assert(kPairBarBytes + 8 <= 256, "barrier area overflows its reserved 256
 
 static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
-template <class Epi, bool kBMNMajor, bool kAMNMajor = false>
+// kFp8: E4M3 operands (tcgen05 kind::f8f6f4).  A 128-byte smem row then holds
+// 128 K elements, so a stage covers K = 128 with the same bytes, each MMA
+// consumes K = 32, and an MN-major B half-tile (128 columns) is one TMA box.
+template <class Epi, bool kBMNMajor, bool kAMNMajor = false, bool kFp8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
@@ -69,7 +72,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int npairs = gridDim.x >> 1;
   const int mt = (M + kPairBM - 1) / kPairBM;
   const int nt = Epi::num_col_tiles(N);
-  const int nk = (K + kBK - 1) / kBK;
+  static_assert(!(kFp8 && kAMNMajor), "FP8 path: A must be K-major");
+  constexpr int kKE = kFp8 ? 128 : kBK;  // K elements per stage (128-byte rows)
+  const int nk = (K + kKE - 1) / kKE;
   const int num_tiles = mt * nt;
   const TileMap tmap{mt, nt, group_m};
   const WaitCtl wc{timeout_ns, &g_coda_status, abort_flag};
@@ -127,9 +132,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(a_dst, &tmA, full_leader, arow, kb * kBK);
             tma_load_2d_pair(a_dst + kBChunkBytes, &tmA, full_leader, arow + 64, kb * kBK);
           } else {
-            tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kBK, arow);
+            tma_load_2d_pair(a_dst, &tmA, full_leader, kb * kKE, arow);
           }
-          if constexpr (kBMNMajor) {
+          if constexpr (kFp8 && kBMNMajor) {
+            // this CTA's 128 B columns (chunks 2r, 2r+1 of the tile) in one 128 x 128 box
+            tma_load_2d_pair(b_dst, &tmB, full_leader, Epi::b_col(nb, 2 * static_cast<int>(rank), N),
+                             kb * kKE);
+          } else if constexpr (kFp8) {
+            tma_load_2d_pair(b_dst, &tmB, full_leader, kb * kKE, bcol);
+          } else if constexpr (kBMNMajor) {
             const int j0 = 2 * static_cast<int>(rank);  // this CTA's two 64-column chunks
             tma_load_2d_pair(b_dst, &tmB, full_leader, Epi::b_col(nb, j0, N), kb * kBK);
             tma_load_2d_pair(b_dst + kBChunkBytes, &tmB, full_leader, Epi::b_col(nb, j0 + 1, N),
@@ -160,7 +171,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (CTA 0 only)
     if (lane == 0) {
       if (leader) {
-        constexpr uint32_t idesc = idesc_bf16_f32(kPairBM, kBN, kAMNMajor, kBMNMajor);
+        constexpr uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPairBM, kBN, false, kBMNMajor)
+                                        : idesc_bf16_f32(kPairBM, kBN, kAMNMajor, kBMNMajor);
         int s = 0;
         uint32_t ph = 0;
         uint32_t it = 0;
@@ -184,11 +196,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t b0 = sB + s * kPairBStageBytes;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
+              // K-major: every MMA consumes 32 bytes of each 128-byte row (16 bf16 or
+              // 32 FP8 elements).  MN-major: 16 (bf16) or 32 (FP8) K rows, i.e. 2 or 4
+              // eight-row groups of 1024 bytes.
               const uint64_t ad = kAMNMajor ? sdesc_sw128(a0 + k * 2048, kBChunkBytes, 1024)
                                             : sdesc_sw128(a0 + k * 32, 16, 1024);
-              const uint64_t bd = kBMNMajor ? sdesc_sw128(b0 + k * 2048, kBChunkBytes, 1024)
-                                            : sdesc_sw128(b0 + k * 32, 16, 1024);
-              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              const uint64_t bd =
+                  kBMNMajor ? sdesc_sw128(b0 + k * (kFp8 ? 4096 : 2048), kFp8 ? 16384 : kBChunkBytes,
+                                          1024)
+                            : sdesc_sw128(b0 + k * 32, 16, 1024);
+              if constexpr (kFp8)
+                umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              else
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             umma_commit_pair_mc(bar_empty + 8u * s, 0x3);
             if (++s == kPairStages) {

@@ -342,3 +342,28 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_m
 }
 
 }  // namespace coda
+
+namespace coda {
+
+// D[tmem of both CTAs] (+)= A * B with FP8 operands (kind::f8f6f4; K = 32 per
+// instruction); same operand split across the CTA pair as umma_bf16_pair.
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format code 0) and an
+// fp32 accumulator; same field positions as idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n, bool a_mn_major,
+                                                      bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+}  // namespace coda

@@ -99,6 +99,41 @@ def make_down_proj_backward(rng, M: int, N1: int, Dout: int) -> dict:
     return {"W2": W2, "dout": dout}
 
 
+E4M3_MAX = 448.0
+
+
+def to_e4m3(a: np.ndarray):
+    """Per-tensor amax scaling to FP8 E4M3: returns (codes as a float8_e4m3fn
+    CPU tensor, scale) with value = code * scale and max |code| = 448."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    scale = float(np.max(np.abs(a))) / E4M3_MAX
+    if scale == 0.0:
+        scale = 1.0
+    codes = torch.from_numpy(a / np.float32(scale)).to(torch.float8_e4m3fn)
+    return codes, scale
+
+
+def make_fp8_forward_inputs(M: int, d: int, N1: int, seed: int = 0) -> dict:
+    """The FP8 forward's inputs: the same draws as make_forward_inputs, with x,
+    W0 and W1 carried as E4M3 codes plus per-tensor scales; z and gamma bf16.
+    The scale of GEMM1's FP8 operand h * gamma is fixed from the input
+    distributions: h = x @ W0 + z has variance 2, so 6 standard deviations of h
+    times max |gamma| maps to the largest E4M3 code."""
+    rng = np.random.default_rng(seed)
+    x = _normal(rng, (M, d), 1.0)
+    z = to_bf16(_normal(rng, (M, d), 1.0))
+    W0 = _normal(rng, (d, d), 1.0 / d)
+    W1 = _normal(rng, (d, N1), 1.0 / d)
+    gamma = to_bf16(1.0 + _normal(rng, (d,), 0.1))
+    xq, sx = to_e4m3(x)
+    W0q, sW0 = to_e4m3(W0)
+    W1q, sW1 = to_e4m3(W1)
+    g_amax = float(gamma.abs().max().to(torch.float32))
+    s_hg = 6.0 * float(np.sqrt(2.0)) * g_amax / E4M3_MAX
+    return {"x_q": xq, "sx": sx, "W0_q": W0q, "sW0": sW0, "W1_q": W1q, "sW1": sW1, "z": z,
+            "gamma": gamma, "s_hg": s_hg}
+
+
 def sample_rows(M: int, n: int, seed: int = 1) -> np.ndarray:
     """Sorted seeded sample of n distinct row indices in [0, M), always
     containing the first row, both sides of the first 128-row tile boundary

@@ -123,6 +123,31 @@ CODA_API coda_status_t coda_fwd_swiglu(const coda_bf16* x, const coda_bf16* W0, 
                                        cudaStream_t stream);
 
 /*
+ * Forward of the chain with FP8 (E4M3) GEMM operands.  The method's benefit
+ * grows as GEMMs get cheaper with low precision ("CODA：将 Transformer 块重写为
+ * GEMM-Epilogue 程序以消除显存瓶颈", blog.hotdry.top, opening section; section
+ * "实践要点": FP8/FP4 shifts the cost to memory traffic).  Values of FP8 tensors
+ * are code * scale (per-tensor fp32 scales > 0):
+ *   1. GEMM0 (tcgen05 kind::f8f6f4): h = (x_q @ W0_q) * sx * sW0 + z, stored
+ *      bf16; partial sums of h^2; GEMM1's operand quantised once in the
+ *      epilogue: hq = E4M3(h * gamma / s_hg), round to nearest even,
+ *      saturating at +-448 (the caller picks s_hg, e.g. from a previous amax);
+ *   2. r = 1 / sqrt(sum / d + eps);
+ *   3. GEMM1: y = r * (s_hg * sW1) * (hq @ W1_q), stored bf16.
+ *   x_q [M, d], W0_q [d, d], W1_q [d, N1]: E4M3 codes (1 byte), row-major.
+ *   z [M, d], gamma [d] bf16; h_out [M, d] bf16, r_out [M] fp32, y_out [M, N1] bf16.
+ *   workspace: at least coda_fwd_fp8_workspace_bytes(M, d, N1) (hq and partials).
+ * d and N1 must be multiples of 16.  Always runs CTA-pair tiles.
+ */
+CODA_API size_t coda_fwd_fp8_workspace_bytes(int64_t M, int64_t d, int64_t N1);
+CODA_API coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, float sW0,
+                                    const coda_bf16* z, const coda_bf16* gamma,
+                                    const uint8_t* W1_q, float sW1, float s_hg, float eps,
+                                    int64_t M, int64_t d, int64_t N1,
+                                    coda_bf16* h_out, float* r_out, coda_bf16* y_out,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Data gradient through the RMSNorm branch, as one GEMM-epilogue program:
  *   grad_h2 = grad_y @ W1^T  accumulated in tensor memory, then in the epilogue
  *   q[m]    = sum_j grad_h2[m,j] * gamma[j] * h[m,j]  (so s = r * q equals

@@ -125,6 +125,20 @@ def test_full_backward_workspace_and_validation(lib):
     assert call(wsb=64) == E["CODA_ERR_WORKSPACE_TOO_SMALL"]
 
 
+def test_fp8_argument_validation(lib):
+    E = {v: k for k, v in lib.STATUS_NAMES.items()}
+    raw = lib.raw()
+
+    def call(d=256, sx=0.1, shg=0.1):
+        return raw.coda_fwd_fp8(FAKE, sx, FAKE, 0.1, FAKE, FAKE, FAKE, 0.1, shg, 1e-5, 128, d, 512,
+                                FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+
+    assert call(d=264) == E["CODA_ERR_UNSUPPORTED_SHAPE"]  # FP8 rows need d % 16 == 0
+    assert call(sx=0.0) == E["CODA_ERR_INVALID_ARG"]
+    assert call(shg=float("nan")) == E["CODA_ERR_INVALID_ARG"]
+    assert lib.coda_fwd_fp8_workspace_bytes(8192, 4096, 28672) == 8192 * 4096 + 32 * 8192 * 4
+
+
 def test_no_device_is_reported_without_gpu(lib):
     import torch
 

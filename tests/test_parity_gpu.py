@@ -345,3 +345,46 @@ def test_folded_rowreduce_is_bit_identical(B, mode, M, d, N1):
     ref = oracle.forward(f64(t["x"]), f64(t["W0"]), f64(t["z"]), f64(t["gamma"]), f64(t["W1"]), 1e-5)
     check("y", f64(fold[2]), ref.y, TOL_HY)
     check_r(f64(fold[1]), ref.r)
+
+
+# ----------------------------------------------------------------------------- FP8 forward
+def run_fp8(B, M, d, N1, eps, seed=0, rows=None, s_hg_factor=1.0):
+    """The oracle models the same quantisation of GEMM1's operand (E4M3, ties to
+    even, saturating); the GPU decides each code from its fp32 h, the oracle from
+    the exact h, so codes can differ where h * gamma / s_hg sits within an fp32
+    rounding of a decision boundary: the normwise bound absorbs those."""
+    dev = torch.device("cuda:0")
+    t = synth.make_fp8_forward_inputs(M, d, N1, seed=seed)
+    s_hg = t["s_hg"] * s_hg_factor
+    h, r, y = B.coda_fwd_fp8(t["x_q"].to(dev), t["sx"], t["W0_q"].to(dev), t["sW0"], t["z"].to(dev),
+                             t["gamma"].to(dev), t["W1_q"].to(dev), t["sW1"], s_hg, eps)
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    idx = torch.as_tensor(sel)
+    f, hq = oracle.forward_fp8(f64(t["x_q"][idx]), t["sx"], f64(t["W0_q"]), t["sW0"],
+                               f64(t["z"][idx]), f64(t["gamma"]), f64(t["W1_q"]), t["sW1"], s_hg, eps)
+    out = {"h": check("h", f64(h.cpu()[idx]), f.h, TOL_HY), "r": check_r(f64(r.cpu()[idx]), f.r),
+           "y": check("y", f64(y.cpu()[idx]), f.y, TOL_HY)}
+    out["saturated"] = float(np.mean(np.abs(hq) >= oracle.E4M3_MAX))
+    return out
+
+
+@pytest.mark.parametrize("M,d,N1", [
+    (128, 256, 512),     # tiny
+    (300, 336, 784),     # ragged in M, d and N1 (multiples of 16 for 1-byte rows)
+    (640, 512, 1536),    # several tiles
+])
+def test_fp8_forward_small(B, M, d, N1):
+    run_fp8(B, M, d, N1, 1e-5)
+
+
+def test_fp8_forward_saturation(B):
+    """A small s_hg saturates many codes at +-448 on both sides."""
+    out = run_fp8(B, 256, 256, 512, 1e-5, s_hg_factor=0.1)
+    assert out["saturated"] > 0.01
+
+
+def test_fp8_forward_llama7b_sampled_rows(B):
+    w = synth.WORKLOADS["llama7b"]
+    run_fp8(B, w.M, w.d, w.N1, w.eps, rows=synth.sample_rows(w.M, 256, seed=4))
