@@ -362,8 +362,8 @@ def run_fp8(B, M, d, N1, eps, seed=0, rows=None, s_hg_factor=1.0):
     assert st == B.CODA_OK, (B.status_string(st), hex(detail))
     sel = np.arange(M) if rows is None else np.asarray(rows)
     idx = torch.as_tensor(sel)
-    f, hq = oracle.forward_fp8(f64(t["x_q"][idx]), t["sx"], f64(t["W0_q"]), t["sW0"],
-                               f64(t["z"][idx]), f64(t["gamma"]), f64(t["W1_q"]), t["sW1"], s_hg, eps)
+    f, hq = oracle.forward_fp8(f64(t["x_q"])[sel], t["sx"], f64(t["W0_q"]), t["sW0"],
+                               f64(t["z"])[sel], f64(t["gamma"]), f64(t["W1_q"]), t["sW1"], s_hg, eps)
     out = {"h": check("h", f64(h.cpu()[idx]), f.h, TOL_HY), "r": check_r(f64(r.cpu()[idx]), f.r),
            "y": check("y", f64(y.cpu()[idx]), f.y, TOL_HY)}
     out["saturated"] = float(np.mean(np.abs(hq) >= oracle.E4M3_MAX))
