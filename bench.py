@@ -252,6 +252,214 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------- GPU arm
+EXTRAS = ("fwd_swiglu", "other_llama_shapes", "fwd_fp8", "fwd_folded_rowreduce", "fwd_unfused",
+          "bwd_swiglu_dgrad", "bwd_full")
+
+
+def time_calls(B, stream, barrier, call, n, launches):
+    """Mean ms per call over n calls, and the mean ms of each of the call's
+    `launches` kernel launches (CUDA events recorded after every launch)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(n)]
+    for ev in evs:  # create the events outside the timed region
+        for e in ev:
+            e.record(stream)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    s0.record(stream)
+    for i in range(n):
+        evs[i][0].record(stream)
+        B.coda_set_launch_events(evs[i][1:])
+        call()
+    s1.record(stream)
+    barrier()
+    B.coda_set_launch_events(None)
+    per = [statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+           for j in range(launches)]
+    return s0.elapsed_time(s1) / n, per
+
+
+def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
+    """The widened paths and the comparison sequence, each timed on its own
+    (none of it is part of `value`)."""
+    want = set(EXTRAS) if args.extras == "all" else set(args.extras.split(",")) - {""}
+    dev = dy.device
+    M, d, N1, eps = w.M, w.d, w.N1, w.eps
+    K = args.steps
+    KS = max(3, min(K, 50))
+    peaks, _ = load_peaks()
+    extras = {}
+
+    def tf(flops, ms):
+        return flops / (ms * 1e-3) / 1e12
+
+    def warm(call):
+        for _ in range(3):
+            call()
+
+    a_sw = torch.empty((M, N1 // 2), dtype=torch.bfloat16, device=dev)
+    if "fwd_swiglu" in want:
+        def fwd_sw():
+            B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw,
+                              ws=ws_f, stream=stream)
+        warm(fwd_sw)
+        ms, _ = time_calls(B, stream, barrier, fwd_sw, KS, 3)
+        extras["fwd_swiglu"] = {"ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS,
+                                "gpu_launches": 3 * KS,
+                                "note": "coda_fwd_swiglu: GEMM1 epilogue applies r and silu(gate)*up"}
+
+    if "other_llama_shapes" in want:
+        # the same forward and data gradient at the other Llama hidden sizes
+        # (device-generated N(0,1) / N(0,1/d) bf16 inputs; timing only)
+        by_w = {}
+        for wn in ("llama1b", "llama70b"):
+            ww = synth.WORKLOADS[wn]
+            Mw, dw, Nw = ww.M, ww.d, ww.N1
+            gw = {"x": torch.randn(Mw, dw, device=dev).to(torch.bfloat16),
+                  "z": torch.randn(Mw, dw, device=dev).to(torch.bfloat16),
+                  "W0": (torch.randn(dw, dw, device=dev) / dw ** 0.5).to(torch.bfloat16),
+                  "W1": (torch.randn(dw, Nw, device=dev) / dw ** 0.5).to(torch.bfloat16),
+                  "gamma": (1 + 0.316 * torch.randn(dw, device=dev)).to(torch.bfloat16)}
+            dyw = (0.1 * torch.randn(Mw, Nw, device=dev)).to(torch.bfloat16)
+            outw = B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, stream=stream)
+            wsw = B.workspace(B.coda_fwd_workspace_bytes(Mw, dw, Nw), dev)
+            wsb = B.workspace(B.coda_bwd_dgrad_workspace_bytes(Mw, dw, Nw), dev)
+            dhw = torch.empty((Mw, dw), dtype=torch.bfloat16, device=dev)
+
+            def fwd_w():
+                B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, h=outw[0],
+                           r=outw[1], y=outw[2], ws=wsw, stream=stream)
+
+            def bwd_w():
+                B.coda_bwd_dgrad(dyw, gw["W1"], outw[0], outw[1], gw["gamma"], dh=dhw, ws=wsb,
+                                 stream=stream)
+            warm(fwd_w)
+            warm(bwd_w)
+            KW = max(3, min(K, 20))
+            f_ms, _ = time_calls(B, stream, barrier, fwd_w, KW, 3)
+            b_ms, _ = time_calls(B, stream, barrier, bwd_w, KW, 1)
+            by_w[wn] = {"shape": [Mw, dw, Nw], "fwd_ms": f_ms, "fwd_tflops": tf(ww.fwd_flops, f_ms),
+                        "dgrad_ms": b_ms, "dgrad_tflops": tf(ww.bwd_flops, b_ms), "calls": KW}
+            del gw, dyw, outw, wsw, wsb, dhw
+        extras["other_llama_shapes"] = by_w
+
+    if "fwd_fp8" in want:
+        # F4: the forward with FP8 (E4M3) GEMM operands
+        t8 = synth.make_fp8_forward_inputs(M, d, N1, seed=rank)
+        f8 = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t8.items()}
+        ws8 = B.workspace(B.coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
+
+        def fwd8():
+            B.coda_fwd_fp8(f8["x_q"], f8["sx"], f8["W0_q"], f8["sW0"], f8["z"], f8["gamma"],
+                           f8["W1_q"], f8["sW1"], f8["s_hg"], eps, h=h, r=r, y=y, ws=ws8,
+                           stream=stream)
+        warm(fwd8)
+        ms, k = time_calls(B, stream, barrier, fwd8, KS, 3)
+        # E4M3 dense tensor peak: the measured bf16 figure times the nominal fp8/bf16 ratio (2)
+        p8 = 2.0 * peaks["bf16_tflops_sustained"]
+        g0, g1 = tf(2 * M * d * d, k[0]), tf(2 * M * d * N1, k[2])
+        extras["fwd_fp8"] = {
+            "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 3 * KS,
+            "kernels_ms": {"gemm0_fp8": k[0], "rowreduce": k[1], "gemm1_fp8": k[2]},
+            "kernels_tflops": {"gemm0_fp8": g0, "gemm1_fp8": g1},
+            "fp8_peak_tflops": p8, "frac_of_fp8_peak": tf(w.fwd_flops, ms) / p8,
+            "kernels_frac_of_fp8_peak": {"gemm0_fp8": g0 / p8, "gemm1_fp8": g1 / p8},
+            "note": "coda_fwd_fp8: E4M3 operands (tcgen05 kind::f8f6f4), per-tensor scales, "
+                    "GEMM1 operand quantised in GEMM0's epilogue; fp8 peak = 2 x measured bf16 "
+                    "sustained (nominal dense ratio)"}
+        del f8, ws8
+
+    if "fwd_folded_rowreduce" in want:
+        # F4: the forward with the row reduction folded into GEMM1's epilogue (2 launches)
+        def fwd():
+            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                       stream=stream)
+        B.coda_set_fold_rowreduce(1)
+        try:
+            warm(fwd)
+            ms, _ = time_calls(B, stream, barrier, fwd, KS, 2)
+        finally:
+            B.coda_set_fold_rowreduce(0)
+        extras["fwd_folded_rowreduce"] = {
+            "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 2 * KS,
+            "note": "coda_fwd with r formed in GEMM1's epilogue (F4)"}
+
+    if "fwd_unfused" in want:
+        # the unfused sequence of this library's own kernels: GEMM0 storing h,
+        # a separate RMSNorm kernel writing the normalised [M, d] tensor, GEMM1
+        # storing y (the round trip the fused forward removes)
+        ws_u = B.workspace(B.coda_fwd_unfused_workspace_bytes(M, d, N1), dev)
+
+        def fwd_u():
+            B.coda_fwd_unfused(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y,
+                               ws=ws_u, stream=stream)
+        warm(fwd_u)
+        ms, k = time_calls(B, stream, barrier, fwd_u, KS, 3)
+        extras["fwd_unfused"] = {
+            "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 3 * KS,
+            "kernels_ms": {"gemm0_plain": k[0], "rmsnorm_rows": k[1], "gemm1_plain": k[2]},
+            "note": "coda_fwd_unfused: GEMM0 -> RMSNorm kernel (normalised tensor through HBM) "
+                    "-> GEMM1; the fused forward's comparison sequence"}
+        del ws_u
+
+    if "bwd_swiglu_dgrad" in want:
+        # backward through the gated activation and the down projection (Dout = d),
+        # statistic formed upstream, tile-local RMSNorm-branch data gradient
+        y_pre = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+        B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw,
+                          y=y_pre, ws=ws_f, stream=stream)
+        W2 = (torch.randn((N1 // 2, d), device=dev) / (N1 // 2) ** 0.5).to(torch.bfloat16)
+        dout = (torch.randn((M, d), device=dev) * 0.1).to(torch.bfloat16)
+        dy_b = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
+        s_b = torch.empty((M,), dtype=torch.float32, device=dev)
+        ws_s = B.workspace(B.coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, d), dev)
+
+        def bwd_sw():
+            B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b,
+                                    dh=dh, ws=ws_s, stream=stream)
+        warm(bwd_sw)
+        ms, k = time_calls(B, stream, barrier, bwd_sw, KS, 3)
+        sb_flops = 2 * M * d * (N1 // 2) + w.bwd_flops
+        extras["bwd_swiglu_dgrad"] = {
+            "ms": ms, "tflops": tf(sb_flops, ms), "calls": KS, "gpu_launches": 3 * KS, "Dout": d,
+            "kernels_ms": {"swiglu_bwd_gemm": k[0], "rowsum_s": k[1], "dgrad_given_s": k[2]},
+            "kernels_tflops": {"swiglu_bwd_gemm": tf(2 * M * d * (N1 // 2), k[0]),
+                               "dgrad_given_s": tf(w.bwd_flops, k[2])},
+            "note": "coda_bwd_swiglu_dgrad: dout@W2^T with SwiGLU-bwd + partial s epilogue, "
+                    "row sum, dy@W1^T with tile-local RMSNorm bwd"}
+        del y_pre, W2, dout, dy_b, s_b, ws_s
+
+    if "bwd_full" in want:
+        # all gradients of the chain (training step backward): coda_bwd, 5 launches
+        dh_res = (torch.randn((M, d), device=dev) * 0.1).to(torch.bfloat16)
+        fb_out = {"dh": dh, "dx": torch.empty((M, d), dtype=torch.bfloat16, device=dev),
+                  "dgamma": torch.empty((d,), dtype=torch.float32, device=dev),
+                  "dW0": torch.empty((d, d), dtype=torch.float32, device=dev),
+                  "dW1": torch.empty((d, N1), dtype=torch.float32, device=dev)}
+        ws_fb = B.workspace(B.coda_bwd_workspace_bytes(M, d, N1), dev)
+        B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                   stream=stream)
+
+        def bwd_all():
+            B.coda_bwd(dy, g["x"], g["W0"], g["W1"], h, r, g["gamma"], dh_res, out=fb_out,
+                       ws=ws_fb, stream=stream)
+        warm(bwd_all)
+        ms, k = time_calls(B, stream, barrier, bwd_all, KS, 5)
+        fb_fl = [2 * M * N1 * d, 0, 2 * d * N1 * M, 2 * M * d * d, 2 * d * d * M]
+        fb_names = ["dgrad_rmsnorm_bwd_dgamma_h2", "colsum_dgamma", "dW1_h2T_dy", "dx_dh_W0T",
+                    "dW0_xT_dh"]
+        extras["bwd_full"] = {
+            "ms": ms, "tflops": tf(sum(fb_fl), ms), "calls": KS, "gpu_launches": 5 * KS,
+            "kernels_ms": dict(zip(fb_names, k)),
+            "kernels_tflops": {n: tf(f, kk) for n, f, kk in zip(fb_names, fb_fl, k) if f},
+            "note": "coda_bwd: all gradients (dh incl. residual grad, dx, dgamma, dW0, dW1)"}
+        del dh_res, fb_out, ws_fb
+
+    st, detail = B.coda_get_device_status()
+    if st != B.CODA_OK:
+        raise RuntimeError(f"device status after extras: {B.status_string(st)} {detail:#x}")
+    return extras
+
+
 def run_coda(args):
     import __graft_entry__ as ge
 
@@ -339,205 +547,7 @@ def run_coda(args):
     flops_step = w.fwd_flops + w.bwd_flops
     value = job_throughput(world, K, flops_step, ms)
 
-    # ---- widened path (not part of `value`): forward with the SwiGLU epilogue
-    a_sw = torch.empty((M, N1 // 2), dtype=torch.bfloat16, device=dev)
-    extras = {}
-    for _ in range(3):
-        B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw,
-                          ws=ws_f, stream=stream)
-    KS = max(3, min(K, 50))
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    s0.record(stream)
-    for _ in range(KS):
-        B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw,
-                          ws=ws_f, stream=stream)
-    s1.record(stream)
-    barrier()
-    sw_ms = s0.elapsed_time(s1) / KS
-    extras["fwd_swiglu"] = {"ms": sw_ms, "tflops": w.fwd_flops / (sw_ms * 1e-3) / 1e12,
-                            "calls": KS, "gpu_launches": 3 * KS,
-                            "note": "coda_fwd_swiglu: GEMM1 epilogue applies r and silu(gate)*up"}
-    # the same forward and data gradient at the other Llama hidden sizes
-    # (device-generated N(0,1) / N(0,1/d) bf16 inputs; timing only)
-    by_w = {}
-    for wn in ("llama1b", "llama70b"):
-        ww = synth.WORKLOADS[wn]
-        Mw, dw, Nw = ww.M, ww.d, ww.N1
-        gw = {"x": torch.randn(Mw, dw, device=dev).to(torch.bfloat16),
-              "z": torch.randn(Mw, dw, device=dev).to(torch.bfloat16),
-              "W0": (torch.randn(dw, dw, device=dev) / dw ** 0.5).to(torch.bfloat16),
-              "W1": (torch.randn(dw, Nw, device=dev) / dw ** 0.5).to(torch.bfloat16),
-              "gamma": (1 + 0.316 * torch.randn(dw, device=dev)).to(torch.bfloat16)}
-        dyw = (0.1 * torch.randn(Mw, Nw, device=dev)).to(torch.bfloat16)
-        outw = B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, stream=stream)
-        wsw = B.workspace(B.coda_fwd_workspace_bytes(Mw, dw, Nw), dev)
-        wsb = B.workspace(B.coda_bwd_dgrad_workspace_bytes(Mw, dw, Nw), dev)
-        dhw = torch.empty((Mw, dw), dtype=torch.bfloat16, device=dev)
-        for _ in range(3):
-            B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, h=outw[0],
-                       r=outw[1], y=outw[2], ws=wsw, stream=stream)
-            B.coda_bwd_dgrad(dyw, gw["W1"], outw[0], outw[1], gw["gamma"], dh=dhw, ws=wsb,
-                             stream=stream)
-        KW = max(3, min(K, 20))
-        barrier()
-        s0.record(stream)
-        for _ in range(KW):
-            B.coda_fwd(gw["x"], gw["W0"], gw["z"], gw["gamma"], gw["W1"], ww.eps, h=outw[0],
-                       r=outw[1], y=outw[2], ws=wsw, stream=stream)
-        s1.record(stream)
-        barrier()
-        f_ms = s0.elapsed_time(s1) / KW
-        s0.record(stream)
-        for _ in range(KW):
-            B.coda_bwd_dgrad(dyw, gw["W1"], outw[0], outw[1], gw["gamma"], dh=dhw, ws=wsb,
-                             stream=stream)
-        s1.record(stream)
-        barrier()
-        b_ms = s0.elapsed_time(s1) / KW
-        by_w[wn] = {"shape": [Mw, dw, Nw], "fwd_ms": f_ms,
-                    "fwd_tflops": ww.fwd_flops / (f_ms * 1e-3) / 1e12, "dgrad_ms": b_ms,
-                    "dgrad_tflops": ww.bwd_flops / (b_ms * 1e-3) / 1e12, "calls": KW}
-        del gw, dyw, outw, wsw, wsb, dhw
-    extras["other_llama_shapes"] = by_w
-
-    # F4: the forward with FP8 (E4M3) GEMM operands
-    t8 = synth.make_fp8_forward_inputs(M, d, N1, seed=rank)
-    f8 = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t8.items()}
-    ws8 = B.workspace(B.coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
-
-    def fwd8():
-        B.coda_fwd_fp8(f8["x_q"], f8["sx"], f8["W0_q"], f8["sW0"], f8["z"], f8["gamma"], f8["W1_q"],
-                       f8["sW1"], f8["s_hg"], eps, h=h, r=r, y=y, ws=ws8, stream=stream)
-
-    for _ in range(3):
-        fwd8()
-    f8ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KS)]
-    for ev in f8ev:
-        for e in ev:
-            e.record(stream)
-    barrier()
-    s0.record(stream)
-    for i in range(KS):
-        f8ev[i][0].record(stream)
-        B.coda_set_launch_events(f8ev[i][1:4])
-        fwd8()
-    s1.record(stream)
-    barrier()
-    B.coda_set_launch_events(None)
-    f8_ms = s0.elapsed_time(s1) / KS
-    f8_k = [statistics.fmean(f8ev[i][j].elapsed_time(f8ev[i][j + 1]) for i in range(KS))
-            for j in range(3)]
-    extras["fwd_fp8"] = {
-        "ms": f8_ms, "tflops": w.fwd_flops / (f8_ms * 1e-3) / 1e12, "calls": KS,
-        "gpu_launches": 3 * KS,
-        "kernels_ms": {"gemm0_fp8": f8_k[0], "rowreduce": f8_k[1], "gemm1_fp8": f8_k[2]},
-        "kernels_tflops": {"gemm0_fp8": 2 * M * d * d / (f8_k[0] * 1e-3) / 1e12,
-                           "gemm1_fp8": 2 * M * d * N1 / (f8_k[2] * 1e-3) / 1e12},
-        "note": "coda_fwd_fp8: E4M3 operands (tcgen05 kind::f8f6f4), per-tensor scales, "
-                "GEMM1 operand quantised in GEMM0's epilogue"}
-    del f8, ws8
-
-    # F4: the forward with the row reduction folded into GEMM1's epilogue (2 launches)
-    B.coda_set_fold_rowreduce(1)
-    try:
-        for _ in range(3):
-            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
-                       stream=stream)
-        barrier()
-        s0.record(stream)
-        for _ in range(KS):
-            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
-                       stream=stream)
-        s1.record(stream)
-        barrier()
-    finally:
-        B.coda_set_fold_rowreduce(0)
-    fo_ms = s0.elapsed_time(s1) / KS
-    extras["fwd_folded_rowreduce"] = {
-        "ms": fo_ms, "tflops": w.fwd_flops / (fo_ms * 1e-3) / 1e12, "calls": KS,
-        "gpu_launches": 2 * KS, "note": "coda_fwd with r formed in GEMM1's epilogue (F4)"}
-
-    # backward through the gated activation and the down projection (Dout = d),
-    # statistic formed upstream, tile-local RMSNorm-branch data gradient
-    y_pre = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
-    B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, a=a_sw, y=y_pre,
-                      ws=ws_f, stream=stream)
-    W2 = (torch.randn((N1 // 2, d), device=dev) / (N1 // 2) ** 0.5).to(torch.bfloat16)
-    dout = (torch.randn((M, d), device=dev) * 0.1).to(torch.bfloat16)
-    dy_b = torch.empty((M, N1), dtype=torch.bfloat16, device=dev)
-    s_b = torch.empty((M,), dtype=torch.float32, device=dev)
-    ws_s = B.workspace(B.coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, d), dev)
-    for _ in range(3):
-        B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b, dh=dh,
-                                ws=ws_s, stream=stream)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KS)]
-    for ev in sev:
-        for e in ev:
-            e.record(stream)
-    barrier()
-    s0.record(stream)
-    for i in range(KS):
-        sev[i][0].record(stream)
-        B.coda_set_launch_events(sev[i][1:4])
-        B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=dy_b, s=s_b, dh=dh,
-                                ws=ws_s, stream=stream)
-    s1.record(stream)
-    barrier()
-    B.coda_set_launch_events(None)
-    sb_ms = s0.elapsed_time(s1) / KS
-    sb_k = [statistics.fmean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(KS))
-            for j in range(3)]
-    sb_flops = 2 * M * d * (N1 // 2) + w.bwd_flops
-    extras["bwd_swiglu_dgrad"] = {
-        "ms": sb_ms, "tflops": sb_flops / (sb_ms * 1e-3) / 1e12, "calls": KS,
-        "gpu_launches": 3 * KS, "Dout": d,
-        "kernels_ms": {"swiglu_bwd_gemm": sb_k[0], "rowsum_s": sb_k[1], "dgrad_given_s": sb_k[2]},
-        "kernels_tflops": {"swiglu_bwd_gemm": 2 * M * d * (N1 // 2) / (sb_k[0] * 1e-3) / 1e12,
-                           "dgrad_given_s": w.bwd_flops / (sb_k[2] * 1e-3) / 1e12},
-        "note": "coda_bwd_swiglu_dgrad: dout@W2^T with SwiGLU-bwd + partial s epilogue, "
-                "row sum, dy@W1^T with tile-local RMSNorm bwd"}
-    # all gradients of the chain (training step backward): coda_bwd, 5 launches
-    dh_res = (torch.randn((M, d), device=dev) * 0.1).to(torch.bfloat16)
-    fb_out = {"dh": dh, "dx": torch.empty((M, d), dtype=torch.bfloat16, device=dev),
-              "dgamma": torch.empty((d,), dtype=torch.float32, device=dev),
-              "dW0": torch.empty((d, d), dtype=torch.float32, device=dev),
-              "dW1": torch.empty((d, N1), dtype=torch.float32, device=dev)}
-    ws_fb = B.workspace(B.coda_bwd_workspace_bytes(M, d, N1), dev)
-    B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
-               stream=stream)
-    for _ in range(3):
-        B.coda_bwd(dy, g["x"], g["W0"], g["W1"], h, r, g["gamma"], dh_res, out=fb_out, ws=ws_fb,
-                   stream=stream)
-    fev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(KS)]
-    for ev in fev:
-        for e in ev:
-            e.record(stream)
-    barrier()
-    s0.record(stream)
-    for i in range(KS):
-        fev[i][0].record(stream)
-        B.coda_set_launch_events(fev[i][1:6])
-        B.coda_bwd(dy, g["x"], g["W0"], g["W1"], h, r, g["gamma"], dh_res, out=fb_out, ws=ws_fb,
-                   stream=stream)
-    s1.record(stream)
-    barrier()
-    B.coda_set_launch_events(None)
-    fb_ms = s0.elapsed_time(s1) / KS
-    fb_k = [statistics.fmean(fev[i][j].elapsed_time(fev[i][j + 1]) for i in range(KS))
-            for j in range(5)]
-    fb_fl = [2 * M * N1 * d, 0, 2 * d * N1 * M, 2 * M * d * d, 2 * d * d * M]
-    fb_names = ["dgrad_rmsnorm_bwd_dgamma_h2", "colsum_dgamma", "dW1_h2T_dy", "dx_dh_W0T",
-                "dW0_xT_dh"]
-    extras["bwd_full"] = {
-        "ms": fb_ms, "tflops": sum(fb_fl) / (fb_ms * 1e-3) / 1e12, "calls": KS,
-        "gpu_launches": 5 * KS,
-        "kernels_ms": dict(zip(fb_names, fb_k)),
-        "kernels_tflops": {n: f / (k * 1e-3) / 1e12 for n, f, k in zip(fb_names, fb_fl, fb_k) if f},
-        "note": "coda_bwd: all gradients (dh incl. residual grad, dx, dgamma, dW0, dW1)"}
-    st, detail = B.coda_get_device_status()
-    if st != B.CODA_OK:
-        raise RuntimeError(f"device status after extras: {B.status_string(st)} {detail:#x}")
+    extras = run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank)
 
     # ---- end to end through the same C-ABI calls with pinned host buffers.
     # Headline form: the weights and gamma are model state, uploaded once before
@@ -697,6 +707,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["coda", "reference"], default="coda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extras", default="all",
+                    help="widened paths timed after the step: 'all', 'none' or a comma list of "
+                         + ", ".join(EXTRAS))
     ap.add_argument("--mma-mode", type=int, choices=[0, 1], default=None,
                     help="0: single-CTA tiles, 1: CTA-pair tiles (library default)")
     args = ap.parse_args()

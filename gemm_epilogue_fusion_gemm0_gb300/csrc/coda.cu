@@ -138,6 +138,26 @@ static auto* const kPairSwigluBwd = &gemm_pair_epilogue_kernel<EpiSwiGLUBackward
 static auto* const kDgradGivenS = &gemm_epilogue_kernel<EpiRmsNormBackwardGivenS, false>;
 static auto* const kPairDgradGivenS = &gemm_pair_epilogue_kernel<EpiRmsNormBackwardGivenS, false>;
 
+// dynamic shared memory of each kernel (ring, barriers, the policy's staging buffers)
+constexpr uint32_t kGemm0Smem = cta_smem_bytes<EpiResidualGammaSumsq>();
+constexpr uint32_t kGemm1Smem = cta_smem_bytes<EpiRowScale>();
+constexpr uint32_t kDgradSmem = cta_smem_bytes<EpiRmsNormBackward>();
+constexpr uint32_t kPairGemm0Smem = pair_smem_bytes<EpiResidualGammaSumsq>();
+constexpr uint32_t kPairGemm1Smem = pair_smem_bytes<EpiRowScale>();
+constexpr uint32_t kPairDgradSmem = pair_smem_bytes<EpiRmsNormBackward>();
+constexpr uint32_t kGemm1SwigluSmem = cta_smem_bytes<EpiRowScaleSwiGLU>();
+constexpr uint32_t kPairGemm1SwigluSmem = pair_smem_bytes<EpiRowScaleSwiGLU>();
+constexpr uint32_t kSwigluBwdSmem = cta_smem_bytes<EpiSwiGLUBackward>();
+constexpr uint32_t kWgradSmem = cta_smem_bytes<EpiStoreF32>();
+constexpr uint32_t kPairGemm0F8Smem = pair_smem_bytes<EpiResidualGammaSumsqFp8>();
+constexpr uint32_t kPairGemm1F8Smem = pair_smem_bytes<EpiRowScaleFp8>();
+constexpr uint32_t kPairWgradSmem = pair_smem_bytes<EpiStoreF32>();
+constexpr uint32_t kXgradSmem = cta_smem_bytes<EpiRowScale>();
+constexpr uint32_t kPairXgradSmem = pair_smem_bytes<EpiRowScale>();
+constexpr uint32_t kPairSwigluBwdSmem = pair_smem_bytes<EpiSwiGLUBackward>();
+constexpr uint32_t kDgradGivenSSmem = cta_smem_bytes<EpiRmsNormBackwardGivenS>();
+constexpr uint32_t kPairDgradGivenSSmem = pair_smem_bytes<EpiRmsNormBackwardGivenS>();
+
 }  // namespace coda
 
 // ---------------------------------------------------------------------------
@@ -201,46 +221,46 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
     } else {
       bool ok = true;
       ok &= cudaFuncSetAttribute(kGemm0, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kGemm0Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kGemm1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kGemm1Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kDgradSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairGemm0, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairGemm0Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairGemm1, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairGemm1Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairDgradSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kGemm1SwigluSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairGemm1SwigluSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kSwigluBwdSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kWgradSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairGemm0F8, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairGemm0F8Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairGemm1F8, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairGemm1F8Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairWgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairWgradSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kXgradSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairXgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairXgradSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairSwigluBwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairSwigluBwdSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) == cudaSuccess;
+                                 kDgradGivenSSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairDgradGivenS, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kPairSmemBytes) == cudaSuccess;
+                                 kPairDgradGivenSSmem) == cudaSuccess;
       if (ok) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (count / 2));
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kPairSmemBytes;
+        cfg.dynamicSmemBytes = kPairDgradSmem;
         int clusters = 0;
         if (cudaOccupancyMaxActiveClusters(&clusters, kPairDgrad, &cfg) == cudaSuccess)
           s.max_pairs = std::min(clusters, count / 2);
@@ -396,9 +416,9 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   p0.part = ws.part;
   const int mtp = static_cast<int>(cdiv(M, kPairBM));
   cudaError_t e =
-      pair ? launch(kPairGemm0, 2 * std::min(max_pairs, mtp * nt0), kThreads, kPairSmemBytes,
+      pair ? launch(kPairGemm0, 2 * std::min(max_pairs, mtp * nt0), kThreads, kPairGemm0Smem,
                     stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, tmo)
-           : launch(kGemm0, std::min(sms, mt * nt0), kThreads, kSmemBytes, stream, false, mA0,
+           : launch(kGemm0, std::min(sms, mt * nt0), kThreads, kGemm0Smem, stream, false, mA0,
                     mB0, Mi, di, di, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -432,17 +452,18 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
     e = pair ? launch(kPairGemm1Swiglu, 2 * std::min(max_pairs, mtp * nt1), kThreads,
-                      kPairSmemBytes, stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, tmo)
-             : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false,
-                      mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
+                      kPairGemm1SwigluSmem, stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM,
+                      ps, tmo)
+             : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kGemm1SwigluSmem,
+                      stream, false, mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
   } else {
     EpiRowScale::Params p1 = {};
     p1.r = fused ? r_out : nullptr;
     p1.fold = fold;
     p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
-    e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes,
+    e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairGemm1Smem,
                       stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
-             : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kSmemBytes, stream, false, mA1,
+             : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kGemm1Smem, stream, false, mA1,
                       mB1, Mi, N1i, di, kGroupM, p1, tmo);
   }
   if (e != cudaSuccess) {
@@ -544,10 +565,10 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   if (tok == 0) tok = 1;
   p.token = tok;
   cudaError_t e =
-      pair ? launch(kPairDgrad, 2 * units, kThreads, kPairSmemBytes, stream, true, mA, mB,
+      pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                     g_timeout_ns.load())
-           : launch(kDgrad, units, kThreads, kSmemBytes, stream, true, mA, mB,
+           : launch(kDgrad, units, kThreads, kDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                     g_timeout_ns.load());
   if (e != cudaSuccess) {
@@ -613,7 +634,8 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   p0.acc_scale = sx * sW0;
   p0.inv_s_hg = 1.0f / s_hg;
   cudaError_t e = launch(kPairGemm0F8, 2 * std::min(max_pairs, mtp * nt0), kThreads,
-                         kPairSmemBytes, stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, tmo);
+                         kPairGemm0F8Smem, stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0,
+                         tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -630,7 +652,7 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   p1.r = r_out;
   p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
   p1.scale = s_hg * sW1;
-  e = launch(kPairGemm1F8, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairSmemBytes, stream,
+  e = launch(kPairGemm1F8, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairGemm1F8Smem, stream,
              false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -712,9 +734,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
-  cudaError_t e = pair ? launch(kPairDgrad, 2 * units, kThreads, kPairSmemBytes, stream, true,
+  cudaError_t e = pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true,
                                 mDy, mW1, Mi, di, N1i, 1, p, tmo)
-                       : launch(kDgrad, units, kThreads, kSmemBytes, stream, true, mDy, mW1, Mi,
+                       : launch(kDgrad, units, kThreads, kDgradSmem, stream, true, mDy, mW1, Mi,
                                 di, N1i, 1, p, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -734,9 +756,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   pw1.out = dW1_out;
   const int mtw = static_cast<int>(cdiv(d, pair ? kPairBM : kBM));
   const int ntw1 = static_cast<int>(cdiv(N1, kBN));
-  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, kPairSmemBytes,
+  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, kPairWgradSmem,
                     stream, false, mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, tmo)
-           : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kSmemBytes, stream, false, mH2,
+           : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kWgradSmem, stream, false, mH2,
                     mDyMN, di, N1i, Mi, kGroupM, pw1, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -748,9 +770,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   px.r = nullptr;
   px.y_out = reinterpret_cast<__nv_bfloat16*>(dx_out);
   const int mtx = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
-  e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, kPairSmemBytes,
+  e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, kPairXgradSmem,
                     stream, false, mDh, mW0, Mi, di, di, kPairGroupM, px, tmo)
-           : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kSmemBytes, stream, false, mDh,
+           : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kXgradSmem, stream, false, mDh,
                     mW0, Mi, di, di, kGroupM, px, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -760,9 +782,9 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   // 5. dW0 = x^T dh   (K = tokens)
   EpiStoreF32::Params pw0 = {};
   pw0.out = dW0_out;
-  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, kPairSmemBytes,
+  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, kPairWgradSmem,
                     stream, false, mX, mDhMN, di, di, Mi, kPairGroupM, pw0, tmo)
-           : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kSmemBytes, stream, false, mX,
+           : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kWgradSmem, stream, false, mX,
                     mDhMN, di, di, Mi, kGroupM, pw0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -826,10 +848,11 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   p0.dy_out = reinterpret_cast<__nv_bfloat16*>(dy_out);
   p0.spart = reinterpret_cast<float*>(workspace);
   cudaError_t e =
-      pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads, kPairSmemBytes,
-                    stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM, p0, tmo)
-           : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, kSmemBytes, stream, false, mA0,
-                    mB0, Mi, halfi, Douti, kGroupM, p0, tmo);
+      pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads,
+                    kPairSwigluBwdSmem, stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM,
+                    p0, tmo)
+           : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, kSwigluBwdSmem, stream, false,
+                    mA0, mB0, Mi, halfi, Douti, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -850,10 +873,11 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   p1.r = r;
   p1.s = s_out;
   p1.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
-  e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads, kPairSmemBytes,
-                    stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, tmo)
-           : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kSmemBytes, stream, false,
-                    mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
+  e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads,
+                    kPairDgradGivenSSmem, stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1,
+                    tmo)
+           : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kDgradGivenSSmem, stream,
+                    false, mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -1033,7 +1057,7 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
   uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
   if (tok == 0) tok = 1;
   p.token = tok;
-  cudaError_t e = launch(kDgrad, grid, kThreads, kSmemBytes, stream, true, mA, mB,
+  cudaError_t e = launch(kDgrad, grid, kThreads, kDgradSmem, stream, true, mA, mB,
                          static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                          g_timeout_ns.load());
   if (e != cudaSuccess) {

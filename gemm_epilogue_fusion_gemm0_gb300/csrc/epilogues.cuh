@@ -8,6 +8,11 @@
 // (bit-reproducible results).  Partials are stored [2 * nt][M], index
 // 2 * nb + half.
 //
+// Rank-2 operand tiles and outputs move between global memory and registers
+// through a per-warp shared-memory staging buffer (Stage below), so that the
+// global accesses are whole row segments rather than one 16-byte piece of 32
+// different rows per instruction.
+//
 // The primitives used are the method's tile-local ones (CODA blog,
 // blog.hotdry.top, section "五类 Epilogue 原语"): an elementwise map (residual
 // add), a rank-1 vector broadcast (gamma, the per-row r), rank-2 tile loads and
@@ -32,24 +37,6 @@ struct EpiDefaultCols {
   static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N + kBN - 1) / kBN; }
   static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
 };
-
-// Loads the four 8-element groups [n0 + 8q, n0 + 8q + 8) of row `rowp` (q = 0..3);
-// groups at or past `limit` (or all of them when !ok) read as zeros.  Issued for
-// the next 32-column chunk before the current one is processed, so global-load
-// latency overlaps the epilogue arithmetic.
-__device__ __forceinline__ void ldg_chunk(const __nv_bfloat16* rowp, int n0, int limit, bool ok,
-                                          Chunk8 (&out)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int n = n0 + q * 8;
-    if (ok && n < limit) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(rowp + n));
-      out[q] = Chunk8{{v.x, v.y, v.z, v.w}};
-    } else {
-      out[q] = Chunk8{{0u, 0u, 0u, 0u}};
-    }
-  }
-}
 
 // r[m] = rsqrt(sum of the row's h^2 partials / d + eps), summed in the same
 // order and with the same expression as the stand-alone row-reduction kernel,
@@ -84,6 +71,117 @@ __device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// p[n .. n + 8), or zeros at or past `limit` (the end of the row)
+__device__ __forceinline__ Chunk8 ldg8_or0(const __nv_bfloat16* p, int n, int limit) {
+  return n < limit ? ldg8(p + n) : Chunk8{{0u, 0u, 0u, 0u}};
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp staging of rank-2 blocks: 32 rows (one per lane) x kRowBytes.
+//
+// Directly, a thread that owns a row moves 16 bytes of it per instruction, so
+// every warp-wide access touches 32 rows: 32 half-used sectors and 32 L1
+// wavefronts.  Staged, the warp moves whole row segments instead (kRowBytes
+// contiguous bytes of 32 / (kRowBytes / 16) rows per instruction) and each
+// lane exchanges its own row with shared memory.  The 16-byte group g of
+// staged row r sits at r * kRowBytes + 16 * (g ^ ((r / kSwz) & (kGroups - 1))),
+// which keeps both the row-wise and the segment-wise accesses free of bank
+// conflicts.  Rows at or past `rows` and bytes at or past `valid` are neither
+// read from nor written to global memory (loads give zeros there).
+// A block moves in one direction at a time: load -> __syncwarp -> get, or
+// put -> __syncwarp -> flush, and a __syncwarp separates a flush or a get from
+// the next load or put that reuses the buffer (each lane's get and put touch
+// only its own row, so a get followed by a put needs none).
+// ---------------------------------------------------------------------------
+template <uint32_t kRowBytes>
+struct Stage {
+  static constexpr uint32_t kGroups = kRowBytes / 16;     // 16-byte groups per row
+  static constexpr uint32_t kRowsPerPass = 32 / kGroups;  // rows one warp-wide access covers
+  static constexpr uint32_t kSwz = 8 / kGroups;           // rows sharing one swizzle value
+  static constexpr uint32_t kBytes = 32 * kRowBytes;
+  static constexpr int kWords = kRowBytes / 4;
+  static_assert(kGroups == 2 || kGroups == 4 || kGroups == 8, "32, 64 or 128-byte rows");
+
+  static __device__ __forceinline__ uint32_t at(uint32_t buf, uint32_t r, uint32_t g) {
+    return buf + r * kRowBytes + 16u * (g ^ ((r / kSwz) & (kGroups - 1)));
+  }
+
+  // this lane's row -> staging buffer
+  static __device__ __forceinline__ void put(uint32_t buf, const uint32_t (&w)[kWords]) {
+    const uint32_t r = threadIdx.x & 31u;
+#pragma unroll
+    for (uint32_t g = 0; g < kGroups; ++g)
+      st_shared_v4(at(buf, r, g), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  }
+
+  // staging buffer -> this lane's row
+  static __device__ __forceinline__ void get(uint32_t buf, uint32_t (&w)[kWords]) {
+    const uint32_t r = threadIdx.x & 31u;
+#pragma unroll
+    for (uint32_t g = 0; g < kGroups; ++g) {
+      const uint4 v = ld_shared_v4(at(buf, r, g));
+      w[4 * g] = v.x;
+      w[4 * g + 1] = v.y;
+      w[4 * g + 2] = v.z;
+      w[4 * g + 3] = v.w;
+    }
+  }
+
+  // global block (staged row i at src + i * pitch bytes) -> staging buffer
+  static __device__ __forceinline__ void load(uint32_t buf, const void* src, size_t pitch,
+                                              int rows, int valid) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t g = lane % kGroups;
+    const char* s = static_cast<const char*>(src);
+    uint4 v[kGroups];
+#pragma unroll
+    for (uint32_t i = 0; i < kGroups; ++i) {
+      const uint32_t r = i * kRowsPerPass + lane / kGroups;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid)
+        v[i] = __ldg(reinterpret_cast<const uint4*>(s + r * pitch + 16u * g));
+    }
+#pragma unroll
+    for (uint32_t i = 0; i < kGroups; ++i) {
+      const uint32_t r = i * kRowsPerPass + lane / kGroups;
+      st_shared_v4(at(buf, r, g), v[i].x, v[i].y, v[i].z, v[i].w);
+    }
+  }
+
+  // staging buffer -> global block (staged row i at dst + i * pitch bytes)
+  static __device__ __forceinline__ void flush(uint32_t buf, void* dst, size_t pitch, int rows,
+                                               int valid) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t g = lane % kGroups;
+    char* d = static_cast<char*>(dst);
+#pragma unroll
+    for (uint32_t i = 0; i < kGroups; ++i) {
+      const uint32_t r = i * kRowsPerPass + lane / kGroups;
+      const uint4 v = ld_shared_v4(at(buf, r, g));
+      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid)
+        *reinterpret_cast<uint4*>(d + r * pitch + 16u * g) = v;
+    }
+  }
+};
+
+using Stage32 = Stage<32>;    // 32 one-byte columns (FP8 codes)
+using Stage64 = Stage<64>;    // 32 bf16 columns
+using Stage128 = Stage<128>;  // 32 fp32 columns
+
+// This warp's block of rows: the first one and how many exist (at most 32).
+struct WarpRows {
+  int row0, rows;
+  __device__ __forceinline__ explicit WarpRows(const TileCtx& c) {
+    row0 = c.mb * kBM + (c.row & ~31);
+    rows = min(32, c.M - row0);
+  }
+};
+
+// Bytes of the 32 columns starting at n0 that lie below column `limit`.
+__device__ __forceinline__ int valid_bytes(int n0, int limit, int esize) {
+  return max(0, min(32, limit - n0)) * esize;
+}
+
 // ---------------------------------------------------------------------------
 // GEMM0 epilogue (step 1 of the reparameterisation, CODA blog section
 // "GEMM-Residual-RMSNorm-GEMM 重参数化"): residual add, gamma scaling and the
@@ -95,6 +193,8 @@ __device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
 // epilogue of the unfused reference sequence.
 // ---------------------------------------------------------------------------
 struct EpiResidualGammaSumsq : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = 2 * Stage64::kBytes;  // z, then h; hg
+
   struct Params {
     const __nv_bfloat16* z;
     const __nv_bfloat16* gamma;
@@ -105,41 +205,45 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
-    const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const WarpRows wr(c);
     const bool fused = p.hg_out != nullptr;
+    const size_t pitch = static_cast<size_t>(c.N) * 2;
+    const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
+      const int valid = valid_bytes(n0, c.N, 2);
+      const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
+      Stage64::load(buf0, p.z + off, pitch, wr.rows, valid);
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      if (row_ok) {
+      __syncwarp();
+      uint32_t zr[16], hw[16], hgw[16];
+      Stage64::get(buf0, zr);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            const Chunk8 zz = ldg8(p.z + rowoff + n);
-            const Chunk8 gg = ldg8(p.gamma + n);
-            uint32_t hw[4], hgw[4];
+      for (int g = 0; g < 4; ++g) {
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zz.w[e]);
-              const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zz.w[e]);
-              ss = fmaf(h0, h0, ss);
-              ss = fmaf(h1, h1, ss);
-              hw[e] = pack_bf16x2(h0, h1);
-              hgw[e] = pack_bf16x2(h0 * bf16lo(gg.w[e]), h1 * bf16hi(gg.w[e]));
-            }
-            stg8(p.h_out + rowoff + n, hw);
-            if (fused) stg8(p.hg_out + rowoff + n, hgw);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zr[4 * g + e]);
+          const float h1 = __uint_as_float(v[g * 8 + 2 * e + 1]) + bf16hi(zr[4 * g + e]);
+          ss = fmaf(h0, h0, ss);  // h is zero past the last row and column
+          ss = fmaf(h1, h1, ss);
+          hw[4 * g + e] = pack_bf16x2(h0, h1);
+          hgw[4 * g + e] = pack_bf16x2(h0 * bf16lo(gg.w[e]), h1 * bf16hi(gg.w[e]));
         }
       }
+      Stage64::put(buf0, hw);
+      if (fused) Stage64::put(buf1, hgw);
+      __syncwarp();
+      Stage64::flush(buf0, p.h_out + off, pitch, wr.rows, valid);
+      if (fused) Stage64::flush(buf1, p.hg_out + off, pitch, wr.rows, valid);
+      __syncwarp();
     }
-    if (row_ok && p.part != nullptr) p.part[partial_index(c, m)] = ss;
+    if (m < c.M && p.part != nullptr) p.part[partial_index(c, m)] = ss;
   }
 };
 
@@ -147,30 +251,27 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
 // Plain fp32 store (weight gradients): out[m, n] = acc.
 // ---------------------------------------------------------------------------
 struct EpiStoreF32 : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = Stage128::kBytes;
+
   struct Params {
     float* out;  // [M, N] row-major
   };
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
-    const int m = c.mb * kBM + c.row;
-    const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const WarpRows wr(c);
+    const size_t pitch = static_cast<size_t>(c.N) * 4;
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
-      if (row_ok) {
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const int n = n0 + g * 4;
-          if (n < c.N)
-            *reinterpret_cast<uint4*>(p.out + rowoff + n) =
-                make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-        }
-      }
+      Stage128::put(c.stage, v);
+      __syncwarp();
+      Stage128::flush(c.stage, p.out + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
+                      valid_bytes(n0, c.N, 4));
+      __syncwarp();
     }
   }
 };
@@ -181,6 +282,8 @@ struct EpiStoreF32 : EpiDefaultCols {
 // reference sequence.
 // ---------------------------------------------------------------------------
 struct EpiRowScale : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = Stage64::kBytes;
+
   struct Params {
     const float* r;  // [M], may be null (scale 1)
     __nv_bfloat16* y_out;
@@ -190,7 +293,8 @@ struct EpiRowScale : EpiDefaultCols {
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const WarpRows wr(c);
+    const size_t pitch = static_cast<size_t>(c.N) * 2;
     float rr = 1.f;
     if (row_ok && p.fold.part != nullptr) {
       rr = folded_rsqrt(p.fold, m, c.M);
@@ -201,24 +305,19 @@ struct EpiRowScale : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
-      if (row_ok) {
+      uint32_t yw[16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            uint32_t yw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              yw[e] = pack_bf16x2(rr * __uint_as_float(v[g * 8 + 2 * e]),
-                                  rr * __uint_as_float(v[g * 8 + 2 * e + 1]));
-            stg8(p.y_out + rowoff + n, yw);
-          }
-        }
-      }
+      for (int e = 0; e < 16; ++e)
+        yw[e] = pack_bf16x2(rr * __uint_as_float(v[2 * e]), rr * __uint_as_float(v[2 * e + 1]));
+      Stage64::put(c.stage, yw);
+      __syncwarp();
+      Stage64::flush(c.stage, p.y_out + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
+                     valid_bytes(n0, c.N, 2));
+      __syncwarp();
     }
   }
 };
@@ -237,6 +336,8 @@ struct EpiRowScale : EpiDefaultCols {
 // depends only on tiles with smaller index and cannot deadlock.
 // ---------------------------------------------------------------------------
 struct EpiRmsNormBackward : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = 2 * Stage64::kBytes;  // h / dh; dh_res / h2
+
   struct Params {
     const __nv_bfloat16* h;
     const __nv_bfloat16* gamma;
@@ -255,30 +356,32 @@ struct EpiRmsNormBackward : EpiDefaultCols {
                                                const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const WarpRows wr(c);
+    const size_t pitch = static_cast<size_t>(c.N) * 2;
+    const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
 
     float qp = 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
+      Stage64::load(buf0, p.h + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
+                    valid_bytes(n0, c.N, 2));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
-      if (row_ok) {
+      __syncwarp();
+      uint32_t hr[16];
+      Stage64::get(buf0, hr);
+      __syncwarp();  // every lane has its row before the buffer is refilled
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            const Chunk8 hh = ldg8(p.h + rowoff + n);
-            const Chunk8 gg = ldg8(p.gamma + n);
+      for (int g = 0; g < 4; ++g) {
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              qp = fmaf(__uint_as_float(v[g * 8 + 2 * e]) * bf16lo(gg.w[e]), bf16lo(hh.w[e]), qp);
-              qp = fmaf(__uint_as_float(v[g * 8 + 2 * e + 1]) * bf16hi(gg.w[e]), bf16hi(hh.w[e]),
-                        qp);
-            }
-          }
+        for (int e = 0; e < 4; ++e) {
+          qp = fmaf(__uint_as_float(v[g * 8 + 2 * e]) * bf16lo(gg.w[e]), bf16lo(hr[4 * g + e]), qp);
+          qp = fmaf(__uint_as_float(v[g * 8 + 2 * e + 1]) * bf16hi(gg.w[e]), bf16hi(hr[4 * g + e]),
+                    qp);
         }
       }
     }
@@ -297,7 +400,7 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     named_bar_sync(1, kEpiThreads);
 
     float q = 0.f;
-    float rr = 0.f;
+    float rr = 0.f;  // stays 0 past the last row: no dgamma contribution there
     if (row_ok) {
       for (int j = 0; j < 2 * c.nt; ++j) q += __ldcg(p.qpart + static_cast<size_t>(j) * c.M + m);
       rr = __ldg(p.r + m);
@@ -308,41 +411,44 @@ struct EpiRmsNormBackward : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
+      const int valid = valid_bytes(n0, c.N, 2);
+      const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
+      Stage64::load(buf0, p.h + off, pitch, wr.rows, valid);
+      if (p.dh_res != nullptr) Stage64::load(buf1, p.dh_res + off, pitch, wr.rows, valid);
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
+      __syncwarp();
+      uint32_t hr[16], rs[16], dw[16], h2w[16];
+      Stage64::get(buf0, hr);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) rs[i] = 0u;
+      if (p.dh_res != nullptr) Stage64::get(buf1, rs);
       float t[32];  // r * h * grad_h2: this row's contribution to dgamma
 #pragma unroll
-      for (int i = 0; i < 32; ++i) t[i] = 0.f;
-      if (row_ok) {
+      for (int g = 0; g < 4; ++g) {
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            const Chunk8 hh = ldg8(p.h + rowoff + n);
-            const Chunk8 gg = ldg8(p.gamma + n);
-            Chunk8 rs = {{0u, 0u, 0u, 0u}};
-            if (p.dh_res != nullptr) rs = ldg8(p.dh_res + rowoff + n);
-            uint32_t dw[4], h2w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a0 = __uint_as_float(v[g * 8 + 2 * e]);
-              const float a1 = __uint_as_float(v[g * 8 + 2 * e + 1]);
-              const float h0 = bf16lo(hh.w[e]), h1 = bf16hi(hh.w[e]);
-              const float g0 = bf16lo(gg.w[e]), g1 = bf16hi(gg.w[e]);
-              const float d0 = rr * g0 * a0 - coef * h0 + bf16lo(rs.w[e]);
-              const float d1 = rr * g1 * a1 - coef * h1 + bf16hi(rs.w[e]);
-              dw[e] = pack_bf16x2(d0, d1);
-              h2w[e] = pack_bf16x2(rr * h0 * g0, rr * h1 * g1);
-              t[g * 8 + 2 * e] = rr * h0 * a0;
-              t[g * 8 + 2 * e + 1] = rr * h1 * a1;
-            }
-            stg8(p.dh_out + rowoff + n, dw);
-            if (p.h2_out != nullptr) stg8(p.h2_out + rowoff + n, h2w);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = __uint_as_float(v[g * 8 + 2 * e]);
+          const float a1 = __uint_as_float(v[g * 8 + 2 * e + 1]);
+          const float h0 = bf16lo(hr[4 * g + e]), h1 = bf16hi(hr[4 * g + e]);
+          const float g0 = bf16lo(gg.w[e]), g1 = bf16hi(gg.w[e]);
+          const float d0 = rr * g0 * a0 - coef * h0 + bf16lo(rs[4 * g + e]);
+          const float d1 = rr * g1 * a1 - coef * h1 + bf16hi(rs[4 * g + e]);
+          dw[4 * g + e] = pack_bf16x2(d0, d1);
+          h2w[4 * g + e] = pack_bf16x2(rr * h0 * g0, rr * h1 * g1);
+          t[g * 8 + 2 * e] = rr * h0 * a0;
+          t[g * 8 + 2 * e + 1] = rr * h1 * a1;
         }
       }
+      Stage64::put(buf0, dw);
+      if (p.h2_out != nullptr) Stage64::put(buf1, h2w);
+      __syncwarp();
+      Stage64::flush(buf0, p.dh_out + off, pitch, wr.rows, valid);
+      if (p.h2_out != nullptr) Stage64::flush(buf1, p.h2_out + off, pitch, wr.rows, valid);
+      __syncwarp();
       if (extras) {
         // Column sums over the warp's 32 rows: butterfly reduction; lane k ends
         // with the sum for column n0 + k.
@@ -380,6 +486,8 @@ struct EpiRmsNormBackward : EpiDefaultCols {
 __device__ __forceinline__ float silu_f(float t) { return t / (1.0f + __expf(-t)); }
 
 struct EpiRowScaleSwiGLU {
+  static constexpr uint32_t kStageBytesPerWarp = 2 * Stage64::kBytes;  // a, then up; gate
+
   struct Params {
     const float* r;         // [M]
     __nv_bfloat16* y_out;   // [M, N1] pre-activation, may be null
@@ -395,7 +503,10 @@ struct EpiRowScaleSwiGLU {
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
+    const WarpRows wr(c);
     const int half = c.N / 2;
+    const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
+    const size_t a_pitch = static_cast<size_t>(half) * 2, y_pitch = static_cast<size_t>(c.N) * 2;
     float rr = 0.f;
     if (row_ok && p.fold.part != nullptr) {
       rr = folded_rsqrt(p.fold, m, c.M);
@@ -403,40 +514,40 @@ struct EpiRowScaleSwiGLU {
     } else if (row_ok) {
       rr = __ldg(p.r + m);
     }
-    const size_t a_row = static_cast<size_t>(row_ok ? m : 0) * half;
-    const size_t y_row = static_cast<size_t>(row_ok ? m : 0) * c.N;
 #pragma unroll 1
     for (int ch = 0; ch < 2; ++ch) {  // this thread's 64 gated outputs of the tile
       const int col = c.half * 64 + ch * 32;
+      const int o0 = c.nb * 128 + col;
+      const int valid = valid_bytes(o0, half, 2);
       uint32_t g[32], u[32];
       tmem_ld32(c.taddr + col, g);
       tmem_ld32(c.taddr + 128 + col, u);
       tmem_ld_wait(g);
       tmem_ld_wait(u);
-      const int o0 = c.nb * 128 + col;
-      if (row_ok) {
+      uint32_t aw[16], gw[16], uw[16];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int o = o0 + q * 8;
-          if (o < half) {
-            uint32_t aw[4], gw[4], uw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float g0 = rr * __uint_as_float(g[q * 8 + 2 * e]);
-              const float g1 = rr * __uint_as_float(g[q * 8 + 2 * e + 1]);
-              const float u0 = rr * __uint_as_float(u[q * 8 + 2 * e]);
-              const float u1 = rr * __uint_as_float(u[q * 8 + 2 * e + 1]);
-              aw[e] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
-              gw[e] = pack_bf16x2(g0, g1);
-              uw[e] = pack_bf16x2(u0, u1);
-            }
-            stg8(p.a_out + a_row + o, aw);
-            if (p.y_out != nullptr) {
-              stg8(p.y_out + y_row + o, gw);
-              stg8(p.y_out + y_row + half + o, uw);
-            }
-          }
-        }
+      for (int e = 0; e < 16; ++e) {
+        const float g0 = rr * __uint_as_float(g[2 * e]);
+        const float g1 = rr * __uint_as_float(g[2 * e + 1]);
+        const float u0 = rr * __uint_as_float(u[2 * e]);
+        const float u1 = rr * __uint_as_float(u[2 * e + 1]);
+        aw[e] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+        gw[e] = pack_bf16x2(g0, g1);
+        uw[e] = pack_bf16x2(u0, u1);
+      }
+      const size_t y_off = static_cast<size_t>(wr.row0) * c.N + o0;
+      Stage64::put(buf0, aw);
+      if (p.y_out != nullptr) Stage64::put(buf1, gw);
+      __syncwarp();
+      Stage64::flush(buf0, p.a_out + static_cast<size_t>(wr.row0) * half + o0, a_pitch, wr.rows,
+                     valid);
+      if (p.y_out != nullptr) Stage64::flush(buf1, p.y_out + y_off, y_pitch, wr.rows, valid);
+      __syncwarp();
+      if (p.y_out != nullptr) {
+        Stage64::put(buf0, uw);
+        __syncwarp();
+        Stage64::flush(buf0, p.y_out + y_off + half, y_pitch, wr.rows, valid);
+        __syncwarp();
       }
     }
   }
@@ -453,6 +564,8 @@ struct EpiRowScaleSwiGLU {
 //   spart[2 nb + half][m] = sum over the half tile of dg * g + du * u   (fp32)
 // ---------------------------------------------------------------------------
 struct EpiSwiGLUBackward : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = 2 * Stage64::kBytes;  // g / dg; u / du
+
   struct Params {
     const __nv_bfloat16* y;  // [M, 2 * half] saved pre-activation [g | u]
     __nv_bfloat16* dy_out;   // [M, 2 * half]
@@ -461,65 +574,51 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
-    const bool row_ok = m < c.M;
+    const WarpRows wr(c);
     const int half = c.N;  // the GEMM's output width is the gated width
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * (2 * static_cast<size_t>(half));
-    const __nv_bfloat16* grow = p.y + rowoff;
-    const __nv_bfloat16* urow = p.y + rowoff + half;
-    const int jbase = c.nb * kBN + c.half * kHalfCols;
+    const size_t pitch = 2 * static_cast<size_t>(half) * 2;
+    const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
-    Chunk8 gc[4], uc[4];
-    ldg_chunk(grow, jbase, half, row_ok, gc);
-    ldg_chunk(urow, jbase, half, row_ok, uc);
-#pragma unroll
+#pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int j0 = c.nb * kBN + col;
+      const int valid = valid_bytes(j0, half, 2);
+      const size_t off = static_cast<size_t>(wr.row0) * (2 * static_cast<size_t>(half)) + j0;
+      Stage64::load(buf0, p.y + off, pitch, wr.rows, valid);
+      Stage64::load(buf1, p.y + off + half, pitch, wr.rows, valid);
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
-      Chunk8 gn[4], un[4];
-      if (ch + 1 < kHalfChunks) {
-        ldg_chunk(grow, j0 + 32, half, row_ok, gn);
-        ldg_chunk(urow, j0 + 32, half, row_ok, un);
-      }
       tmem_ld_wait(v);
-      if (row_ok) {
+      __syncwarp();
+      uint32_t gr[16], ur[16], dgw[16], duw[16];
+      Stage64::get(buf0, gr);
+      Stage64::get(buf1, ur);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j = j0 + q * 8;
-          if (j < half) {
-            uint32_t dgw[4], duw[4];
+      for (int e = 0; e < 16; ++e) {
+        float dgv[2], duv[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float dgv[2], duv[2];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const float da = __uint_as_float(v[q * 8 + 2 * e + k]);
-                const float g = k ? bf16hi(gc[q].w[e]) : bf16lo(gc[q].w[e]);
-                const float u = k ? bf16hi(uc[q].w[e]) : bf16lo(uc[q].w[e]);
-                const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
-                dgv[k] = da * u * sig * (1.0f + g * (1.0f - sig));
-                duv[k] = da * g * sig;
-                ss = fmaf(dgv[k], g, ss);
-                ss = fmaf(duv[k], u, ss);
-              }
-              dgw[e] = pack_bf16x2(dgv[0], dgv[1]);
-              duw[e] = pack_bf16x2(duv[0], duv[1]);
-            }
-            stg8(p.dy_out + rowoff + j, dgw);
-            stg8(p.dy_out + rowoff + half + j, duw);
-          }
+        for (int k = 0; k < 2; ++k) {
+          const float da = __uint_as_float(v[2 * e + k]);
+          const float g = k ? bf16hi(gr[e]) : bf16lo(gr[e]);
+          const float u = k ? bf16hi(ur[e]) : bf16lo(ur[e]);
+          const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
+          dgv[k] = da * u * sig * (1.0f + g * (1.0f - sig));
+          duv[k] = da * g * sig;
+          ss = fmaf(dgv[k], g, ss);  // da is zero past the last row and column
+          ss = fmaf(duv[k], u, ss);
         }
+        dgw[e] = pack_bf16x2(dgv[0], dgv[1]);
+        duw[e] = pack_bf16x2(duv[0], duv[1]);
       }
-      if (ch + 1 < kHalfChunks) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          gc[q] = gn[q];
-          uc[q] = un[q];
-        }
-      }
+      Stage64::put(buf0, dgw);
+      Stage64::put(buf1, duw);
+      __syncwarp();
+      Stage64::flush(buf0, p.dy_out + off, pitch, wr.rows, valid);
+      Stage64::flush(buf1, p.dy_out + off + half, pitch, wr.rows, valid);
+      __syncwarp();
     }
-    if (row_ok) p.spart[partial_index(c, m)] = ss;
+    if (m < c.M) p.spart[partial_index(c, m)] = ss;
   }
 };
 
@@ -529,6 +628,8 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
 // Purely tile-local: no cross-tile exchange, any tile order.
 // ---------------------------------------------------------------------------
 struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = Stage64::kBytes;  // h / dh
+
   struct Params {
     const __nv_bfloat16* h;
     const __nv_bfloat16* gamma;
@@ -540,50 +641,39 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
     const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const WarpRows wr(c);
+    const size_t pitch = static_cast<size_t>(c.N) * 2;
     const float rr = row_ok ? __ldg(p.r + m) : 0.f;
     const float coef = row_ok ? rr * rr * __ldg(p.s + m) / static_cast<float>(c.N) : 0.f;
-    const int nbase = c.nb * kBN + c.half * kHalfCols;
-    Chunk8 hc[4], gc[4];
-    ldg_chunk(p.h + rowoff, nbase, c.N, row_ok, hc);
-    ldg_chunk(p.gamma, nbase, c.N, row_ok, gc);
-#pragma unroll
+#pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
+      const int valid = valid_bytes(n0, c.N, 2);
+      const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
+      Stage64::load(c.stage, p.h + off, pitch, wr.rows, valid);
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
-      Chunk8 hn[4], gn[4];
-      if (ch + 1 < kHalfChunks) {
-        ldg_chunk(p.h + rowoff, n0 + 32, c.N, row_ok, hn);
-        ldg_chunk(p.gamma, n0 + 32, c.N, row_ok, gn);
-      }
       tmem_ld_wait(v);
-      if (row_ok) {
+      __syncwarp();
+      uint32_t hr[16], dw[16];
+      Stage64::get(c.stage, hr);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            uint32_t dw[4];
+      for (int g = 0; g < 4; ++g) {
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float d0 = rr * bf16lo(gc[g].w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
-                               coef * bf16lo(hc[g].w[e]);
-              const float d1 = rr * bf16hi(gc[g].w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
-                               coef * bf16hi(hc[g].w[e]);
-              dw[e] = pack_bf16x2(d0, d1);
-            }
-            stg8(p.dh_out + rowoff + n, dw);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
+                           coef * bf16lo(hr[4 * g + e]);
+          const float d1 = rr * bf16hi(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e + 1]) -
+                           coef * bf16hi(hr[4 * g + e]);
+          dw[4 * g + e] = pack_bf16x2(d0, d1);
         }
       }
-      if (ch + 1 < kHalfChunks) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          hc[q] = hn[q];
-          gc[q] = gn[q];
-        }
-      }
+      Stage64::put(c.stage, dw);
+      __syncwarp();
+      Stage64::flush(c.stage, p.dh_out + off, pitch, wr.rows, valid);
+      __syncwarp();
     }
   }
 };
@@ -601,6 +691,8 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
 }
 
 struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = Stage64::kBytes + Stage32::kBytes;  // z / h; hq
+
   struct Params {
     const __nv_bfloat16* z;
     const __nv_bfloat16* gamma;
@@ -613,48 +705,55 @@ struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
-    const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
+    const WarpRows wr(c);
+    const size_t pitch = static_cast<size_t>(c.N) * 2;
+    const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
+      const int valid = valid_bytes(n0, c.N, 2);
+      const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
+      Stage64::load(buf0, p.z + off, pitch, wr.rows, valid);
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      if (row_ok) {
+      __syncwarp();
+      uint32_t zr[16], hw[16], qw[8];
+      Stage64::get(buf0, zr);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            const Chunk8 zz = ldg8(p.z + rowoff + n);
-            const Chunk8 gg = ldg8(p.gamma + n);
-            uint32_t hw[4];
-            float q[8];
+      for (int g = 0; g < 4; ++g) {
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
+        float q[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float h0 = __uint_as_float(v[g * 8 + 2 * e]) * p.acc_scale + bf16lo(zz.w[e]);
-              const float h1 =
-                  __uint_as_float(v[g * 8 + 2 * e + 1]) * p.acc_scale + bf16hi(zz.w[e]);
-              ss = fmaf(h0, h0, ss);
-              ss = fmaf(h1, h1, ss);
-              hw[e] = pack_bf16x2(h0, h1);
-              q[2 * e] = h0 * bf16lo(gg.w[e]) * p.inv_s_hg;
-              q[2 * e + 1] = h1 * bf16hi(gg.w[e]) * p.inv_s_hg;
-            }
-            stg8(p.h_out + rowoff + n, hw);
-            *reinterpret_cast<uint2*>(p.hq_out + rowoff + n) =
-                make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]), pack_e4m3x4(q[4], q[5], q[6], q[7]));
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float h0 = __uint_as_float(v[g * 8 + 2 * e]) * p.acc_scale + bf16lo(zr[4 * g + e]);
+          const float h1 =
+              __uint_as_float(v[g * 8 + 2 * e + 1]) * p.acc_scale + bf16hi(zr[4 * g + e]);
+          ss = fmaf(h0, h0, ss);  // h is zero past the last row and column
+          ss = fmaf(h1, h1, ss);
+          hw[4 * g + e] = pack_bf16x2(h0, h1);
+          q[2 * e] = h0 * bf16lo(gg.w[e]) * p.inv_s_hg;
+          q[2 * e + 1] = h1 * bf16hi(gg.w[e]) * p.inv_s_hg;
         }
+        qw[2 * g] = pack_e4m3x4(q[0], q[1], q[2], q[3]);
+        qw[2 * g + 1] = pack_e4m3x4(q[4], q[5], q[6], q[7]);
       }
+      Stage64::put(buf0, hw);
+      Stage32::put(buf1, qw);
+      __syncwarp();
+      Stage64::flush(buf0, p.h_out + off, pitch, wr.rows, valid);
+      Stage32::flush(buf1, p.hq_out + off, static_cast<size_t>(c.N), wr.rows, valid / 2);
+      __syncwarp();
     }
-    if (row_ok) p.part[partial_index(c, m)] = ss;
+    if (m < c.M) p.part[partial_index(c, m)] = ss;
   }
 };
 
 struct EpiRowScaleFp8 : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = Stage64::kBytes;
+
   struct Params {
     const float* r;  // [M]
     __nv_bfloat16* y_out;
@@ -663,30 +762,25 @@ struct EpiRowScaleFp8 : EpiDefaultCols {
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl&, const TileCtx& c) {
     const int m = c.mb * kBM + c.row;
-    const bool row_ok = m < c.M;
-    const size_t rowoff = static_cast<size_t>(row_ok ? m : 0) * c.N;
-    const float rr = row_ok ? __ldg(p.r + m) * p.scale : 0.f;
+    const WarpRows wr(c);
+    const size_t pitch = static_cast<size_t>(c.N) * 2;
+    const float rr = m < c.M ? __ldg(p.r + m) * p.scale : 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
+      const int n0 = c.nb * kBN + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
-      const int n0 = c.nb * kBN + col;
-      if (row_ok) {
+      uint32_t yw[16];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 8;
-          if (n < c.N) {
-            uint32_t yw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              yw[e] = pack_bf16x2(rr * __uint_as_float(v[g * 8 + 2 * e]),
-                                  rr * __uint_as_float(v[g * 8 + 2 * e + 1]));
-            stg8(p.y_out + rowoff + n, yw);
-          }
-        }
-      }
+      for (int e = 0; e < 16; ++e)
+        yw[e] = pack_bf16x2(rr * __uint_as_float(v[2 * e]), rr * __uint_as_float(v[2 * e + 1]));
+      Stage64::put(c.stage, yw);
+      __syncwarp();
+      Stage64::flush(c.stage, p.y_out + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
+                     valid_bytes(n0, c.N, 2));
+      __syncwarp();
     }
   }
 };

@@ -36,6 +36,7 @@ constexpr int kBK = 64;
 constexpr int kStages = 4;
 constexpr int kThreads = 320;       // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kEpiFirstThread = 64;
 constexpr uint32_t kAStageBytes = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kBStageBytes = kBN * kBK * 2;   // 32 KB
@@ -51,6 +52,14 @@ constexpr uint32_t kBarBytes = 8u * (2 * kStages + 5);
 constexpr uint32_t kSmemBytes = kSmemBar + 256 + 1024;  // barriers + 1 KB alignment slack
 
 static_assert(kBarBytes + 8 <= 256, "barrier area overflows its reserved 256 bytes");
+
+// Epilogue store staging: policies that stage their output stores through
+// shared memory (Epi::kStageBytesPerWarp > 0) get that many bytes per epilogue
+// warp right after the barrier area.
+template <class Epi>
+__host__ __device__ constexpr uint32_t cta_smem_bytes() {
+  return kSmemBytes + kEpiWarps * Epi::kStageBytesPerWarp;
+}
 
 // Serpentine K order: on odd waves of a block's persistent tile loop the
 // producer walks K backwards, so the next wave starts on the K slices that
@@ -85,6 +94,7 @@ struct TileCtx {
   int half;        // which 128-column half of the tile this thread drains (0, 1)
   int M, N;        // problem size (N = output columns)
   int nt;          // number of column tiles
+  uint32_t stage;  // this warp's store-staging buffer (shared address), if the policy has one
 };
 
 __device__ __forceinline__ bool epi_all(bool ok) {
@@ -123,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(smem + kSmemBar + kBarBytes + 4);
 
+  static_assert(cta_smem_bytes<Epi>() <= 232448, "exceeds the 227 KB per-block shared memory limit");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int mt = (M + kBM - 1) / kBM;
@@ -290,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.M = M;
       c.N = N;
       c.nt = nt;
+      c.stage = base + kSmemBar + 256u + static_cast<uint32_t>(warp - 2) * Epi::kStageBytesPerWarp;
       Epi::apply(ep, wc, c);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8u * b);

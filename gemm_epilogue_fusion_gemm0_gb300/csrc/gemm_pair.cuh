@@ -38,6 +38,12 @@ static_assert(kPairBarBytes + 8 <= 256, "barrier area overflows its reserved 256
 
 static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
+// plus the policy's store-staging buffers after the barrier area (see cta_smem_bytes)
+template <class Epi>
+__host__ __device__ constexpr uint32_t pair_smem_bytes() {
+  return kPairSmemBytes + kEpiWarps * Epi::kStageBytesPerWarp;
+}
+
 // kFp8: E4M3 operands (tcgen05 kind::f8f6f4).  A 128-byte smem row then holds
 // 128 K elements, so a stage covers K = 128 with the same bytes, each MMA
 // consumes K = 32, and an MN-major B half-tile (128 columns) is one TMA box.
@@ -64,6 +70,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag =
       reinterpret_cast<volatile uint32_t*>(smem + kPairSmemBar + kPairBarBytes + 4);
 
+  static_assert(pair_smem_bytes<Epi>() <= 232448, "exceeds the 227 KB per-block shared memory limit");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -254,6 +261,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       c.M = M;
       c.N = N;
       c.nt = nt;
+      c.stage = base + kPairSmemBar + 256u + static_cast<uint32_t>(warp - 2) * Epi::kStageBytesPerWarp;
       Epi::apply(ep, wc, c);
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
