@@ -127,7 +127,35 @@ struct Stage {
     }
   }
 
-  // global block (staged row i at src + i * pitch bytes) -> staging buffer
+  // The global half of a block load: this lane's kGroups pieces of the block
+  // (staged row i at src + i * pitch bytes) into registers.  Issued a chunk
+  // ahead, its latency overlaps the work on the current chunk.
+  static __device__ __forceinline__ void fetch(uint4 (&v)[kGroups], const void* src, size_t pitch,
+                                               int rows, int valid) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t g = lane % kGroups;
+    const char* s = static_cast<const char*>(src);
+#pragma unroll
+    for (uint32_t i = 0; i < kGroups; ++i) {
+      const uint32_t r = i * kRowsPerPass + lane / kGroups;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid)
+        v[i] = __ldg(reinterpret_cast<const uint4*>(s + r * pitch + 16u * g));
+    }
+  }
+
+  // The shared half: the fetched pieces into the staging buffer.
+  static __device__ __forceinline__ void deposit(uint32_t buf, const uint4 (&v)[kGroups]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t g = lane % kGroups;
+#pragma unroll
+    for (uint32_t i = 0; i < kGroups; ++i) {
+      const uint32_t r = i * kRowsPerPass + lane / kGroups;
+      st_shared_v4(at(buf, r, g), v[i].x, v[i].y, v[i].z, v[i].w);
+    }
+  }
+
+  // global block -> staging buffer (fetch, then deposit)
   static __device__ __forceinline__ void load(uint32_t buf, const void* src, size_t pitch,
                                               int rows, int valid) {
     const uint32_t lane = threadIdx.x & 31u;
@@ -210,13 +238,19 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
     const size_t pitch = static_cast<size_t>(c.N) * 2;
     const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
+    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    const size_t rbase = static_cast<size_t>(wr.row0) * c.N;
+    uint4 zf[Stage64::kGroups];  // the next chunk's z block, in flight during this chunk
+    Stage64::fetch(zf, p.z + rbase + nbase, pitch, wr.rows, valid_bytes(nbase, c.N, 2));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
       const int valid = valid_bytes(n0, c.N, 2);
-      const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
-      Stage64::load(buf0, p.z + off, pitch, wr.rows, valid);
+      const size_t off = rbase + n0;
+      Stage64::deposit(buf0, zf);
+      if (ch + 1 < kHalfChunks)
+        Stage64::fetch(zf, p.z + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.N, 2));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
@@ -709,13 +743,19 @@ struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
     const size_t pitch = static_cast<size_t>(c.N) * 2;
     const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
+    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    const size_t rbase = static_cast<size_t>(wr.row0) * c.N;
+    uint4 zf[Stage64::kGroups];  // the next chunk's z block, in flight during this chunk
+    Stage64::fetch(zf, p.z + rbase + nbase, pitch, wr.rows, valid_bytes(nbase, c.N, 2));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
       const int valid = valid_bytes(n0, c.N, 2);
-      const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
-      Stage64::load(buf0, p.z + off, pitch, wr.rows, valid);
+      const size_t off = rbase + n0;
+      Stage64::deposit(buf0, zf);
+      if (ch + 1 < kHalfChunks)
+        Stage64::fetch(zf, p.z + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.N, 2));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
