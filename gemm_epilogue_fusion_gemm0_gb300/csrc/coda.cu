@@ -125,6 +125,8 @@ static auto* const kDgrad = &gemm_epilogue_kernel<EpiRmsNormBackward, false>;
 static auto* const kPairGemm0 = &gemm_pair_epilogue_kernel<EpiResidualGammaSumsq, true>;
 static auto* const kPairGemm1 = &gemm_pair_epilogue_kernel<EpiRowScale, true>;
 static auto* const kPairDgrad = &gemm_pair_epilogue_kernel<EpiRmsNormBackward, false>;
+static auto* const kDgradFull = &gemm_epilogue_kernel<EpiRmsNormBackwardFull, false>;
+static auto* const kPairDgradFull = &gemm_pair_epilogue_kernel<EpiRmsNormBackwardFull, false>;
 static auto* const kGemm1Swiglu = &gemm_epilogue_kernel<EpiRowScaleSwiGLU, true>;
 static auto* const kPairGemm1Swiglu = &gemm_pair_epilogue_kernel<EpiRowScaleSwiGLU, true>;
 static auto* const kSwigluBwd = &gemm_epilogue_kernel<EpiSwiGLUBackward, false>;
@@ -145,6 +147,8 @@ constexpr uint32_t kDgradSmem = cta_smem_bytes<EpiRmsNormBackward>();
 constexpr uint32_t kPairGemm0Smem = pair_smem_bytes<EpiResidualGammaSumsq>();
 constexpr uint32_t kPairGemm1Smem = pair_smem_bytes<EpiRowScale>();
 constexpr uint32_t kPairDgradSmem = pair_smem_bytes<EpiRmsNormBackward>();
+constexpr uint32_t kDgradFullSmem = cta_smem_bytes<EpiRmsNormBackwardFull>();
+constexpr uint32_t kPairDgradFullSmem = pair_smem_bytes<EpiRmsNormBackwardFull>();
 constexpr uint32_t kGemm1SwigluSmem = cta_smem_bytes<EpiRowScaleSwiGLU>();
 constexpr uint32_t kPairGemm1SwigluSmem = pair_smem_bytes<EpiRowScaleSwiGLU>();
 constexpr uint32_t kSwigluBwdSmem = cta_smem_bytes<EpiSwiGLUBackward>();
@@ -232,6 +236,10 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
                                  kPairGemm1Smem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairDgrad, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kPairDgradSmem) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kDgradFull, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kDgradFullSmem) == cudaSuccess;
+      ok &= cudaFuncSetAttribute(kPairDgradFull, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPairDgradFullSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemm1SwigluSmem) == cudaSuccess;
       ok &= cudaFuncSetAttribute(kPairGemm1Swiglu, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -722,7 +730,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   if (!ok) return CODA_ERR_LAUNCH;
 
   // 1. dgrad + RMSNorm backward + residual gradient + h2 + dgamma partials
-  EpiRmsNormBackward::Params p = {};
+  EpiRmsNormBackwardFull::Params p = {};
   p.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p.r = r;
@@ -734,10 +742,10 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
-  cudaError_t e = pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true,
-                                mDy, mW1, Mi, di, N1i, 1, p, tmo)
-                       : launch(kDgrad, units, kThreads, kDgradSmem, stream, true, mDy, mW1, Mi,
-                                di, N1i, 1, p, tmo);
+  cudaError_t e = pair ? launch(kPairDgradFull, 2 * units, kThreads, kPairDgradFullSmem, stream,
+                                true, mDy, mW1, Mi, di, N1i, 1, p, tmo)
+                       : launch(kDgradFull, units, kThreads, kDgradFullSmem, stream, true, mDy, mW1,
+                                Mi, di, N1i, 1, p, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;

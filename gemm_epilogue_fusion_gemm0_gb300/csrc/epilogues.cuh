@@ -369,8 +369,11 @@ struct EpiRowScale : EpiDefaultCols {
 // row-major order with at most gridDim.x column tiles per row; then every wait
 // depends only on tiles with smaller index and cannot deadlock.
 // ---------------------------------------------------------------------------
-struct EpiRmsNormBackward : EpiDefaultCols {
-  static constexpr uint32_t kStageBytesPerWarp = 2 * Stage64::kBytes;  // h / dh; dh_res / h2
+// kExtras: the full backward's additions (dh_res, h2, dgamma partials) are
+// compiled in; the plain data gradient leaves them out and keeps fewer registers.
+template <bool kExtras>
+struct EpiRmsNormBackwardT : EpiDefaultCols {
+  static constexpr uint32_t kStageBytesPerWarp = (kExtras ? 2 : 1) * Stage64::kBytes;
 
   struct Params {
     const __nv_bfloat16* h;
@@ -380,8 +383,8 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     float* qpart;     // [2 * nt][M]
     uint64_t* flags;  // [mt][nt]
     uint64_t token;
-    // Optional extras of the full backward (all null for the plain dgrad):
-    const __nv_bfloat16* dh_res;  // [M, d] gradient reaching h through the residual; added to dh
+    // Extras of the full backward (read only with kExtras):
+    const __nv_bfloat16* dh_res;  // [M, d] gradient reaching h through the residual, or null
     __nv_bfloat16* h2_out;        // [M, d] normalised activation r * h * gamma (dW1's operand)
     float* gpart;                 // [4 * slabs][d] per-warp column partials of dgamma
   };
@@ -395,12 +398,27 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
 
     float qp = 0.f;
+    // Without the extras there are registers to spare: the next chunk's h block
+    // is fetched while the current one is processed (the last fetch of pass 1
+    // brings pass 2's first block).
+    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    uint4 hf[Stage64::kGroups];
+    if constexpr (!kExtras)
+      Stage64::fetch(hf, p.h + static_cast<size_t>(wr.row0) * c.N + nbase, pitch, wr.rows,
+                     valid_bytes(nbase, c.N, 2));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int n0 = c.nb * kBN + col;
-      Stage64::load(buf0, p.h + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
-                    valid_bytes(n0, c.N, 2));
+      if constexpr (!kExtras) {
+        Stage64::deposit(buf0, hf);
+        const int nn = ch + 1 < kHalfChunks ? n0 + 32 : nbase;
+        Stage64::fetch(hf, p.h + static_cast<size_t>(wr.row0) * c.N + nn, pitch, wr.rows,
+                       valid_bytes(nn, c.N, 2));
+      } else {
+        Stage64::load(buf0, p.h + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
+                      valid_bytes(n0, c.N, 2));
+      }
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
@@ -440,7 +458,7 @@ struct EpiRmsNormBackward : EpiDefaultCols {
       rr = __ldg(p.r + m);
     }
     const float coef = rr * rr * rr * q / static_cast<float>(c.N);
-    const bool extras = p.gpart != nullptr;
+    const bool res = kExtras && p.dh_res != nullptr;
 
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
@@ -448,8 +466,14 @@ struct EpiRmsNormBackward : EpiDefaultCols {
       const int n0 = c.nb * kBN + col;
       const int valid = valid_bytes(n0, c.N, 2);
       const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
-      Stage64::load(buf0, p.h + off, pitch, wr.rows, valid);
-      if (p.dh_res != nullptr) Stage64::load(buf1, p.dh_res + off, pitch, wr.rows, valid);
+      if constexpr (!kExtras) {
+        Stage64::deposit(buf0, hf);
+        if (ch + 1 < kHalfChunks)
+          Stage64::fetch(hf, p.h + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.N, 2));
+      } else {
+        Stage64::load(buf0, p.h + off, pitch, wr.rows, valid);
+        if (res) Stage64::load(buf1, p.dh_res + off, pitch, wr.rows, valid);
+      }
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
@@ -458,8 +482,8 @@ struct EpiRmsNormBackward : EpiDefaultCols {
       Stage64::get(buf0, hr);
 #pragma unroll
       for (int i = 0; i < 16; ++i) rs[i] = 0u;
-      if (p.dh_res != nullptr) Stage64::get(buf1, rs);
-      float t[32];  // r * h * grad_h2: this row's contribution to dgamma
+      if (res) Stage64::get(buf1, rs);
+      float t[32];  // r * h * grad_h2: this row's contribution to dgamma (kExtras)
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
@@ -469,21 +493,25 @@ struct EpiRmsNormBackward : EpiDefaultCols {
           const float a1 = __uint_as_float(v[g * 8 + 2 * e + 1]);
           const float h0 = bf16lo(hr[4 * g + e]), h1 = bf16hi(hr[4 * g + e]);
           const float g0 = bf16lo(gg.w[e]), g1 = bf16hi(gg.w[e]);
-          const float d0 = rr * g0 * a0 - coef * h0 + bf16lo(rs[4 * g + e]);
-          const float d1 = rr * g1 * a1 - coef * h1 + bf16hi(rs[4 * g + e]);
-          dw[4 * g + e] = pack_bf16x2(d0, d1);
-          h2w[4 * g + e] = pack_bf16x2(rr * h0 * g0, rr * h1 * g1);
-          t[g * 8 + 2 * e] = rr * h0 * a0;
-          t[g * 8 + 2 * e + 1] = rr * h1 * a1;
+          if constexpr (kExtras) {
+            const float d0 = rr * g0 * a0 - coef * h0 + bf16lo(rs[4 * g + e]);
+            const float d1 = rr * g1 * a1 - coef * h1 + bf16hi(rs[4 * g + e]);
+            dw[4 * g + e] = pack_bf16x2(d0, d1);
+            h2w[4 * g + e] = pack_bf16x2(rr * h0 * g0, rr * h1 * g1);
+            t[g * 8 + 2 * e] = rr * h0 * a0;
+            t[g * 8 + 2 * e + 1] = rr * h1 * a1;
+          } else {
+            dw[4 * g + e] = pack_bf16x2(rr * g0 * a0 - coef * h0, rr * g1 * a1 - coef * h1);
+          }
         }
       }
       Stage64::put(buf0, dw);
-      if (p.h2_out != nullptr) Stage64::put(buf1, h2w);
+      if (kExtras && p.h2_out != nullptr) Stage64::put(buf1, h2w);
       __syncwarp();
       Stage64::flush(buf0, p.dh_out + off, pitch, wr.rows, valid);
-      if (p.h2_out != nullptr) Stage64::flush(buf1, p.h2_out + off, pitch, wr.rows, valid);
+      if (kExtras && p.h2_out != nullptr) Stage64::flush(buf1, p.h2_out + off, pitch, wr.rows, valid);
       __syncwarp();
-      if (extras) {
+      if (kExtras && p.gpart != nullptr) {
         // Column sums over the warp's 32 rows: butterfly reduction; lane k ends
         // with the sum for column n0 + k.
         const int lane = threadIdx.x & 31;
@@ -503,6 +531,9 @@ struct EpiRmsNormBackward : EpiDefaultCols {
     }
   }
 };
+
+using EpiRmsNormBackward = EpiRmsNormBackwardT<false>;     // coda_bwd_dgrad
+using EpiRmsNormBackwardFull = EpiRmsNormBackwardT<true>;  // coda_bwd
 
 // ---------------------------------------------------------------------------
 // GEMM1 epilogue with the gated activation (CODA blog, SwiGLU gating among the
