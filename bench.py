@@ -253,7 +253,7 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 EXTRAS = ("fwd_swiglu", "other_llama_shapes", "fwd_fp8", "fwd_folded_rowreduce", "fwd_unfused",
-          "bwd_swiglu_dgrad", "bwd_full")
+          "fwd_l2_flushed", "torch_chain", "bwd_swiglu_dgrad", "bwd_full")
 
 
 def time_calls(B, stream, barrier, call, n, launches):
@@ -382,6 +382,74 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
         extras["fwd_folded_rowreduce"] = {
             "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 2 * KS,
             "note": "coda_fwd with r formed in GEMM1's epilogue (F4)"}
+
+    if "fwd_l2_flushed" in want:
+        # the forward alone with L2 flushed before every call (a 256 MB write,
+        # twice the 129 MB L2), timed per call with events on the stream
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def fwd():
+            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                       stream=stream)
+        warm(fwd)
+        n = 50
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        barrier()
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            fwd()
+            b.record(stream)
+        barrier()
+        t = sorted(a.elapsed_time(b) for a, b in evs)
+        med = statistics.median(t)
+        extras["fwd_l2_flushed"] = {
+            "ms_median": med, "tflops": tf(w.fwd_flops, med), "ms_min": t[0], "ms_max": t[-1],
+            "calls": n, "note": "coda_fwd alone, L2 flushed (256 MB write) before each call"}
+        del flush
+
+    if "torch_chain" in want:
+        # context: the same forward as plain PyTorch ops on cuBLAS (x@W0 + z, rms_norm, @W1),
+        # the unfused library sequence a framework would run; not this library's code.
+        # Timed in alternating rounds with coda_fwd so both see the same power state.
+        gam = g["gamma"]
+
+        def chain():
+            hh = torch.addmm(g["z"], g["x"], g["W0"])
+            hn = torch.nn.functional.rms_norm(hh, (d,), gam, eps)
+            return torch.mm(hn, g["W1"])
+
+        def fwd():
+            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                       stream=stream)
+
+        def timed(call, n):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            s0.record(stream)
+            for _ in range(n):
+                call()
+            s1.record(stream)
+            barrier()
+            return s0.elapsed_time(s1) / n
+
+        warm(chain)
+        warm(fwd)
+        rounds, n = 6, 20
+        t_chain, t_fwd = [], []
+        for i in range(rounds):
+            first, second = (chain, fwd) if i % 2 == 0 else (fwd, chain)
+            a, b = timed(first, n), timed(second, n)
+            t_chain.append(a if first is chain else b)
+            t_fwd.append(b if first is chain else a)
+        mc, mf = statistics.median(t_chain), statistics.median(t_fwd)
+        extras["torch_chain"] = {
+            "ms": mc, "tflops": tf(w.fwd_flops, mc), "coda_fwd_ms": mf,
+            "coda_fwd_tflops": tf(w.fwd_flops, mf), "rounds": rounds, "calls_per_round": n,
+            "torch": torch.__version__,
+            "note": "context only: torch.addmm + torch.nn.functional.rms_norm + torch.mm (cuBLAS), "
+                    "same shapes and dtypes, medians of alternating rounds with coda_fwd"}
 
     if "fwd_unfused" in want:
         # the unfused sequence of this library's own kernels: GEMM0 storing h,
@@ -617,6 +685,31 @@ def run_coda(args):
     if not torch.equal(host_out[(KE - 1) % nbuf]["dh"], dh_ref):
         raise RuntimeError("pipelined end-to-end step returned different outputs")
 
+    # The copy engines' rate with both directions busy (the step's copies alone,
+    # no compute): the bound that the pipelined form can reach is the slower of
+    # the compute and these copies.
+    def copies_only():
+        b = dbuf[0]
+        with torch.cuda.stream(s_in):
+            for k in ("x", "z", "dy"):
+                b[k].copy_(host_in[k], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for k in ("h", "r", "y", "dh"):
+                host_out[0][k].copy_(b[k], non_blocking=True)
+
+    copies_only()
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    for _ in range(3):
+        copies_only()
+    torch.cuda.synchronize()
+    copy_ms = (time.perf_counter() - c0) / 3 * 1e3
+    copy_bound = {"copy_ms_per_step": copy_ms,
+                  "copy_gbs_per_direction": max(h2d, d2h) / (copy_ms * 1e-3) / 1e9,
+                  "bound_tflops": flops_step / (max(copy_ms, ms / K) * 1e-3) / 1e12,
+                  "note": "both directions' copies of one step timed alone on the copy streams; "
+                          "e2e cannot beat the slower of these copies and the compute"}
+
     # Strict serial form: every operand, weights included, copied in and all
     # outputs copied out, one step after another on one stream.
     host_all = {k: v.pin_memory() for k, v in t.items() if k != "_rng"}
@@ -689,6 +782,7 @@ def run_coda(args):
                 "d2h_bytes_per_step": d2h, "steps": KE,
                 "form": "weights resident (model state); per step the batch x, z, dy copied in and "
                         "h, r, y, dh copied out, on copy streams overlapping compute",
+                "copy_bound": copy_bound,
                 "serial_all_operands": e2e_serial},
         "gpu_launches": 4 * K,
         "cpu_baseline": cpu,
