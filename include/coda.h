@@ -283,12 +283,14 @@ CODA_API coda_status_t coda_fwd_unfused(const coda_bf16* x, const coda_bf16* W0,
 
 /*
  * Measurement hook.  While `events` is non-NULL, every kernel launch k
- * (0-based, counted within one coda_fwd / coda_fwd_unfused / coda_bwd_dgrad
- * call) is followed by cudaEventRecord(events[k], stream) for k < n, so that
- * a caller that records its own event before the call can time each launch
- * on the launching stream.  coda_fwd launches 3 kernels (GEMM0, row
- * reduction, GEMM1), coda_bwd_dgrad 1.  The events are caller-owned; pass
- * NULL to stop.  Process-wide setting, not thread-safe; no effect on results.
+ * (0-based, counted within one call of any entry point above except
+ * coda_bwd_dgrad_noalloc) is followed by cudaEventRecord(events[k], stream)
+ * for k < n, so that a caller that records its own event before the call can
+ * time each launch on the launching stream.  coda_fwd, coda_fwd_swiglu,
+ * coda_fwd_unfused, coda_fwd_fp8 and coda_bwd_swiglu_dgrad launch 3 kernels
+ * (2 for the forwards with the folded row reduction), coda_bwd 5,
+ * coda_bwd_dgrad 1.  The events are caller-owned; pass NULL to stop.
+ * Process-wide setting, not thread-safe; no effect on results.
  */
 CODA_API void coda_set_launch_events(cudaEvent_t* events, int n);
 
@@ -309,8 +311,10 @@ CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t 
  * code running inside an allocator or memory-pool callback, runtimes that
  * forbid allocation mid-step (an allocation can synchronise the device or
  * fragment a pool sized up front), and embedders whose device memory is fully
- * reserved in advance.  It computes exactly what coda_bwd_dgrad computes, with
- * the same kernel, but takes only inputs and outputs: the per-tile partial row
+ * reserved in advance.  It computes what coda_bwd_dgrad computes, with the same
+ * epilogue program on single-CTA tiles (the coda_set_mma_mode(0) kernel; the
+ * result equals the default CTA-pair kernel's bit for bit in the tests), but
+ * takes only inputs and outputs: the per-tile partial row
  * statistics and the completion flags live in a fixed array inside the
  * library (2 * CODA_NOALLOC_MAX_PARTIALS floats + CODA_NOALLOC_MAX_TILES 64-bit
  * flags, about 4.1 MiB), which every GPU that loads the library holds until

@@ -6,9 +6,9 @@ mid-step, embedders with all device memory reserved up front).  This entry
 point keeps its scratch in a fixed array inside the library instead of a
 caller-provided workspace.  The test calls it through the C ABI twice in a
 row, on different inputs, and checks each result against coda_bwd_dgrad on
-the same inputs (same tolerance as the parity tests; the kernel is the same,
-so the results are also bit-identical), then checks that a shape beyond the
-static maximum is refused without a launch.
+the same inputs (same tolerance as the parity tests; the arithmetic is the
+same, so the results are also bit-identical), then checks that a shape beyond
+the static maximum is refused without a launch.
 
 The file name makes pytest collect it last.
 """
