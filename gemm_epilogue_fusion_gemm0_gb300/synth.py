@@ -12,6 +12,9 @@ Distributions (the Llama-shaped workloads the method is evaluated on):
 Values are drawn as float32 from one ``numpy.random.default_rng(seed)`` in the
 fixed order x, z, W0, W1, gamma (then dy), then rounded to bfloat16 with
 round-to-nearest-even.  Weights are stored [in, out] (W0 [d, d], W1 [d, N1]).
+Workloads too large to draw on the host in seconds (billions of elements) are
+drawn on the device instead by ``make_inputs_on_device``: the same
+distributions and order from a seeded torch generator (a different stream).
 """
 
 from __future__ import annotations
@@ -145,3 +148,25 @@ def sample_rows(M: int, n: int, seed: int = 1) -> np.ndarray:
     pool = np.setdiff1d(np.arange(M), np.array(must))
     extra = rng.choice(pool, size=max(0, n - len(set(must))), replace=False)
     return np.unique(np.concatenate([np.array(must, dtype=np.int64), extra]))
+
+
+def make_inputs_on_device(M: int, d: int, N1: int, seed: int, device) -> dict:
+    """bf16 tensors x, z [M,d], W0 [d,d], W1 [d,N1], gamma [d] and dy [M,N1] on
+    `device`, with the distributions above, drawn as float32 in that order from
+    one ``torch.Generator(device).manual_seed(seed)`` and rounded to bf16."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+
+    def normal(shape, var):
+        a = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        if var != 1.0:
+            a.mul_(float(np.float32(np.sqrt(var))))
+        return a.to(torch.bfloat16)
+
+    x = normal((M, d), 1.0)
+    z = normal((M, d), 1.0)
+    W0 = normal((d, d), 1.0 / d)
+    W1 = normal((d, N1), 1.0 / d)
+    gamma = (1.0 + torch.randn((d,), generator=gen, device=device, dtype=torch.float32)
+             * float(np.float32(np.sqrt(0.1)))).to(torch.bfloat16)
+    dy = normal((M, N1), 1e-2)
+    return {"x": x, "z": z, "W0": W0, "W1": W1, "gamma": gamma, "dy": dy}

@@ -347,6 +347,39 @@ def test_folded_rowreduce_is_bit_identical(B, mode, M, d, N1):
     check_r(f64(fold[1]), ref.r)
 
 
+# ----------------------------------------------------------------------------- element offsets past 2^31
+def test_large_batch_element_offsets_past_int32(B, mode):
+    """81920 tokens at the llama7b widths: y and dy hold 2.35e9 elements, more
+    than 2^31, so a 32-bit element offset would wrap from row 74898 on.  Rows on
+    both sides of that boundary, the first rows and the last rows are checked
+    against the oracle (inputs drawn on the device: the host would take minutes)."""
+    dev = torch.device("cuda:0")
+    M, d, N1, eps = 81920, 4096, 28672, 1e-5
+    g = synth.make_inputs_on_device(M, d, N1, seed=7, device=dev)
+    h, r, y = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps)
+    dh = B.coda_bwd_dgrad(g["dy"], g["W1"], h, r, g["gamma"])
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    assert M * N1 > 2 ** 31
+    edge = 2 ** 31 // N1
+    rows = sorted({0, 127, 128, edge - 1, edge, edge + 1, M - 129, M - 1})
+    idx = torch.as_tensor(rows, device=dev)
+
+    def pick(t):
+        return f64(t.index_select(0, idx))
+
+    W1 = f64(g["W1"])
+    ref = oracle.forward(pick(g["x"]), f64(g["W0"]), pick(g["z"]), f64(g["gamma"]), W1, eps)
+    hG, rG = pick(h), pick(r)
+    check("h", hG, ref.h, TOL_HY)
+    check_r(rG, ref.r)
+    check("y", pick(y), ref.y, TOL_HY)
+    bref = oracle.backward_dgrad(pick(g["dy"]), W1, hG, rG, f64(g["gamma"]))
+    check("dh", pick(dh), bref.dh, TOL_DH)
+    del g, h, r, y, dh
+    torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------------------- FP8 forward
 def run_fp8(B, M, d, N1, eps, seed=0, rows=None, s_hg_factor=1.0):
     """The oracle models the same quantisation of GEMM1's operand (E4M3, ties to

@@ -45,3 +45,22 @@ def test_sample_rows():
         assert r in rows
     assert np.all(np.diff(rows) > 0)
     assert np.array_equal(synth.sample_rows(100, 512), np.arange(100))
+
+
+def test_device_generator_shapes_determinism_and_distributions():
+    """make_inputs_on_device (used for workloads too large to draw on the
+    host) run on the CPU device: shapes, dtypes, seeding, distributions."""
+    a = synth.make_inputs_on_device(512, 256, 384, seed=5, device="cpu")
+    b = synth.make_inputs_on_device(512, 256, 384, seed=5, device="cpu")
+    c = synth.make_inputs_on_device(512, 256, 384, seed=6, device="cpu")
+    shapes = {"x": (512, 256), "z": (512, 256), "W0": (256, 256), "W1": (256, 384),
+              "gamma": (256,), "dy": (512, 384)}
+    for k, shp in shapes.items():
+        assert tuple(a[k].shape) == shp and a[k].dtype == torch.bfloat16, k
+        assert torch.equal(a[k], b[k]), k
+        assert not torch.equal(a[k], c[k]), k
+    std = {k: float(a[k].float().std()) for k in shapes}
+    assert abs(std["x"] - 1.0) < 0.02 and abs(std["z"] - 1.0) < 0.02
+    assert abs(std["W0"] - 256 ** -0.5) < 0.003 and abs(std["W1"] - 256 ** -0.5) < 0.003
+    assert abs(std["dy"] - 0.1) < 0.003
+    assert abs(float(a["gamma"].float().mean()) - 1.0) < 0.06 and abs(std["gamma"] - 0.1 ** 0.5) < 0.06
