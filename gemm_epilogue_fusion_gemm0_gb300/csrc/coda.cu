@@ -10,11 +10,9 @@
 //   launch 1  GEMM dy @ W1^T with EpiRmsNormBackward    -> grad_h (cooperative launch)
 
 #include <atomic>
-#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <mutex>
-#include <random>
 
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -188,8 +186,6 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_fold_rowreduce{0};  // 1: r computed in GEMM1's epilogue (no separate launch)
 std::atomic<int> g_mma_mode{1};  // 0: single-CTA 128x256 tiles, 1: CTA-pair 256x256 tiles (default)
-std::atomic<uint64_t> g_token_ctr{0};
-uint64_t g_token_salt = 0;
 cudaEvent_t* g_launch_events = nullptr;  // measurement hook (coda_set_launch_events)
 int g_launch_events_n = 0;
 
@@ -285,12 +281,6 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
         } else {
           ok = false;
         }
-      }
-      if (g_token_salt == 0) {
-        std::random_device rd;
-        g_token_salt = (static_cast<uint64_t>(rd()) << 32) ^ rd() ^
-                       static_cast<uint64_t>(
-                           std::chrono::steady_clock::now().time_since_epoch().count());
       }
       if (!ok) {
         cudaGetLastError();
@@ -498,10 +488,11 @@ size_t coda_fwd_unfused_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
 
 size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
-  // one flag per (128-row slab, column tile); CTA-pair tiles cover 2 * ceil(M/256) slabs
+  // one flag per (128-row slab, column tile); CTA-pair tiles cover 2 * ceil(M/256) slabs;
+  // then the launch epoch (8 bytes in a 256-byte slot)
   const int64_t slabs = 2 * cdiv(M, kPairBM), nt = cdiv(d, kBN);
   return align256(static_cast<size_t>(2 * nt) * M * 4) +
-         align256(static_cast<size_t>(slabs) * nt * 8);
+         align256(static_cast<size_t>(slabs) * nt * 8) + 256;
 }
 
 coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
@@ -569,9 +560,8 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   p.qpart = reinterpret_cast<float*>(workspace);
   p.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
                                         align256(static_cast<size_t>(2 * nt) * M * 4));
-  uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
-  if (tok == 0) tok = 1;
-  p.token = tok;
+  p.epoch = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
+                                        coda_bwd_dgrad_workspace_bytes(M, d, N1) - 256);
   cudaError_t e =
       pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
@@ -737,8 +727,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
   p.qpart = qpart;
   p.flags = flags;
-  uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
-  p.token = tok == 0 ? 1 : tok;
+  p.epoch = reinterpret_cast<uint64_t*>(ws + coda_bwd_dgrad_workspace_bytes(M, d, N1) - 256);
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
@@ -987,11 +976,12 @@ coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t stream) {
 constexpr size_t kNoAllocPartials = 2 * CODA_NOALLOC_MAX_PARTIALS;  // fp32, two per (row, column tile)
 constexpr size_t kNoAllocFlags = CODA_NOALLOC_MAX_TILES;        // u64 per output tile
 constexpr size_t kNoAllocFlagOffset = kNoAllocPartials * sizeof(float);
-constexpr size_t kNoAllocBytes = kNoAllocFlagOffset + kNoAllocFlags * sizeof(uint64_t);
+constexpr size_t kNoAllocEpochOffset = kNoAllocFlagOffset + kNoAllocFlags * sizeof(uint64_t);
+constexpr size_t kNoAllocBytes = kNoAllocEpochOffset + 256;
 
-// 4 MiB of partials + 128 KiB of flags.  The flags need no clearing: each
-// call publishes a fresh 64-bit token, so values left by an earlier call never
-// match (and the array starts zeroed, a value no call ever uses).
+// 4 MiB of partials + 128 KiB of flags + the launch epoch.  The flags need no
+// clearing: each launch publishes epoch + 1 and then advances the epoch, so
+// values left by an earlier call never match (the array starts zeroed).
 static __device__ __align__(256) unsigned char g_noalloc_dgrad_scratch[kNoAllocBytes];
 
 namespace {
@@ -1062,9 +1052,7 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
   p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
   p.qpart = reinterpret_cast<float*>(scratch);
   p.flags = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(scratch) + kNoAllocFlagOffset);
-  uint64_t tok = g_token_salt + (g_token_ctr.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
-  if (tok == 0) tok = 1;
-  p.token = tok;
+  p.epoch = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(scratch) + kNoAllocEpochOffset);
   cudaError_t e = launch(kDgrad, grid, kThreads, kDgradSmem, stream, true, mA, mB,
                          static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                          g_timeout_ns.load());

@@ -20,6 +20,7 @@
 // (per-tile sums of squares / of grad_h2 * gamma * h).
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_fp8.h>
 
 #include "gemm.cuh"
@@ -36,6 +37,9 @@ struct Chunk8 {
 struct EpiDefaultCols {
   static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N + kBN - 1) / kBN; }
   static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
+  // run by every thread of the grid after the block's last tile (nothing by default)
+  template <class P>
+  static __device__ __forceinline__ void at_exit(const P&) {}
 };
 
 // r[m] = rsqrt(sum of the row's h^2 partials / d + eps), summed in the same
@@ -360,7 +364,7 @@ struct EpiRowScale : EpiDefaultCols {
 // Data-gradient epilogue (CODA blog, section "反向传播的 GEMM-Epilogue 结构"):
 // acc = grad_h2 = grad_y @ W1^T for this tile.
 //   pass 1: qpart[2 nb + half][m] = sum over the half tile of acc * gamma * h;
-//           publish it with a release flag carrying this call's token;
+//           publish it with a release flag carrying this launch's token;
 //   then:   wait until every column tile of this row block has published,
 //           q[m] = sum of the row's 2 nt partials (fixed order), coef = r^3 q / d;
 //   pass 2: grad_h = r * gamma * acc - coef * h   -> dh_out bf16.
@@ -368,6 +372,11 @@ struct EpiRowScale : EpiDefaultCols {
 // needs every block of the launch resident (cooperative launch) and tiles in
 // row-major order with at most gridDim.x column tiles per row; then every wait
 // depends only on tiles with smaller index and cannot deadlock.
+// The token is epoch + 1, epoch being a counter in the caller's workspace that
+// the launch reads and, once every block is done (a grid-wide barrier: the
+// launch is cooperative), advances by one.  Flags left by an earlier launch hold
+// an older token, so the workspace never needs clearing, and a launch replayed
+// from a CUDA graph draws a fresh token each time.
 // ---------------------------------------------------------------------------
 // kExtras: the full backward's additions (dh_res, h2, dgamma partials) are
 // compiled in; the plain data gradient leaves them out and keeps fewer registers.
@@ -382,12 +391,19 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
     __nv_bfloat16* dh_out;
     float* qpart;     // [2 * nt][M]
     uint64_t* flags;  // [mt][nt]
-    uint64_t token;
+    uint64_t* epoch;  // launch counter (any initial value); this launch's token is *epoch + 1
     // Extras of the full backward (read only with kExtras):
     const __nv_bfloat16* dh_res;  // [M, d] gradient reaching h through the residual, or null
     __nv_bfloat16* h2_out;        // [M, d] normalised activation r * h * gamma (dW1's operand)
     float* gpart;                 // [4 * slabs][d] per-warp column partials of dgamma
   };
+
+  // Every block has finished its tiles once the grid barrier is passed, so no
+  // flag of this launch is read any more: advance the epoch.
+  static __device__ __forceinline__ void at_exit(const Params& p) {
+    cooperative_groups::this_grid().sync();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.epoch = *p.epoch + 1;
+  }
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
                                                const TileCtx& c) {
@@ -443,10 +459,11 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
     named_bar_sync(1, kEpiThreads);
     uint64_t* row_flags = p.flags + static_cast<size_t>(c.mb) * c.nt;
     if (threadIdx.x == kEpiFirstThread) {
+      const uint64_t token = *reinterpret_cast<volatile uint64_t*>(p.epoch) + 1;
       __threadfence();
-      st_release_gpu_u64(row_flags + c.nb, p.token);
+      st_release_gpu_u64(row_flags + c.nb, token);
       for (int j = 0; j < c.nt; ++j)
-        if (!flag_wait(row_flags + j, p.token, wc, kSiteRowFlags)) break;
+        if (!flag_wait(row_flags + j, token, wc, kSiteRowFlags)) break;
       __threadfence();
     }
     named_bar_sync(1, kEpiThreads);
@@ -552,6 +569,8 @@ __device__ __forceinline__ float silu_f(float t) { return t / (1.0f + __expf(-t)
 
 struct EpiRowScaleSwiGLU {
   static constexpr uint32_t kStageBytesPerWarp = 2 * Stage64::kBytes;  // a, then up; gate
+  template <class P>
+  static __device__ __forceinline__ void at_exit(const P&) {}
 
   struct Params {
     const float* r;         // [M]

@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  Epi::at_exit(ep);
 }
 
 }  // namespace coda

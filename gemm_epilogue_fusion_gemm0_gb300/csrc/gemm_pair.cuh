@@ -276,6 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc_pair(tmem_base, kTmemCols);
   }
+  Epi::at_exit(ep);
 }
 
 }  // namespace coda

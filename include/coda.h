@@ -161,9 +161,11 @@ CODA_API coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t*
  *   gamma   [d]     bf16 in
  *   dh_out  [M, d]  bf16 out
  *   workspace: at least coda_bwd_dgrad_workspace_bytes(M, d, N1) bytes.  The
- *   completion flags carry a per-call 64-bit token, so the workspace needs no
- *   clearing between calls; two calls that share a workspace must not run
- *   concurrently.
+ *   completion flags carry a token taken from a launch counter kept in the
+ *   workspace, which every launch advances once all its blocks are done: the
+ *   workspace needs no clearing (any initial contents work), and a call
+ *   captured in a CUDA graph draws a fresh token at every replay.  Two calls
+ *   that share a workspace must not run concurrently.
  * The kernel is a cooperative launch (all its blocks are resident at once).
  */
 CODA_API coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const coda_bf16* h,
@@ -327,8 +329,9 @@ CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t 
  *  - The first call on each device looks up the device address of the array
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
- *  - Every call uses the same array.  Nothing in it needs clearing (each call
- *    tags its flags with a fresh 64-bit token), but calls whose kernels
+ *  - Every call uses the same array.  Nothing in it needs clearing (each
+ *    launch tags its flags with a fresh token from a launch counter kept in
+ *    the array), but calls whose kernels
  *    overlap on the GPU, on different streams or from different host threads,
  *    race on it and give wrong results: order them (one stream, or events).
  *  - Otherwise the arguments, checks and errors are those of coda_bwd_dgrad.

@@ -51,9 +51,10 @@ def test_workspace_sizes(lib):
     M, d, N1 = 8192, 4096, 28672
     assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 32 * M * 4
     assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == M * d * 2
-    # qpart [2 * 16, M] fp32 + flags [2 * ceil(M/256) * 16] u64 (one per 128-row slab and column tile)
-    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 32 * M * 4 + 64 * 16 * 8
-    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 2560 + 256  # 4 slabs x 1 tile
+    # qpart [2 * 16, M] fp32 + flags [2 * ceil(M/256) * 16] u64 (one per 128-row slab and column
+    # tile) + a 256-byte slot for the launch counter
+    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 32 * M * 4 + 64 * 16 * 8 + 256
+    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 2560 + 256 + 256  # 4 slabs x 1 tile
     assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
     assert lib.coda_fwd_workspace_bytes(300, 328, 776) == 196864 + 4864  # ragged: rounded up
     assert lib.coda_fwd_workspace_bytes(10, 12, 16) == 0  # d % 8 != 0: unsupported

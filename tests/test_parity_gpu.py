@@ -347,6 +347,71 @@ def test_folded_rowreduce_is_bit_identical(B, mode, M, d, N1):
     check_r(f64(fold[1]), ref.r)
 
 
+# ----------------------------------------------------------------------------- CUDA graphs
+def test_step_replays_from_a_cuda_graph(B, mode):
+    """coda_fwd + coda_bwd_dgrad captured once into a CUDA graph and replayed,
+    twice per input set, on three input sets copied into the captured buffers:
+    every replay equals the eager calls on the same inputs bit for bit.  The
+    dgrad's launch counter (the last 8 bytes of its workspace) advances by one
+    per replay and every completion flag holds the last replay's token, so
+    flags left by one replay never satisfy the next one's waits."""
+    dev = torch.device("cuda:0")
+    M, d, N1, eps = 640, 512, 1280, 1e-5
+    sets = []
+    for seed in (21, 22, 23):
+        t = synth.make_forward_inputs(M, d, N1, seed=seed)
+        dy = synth.make_grad_output(t["_rng"], M, N1)
+        sets.append({**{k: v.to(dev) for k, v in t.items() if k != "_rng"}, "dy": dy.to(dev)})
+    buf = {k: torch.empty_like(v) for k, v in sets[0].items()}
+    bf = torch.bfloat16
+    h, dh = (torch.empty((M, d), dtype=bf, device=dev) for _ in range(2))
+    r = torch.empty((M,), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N1), dtype=bf, device=dev)
+    ws_f = B.workspace(B.coda_fwd_workspace_bytes(M, d, N1), dev)
+    nb = B.coda_bwd_dgrad_workspace_bytes(M, d, N1)
+    ws_b = B.workspace(nb, dev)
+
+    def step():
+        st = torch.cuda.current_stream()
+        B.coda_fwd(buf["x"], buf["W0"], buf["z"], buf["gamma"], buf["W1"], eps, h=h, r=r, y=y,
+                   ws=ws_f, stream=st)
+        B.coda_bwd_dgrad(buf["dy"], buf["W1"], h, r, buf["gamma"], dh=dh, ws=ws_b, stream=st)
+
+    def epoch():
+        return int(ws_b[nb - 256:nb - 248].view(torch.int64).item())
+
+    for k in buf:
+        buf[k].copy_(sets[0][k])
+    step()  # device set-up happens on a first call, before any capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    nt = (d + 255) // 256
+    flags = ws_b[((2 * nt * M * 4 + 255) // 256) * 256:].view(torch.int64)
+    for data in sets:
+        for k in buf:
+            buf[k].copy_(data[k])
+        step()
+        torch.cuda.synchronize()
+        ref = [t.clone() for t in (h, r, y, dh)]
+        for t in (h, y, dh):
+            t.fill_(float("nan"))
+        r.fill_(-1.0)
+        e0 = epoch()
+        graph.replay()
+        graph.replay()
+        torch.cuda.synchronize()
+        st, detail = B.coda_get_device_status()
+        assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+        for got, want in zip((h, r, y, dh), ref):
+            assert torch.equal(got, want)
+        e2 = epoch()
+        assert (e2 - e0) % 2 ** 64 == 2  # the counter starts at whatever the workspace held
+        used = flags[: ((M + 127) // 128) * nt]
+        assert torch.all(used == e2), "every flag holds the last replay's token"
+
+
 # ----------------------------------------------------------------------------- element offsets past 2^31
 def test_large_batch_element_offsets_past_int32(B, mode):
     """81920 tokens at the llama7b widths: y and dy hold 2.35e9 elements, more
