@@ -253,7 +253,7 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 EXTRAS = ("fwd_swiglu", "other_llama_shapes", "fwd_fp8", "fwd_folded_rowreduce", "fwd_unfused",
-          "fwd_l2_flushed", "torch_chain", "bwd_swiglu_dgrad", "bwd_full")
+          "fwd_l2_flushed", "torch_chain", "tiny_graph", "bwd_swiglu_dgrad", "bwd_full")
 
 
 def time_calls(B, stream, barrier, call, n, launches):
@@ -450,6 +450,53 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
             "torch": torch.__version__,
             "note": "context only: torch.addmm + torch.nn.functional.rms_norm + torch.mm (cuBLAS), "
                     "same shapes and dtypes, medians of alternating rounds with coda_fwd"}
+
+    if "tiny_graph" in want:
+        # the launch-bound tiny workload (128 x 256 x 512): one step (forward + data gradient,
+        # 4 launches) issued eagerly against the same step captured once in a CUDA graph
+        tw = synth.WORKLOADS["tiny"]
+        tt = synth.make_forward_inputs(tw.M, tw.d, tw.N1, seed=rank)
+        tg = {k: v.to(dev) for k, v in tt.items() if k != "_rng"}
+        tdy = synth.make_grad_output(tt["_rng"], tw.M, tw.N1).to(dev)
+        bf = torch.bfloat16
+        th, tdh = (torch.empty((tw.M, tw.d), dtype=bf, device=dev) for _ in range(2))
+        tr = torch.empty((tw.M,), dtype=torch.float32, device=dev)
+        ty = torch.empty((tw.M, tw.N1), dtype=bf, device=dev)
+        twf = B.workspace(B.coda_fwd_workspace_bytes(tw.M, tw.d, tw.N1), dev)
+        twb = B.workspace(B.coda_bwd_dgrad_workspace_bytes(tw.M, tw.d, tw.N1), dev)
+
+        def tiny_step():
+            st = torch.cuda.current_stream()
+            B.coda_fwd(tg["x"], tg["W0"], tg["z"], tg["gamma"], tg["W1"], tw.eps, h=th, r=tr,
+                       y=ty, ws=twf, stream=st)
+            B.coda_bwd_dgrad(tdy, tg["W1"], th, tr, tg["gamma"], dh=tdh, ws=twb, stream=st)
+        warm(tiny_step)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            tiny_step()
+        n = 200
+
+        def per_step(call):
+            t = []
+            for _ in range(3):
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                barrier()
+                s0.record(stream)
+                for _ in range(n):
+                    call()
+                s1.record(stream)
+                barrier()
+                t.append(s0.elapsed_time(s1) / n)
+            return statistics.median(t)
+        e_ms, g_ms = per_step(tiny_step), per_step(graph.replay)
+        flops = tw.fwd_flops + tw.bwd_flops
+        extras["tiny_graph"] = {
+            "eager_us_per_step": e_ms * 1e3, "graph_us_per_step": g_ms * 1e3,
+            "eager_tflops": tf(flops, e_ms), "graph_tflops": tf(flops, g_ms), "steps": n,
+            "note": "tiny workload (one tile), launch-bound: coda_fwd + coda_bwd_dgrad eager "
+                    "against the same step replayed from a CUDA graph"}
+        del graph
 
     if "fwd_unfused" in want:
         # the unfused sequence of this library's own kernels: GEMM0 storing h,
