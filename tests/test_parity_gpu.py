@@ -412,6 +412,87 @@ def test_step_replays_from_a_cuda_graph(B, mode):
         assert torch.all(used == e2), "every flag holds the last replay's token"
 
 
+@pytest.mark.parametrize("entry", ["fwd_swiglu", "bwd_swiglu_dgrad", "bwd", "fwd_fp8"])
+def test_entry_points_replay_from_a_cuda_graph(B, entry):
+    """Each remaining workspace entry point captured once into a CUDA graph:
+    two replays on the captured buffers equal an eager call bit for bit."""
+    dev = torch.device("cuda:0")
+    M, d, N1, eps = 384, 512, 1024, 1e-5
+    bf = torch.bfloat16
+    t = synth.make_forward_inputs(M, d, N1, seed=31)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    outs = {}
+    if entry == "fwd_swiglu":
+        ws = B.workspace(B.coda_fwd_workspace_bytes(M, d, N1), dev)
+        outs = {"h": torch.empty((M, d), dtype=bf, device=dev),
+                "r": torch.empty((M,), dtype=torch.float32, device=dev),
+                "a": torch.empty((M, N1 // 2), dtype=bf, device=dev),
+                "y": torch.empty((M, N1), dtype=bf, device=dev)}
+
+        def call():
+            B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=outs["h"],
+                              r=outs["r"], a=outs["a"], y=outs["y"], ws=ws,
+                              stream=torch.cuda.current_stream())
+    elif entry == "bwd_swiglu_dgrad":
+        h, r, _ = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps)
+        rng = t["_rng"]
+        dy = synth.make_grad_output(rng, M, N1).to(dev)
+        extra = synth.make_down_proj_backward(rng, M, N1, d)
+        W2, dout = extra["W2"].to(dev), extra["dout"].to(dev)
+        ws = B.workspace(B.coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, d), dev)
+        outs = {"dy": torch.empty((M, N1), dtype=bf, device=dev),
+                "s": torch.empty((M,), dtype=torch.float32, device=dev),
+                "dh": torch.empty((M, d), dtype=bf, device=dev)}
+        y_pre = dy  # any saved pre-activation of the right shape serves for replay equality
+
+        def call():
+            B.coda_bwd_swiglu_dgrad(dout, W2, y_pre, g["W1"], h, r, g["gamma"], dy=outs["dy"],
+                                    s=outs["s"], dh=outs["dh"], ws=ws,
+                                    stream=torch.cuda.current_stream())
+    elif entry == "bwd":
+        h, r, _ = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps)
+        rng = t["_rng"]
+        dy = synth.make_grad_output(rng, M, N1).to(dev)
+        dh_res = synth.make_residual_grad(rng, M, d).to(dev)
+        ws = B.workspace(B.coda_bwd_workspace_bytes(M, d, N1), dev)
+        outs = {"dh": torch.empty((M, d), dtype=bf, device=dev),
+                "dx": torch.empty((M, d), dtype=bf, device=dev),
+                "dgamma": torch.empty((d,), dtype=torch.float32, device=dev),
+                "dW0": torch.empty((d, d), dtype=torch.float32, device=dev),
+                "dW1": torch.empty((d, N1), dtype=torch.float32, device=dev)}
+
+        def call():
+            B.coda_bwd(dy, g["x"], g["W0"], g["W1"], h, r, g["gamma"], dh_res, out=outs, ws=ws,
+                       stream=torch.cuda.current_stream())
+    else:
+        f8 = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+              for k, v in synth.make_fp8_forward_inputs(M, d, N1, seed=31).items()}
+        ws = B.workspace(B.coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
+        outs = {"h": torch.empty((M, d), dtype=bf, device=dev),
+                "r": torch.empty((M,), dtype=torch.float32, device=dev),
+                "y": torch.empty((M, N1), dtype=bf, device=dev)}
+
+        def call():
+            B.coda_fwd_fp8(f8["x_q"], f8["sx"], f8["W0_q"], f8["sW0"], f8["z"], f8["gamma"],
+                           f8["W1_q"], f8["sW1"], f8["s_hg"], eps, h=outs["h"], r=outs["r"],
+                           y=outs["y"], ws=ws, stream=torch.cuda.current_stream())
+    call()
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in outs.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for v in outs.values():
+        v.fill_(-3.0)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    for k, v in outs.items():
+        assert torch.equal(v, ref[k]), k
+
+
 # ----------------------------------------------------------------------------- element offsets past 2^31
 def test_large_batch_element_offsets_past_int32(B, mode):
     """81920 tokens at the llama7b widths: y and dy hold 2.35e9 elements, more
