@@ -278,6 +278,26 @@ def time_calls(B, stream, barrier, call, n, launches):
     return s0.elapsed_time(s1) / n, per
 
 
+def alternating(stream, barrier, calls, rounds=6, n=20):
+    """Median ms per call of each callable in `calls` (name -> callable), timed
+    in rounds of n calls whose order rotates every round, so that every form
+    sees the same power and thermal state."""
+    names = list(calls)
+    out = {k: [] for k in names}
+    for i in range(rounds):
+        order = names[i % len(names):] + names[:i % len(names)]
+        for k in order:
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            s0.record(stream)
+            for _ in range(n):
+                calls[k]()
+            s1.record(stream)
+            barrier()
+            out[k].append(s0.elapsed_time(s1) / n)
+    return {k: statistics.median(v) for k, v in out.items()}
+
+
 def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
     """The widened paths and the comparison sequence, each timed on its own
     (none of it is part of `value`)."""
@@ -373,15 +393,21 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
         def fwd():
             B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
                        stream=stream)
-        B.coda_set_fold_rowreduce(1)
-        try:
-            warm(fwd)
-            ms, _ = time_calls(B, stream, barrier, fwd, KS, 2)
-        finally:
-            B.coda_set_fold_rowreduce(0)
+        def fwd_fold():
+            B.coda_set_fold_rowreduce(1)
+            try:
+                fwd()
+            finally:
+                B.coda_set_fold_rowreduce(0)
+        warm(fwd_fold)
+        ms, _ = time_calls(B, stream, barrier, fwd_fold, KS, 2)
+        warm(fwd)
+        t = alternating(stream, barrier, {"fold": fwd_fold, "fwd": fwd})
         extras["fwd_folded_rowreduce"] = {
             "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 2 * KS,
-            "note": "coda_fwd with r formed in GEMM1's epilogue (F4)"}
+            "alternating_ms": {"folded": t["fold"], "coda_fwd": t["fwd"]},
+            "note": "coda_fwd with r formed in GEMM1's epilogue (F4); alternating_ms: medians of "
+                    "alternating rounds against the default three-launch forward"}
 
     if "fwd_l2_flushed" in want:
         # the forward alone with L2 flushed before every call (a 256 MB write,
@@ -424,26 +450,11 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
             B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
                        stream=stream)
 
-        def timed(call, n):
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            barrier()
-            s0.record(stream)
-            for _ in range(n):
-                call()
-            s1.record(stream)
-            barrier()
-            return s0.elapsed_time(s1) / n
-
         warm(chain)
         warm(fwd)
         rounds, n = 6, 20
-        t_chain, t_fwd = [], []
-        for i in range(rounds):
-            first, second = (chain, fwd) if i % 2 == 0 else (fwd, chain)
-            a, b = timed(first, n), timed(second, n)
-            t_chain.append(a if first is chain else b)
-            t_fwd.append(b if first is chain else a)
-        mc, mf = statistics.median(t_chain), statistics.median(t_fwd)
+        t = alternating(stream, barrier, {"chain": chain, "fwd": fwd}, rounds, n)
+        mc, mf = t["chain"], t["fwd"]
         extras["torch_chain"] = {
             "ms": mc, "tflops": tf(w.fwd_flops, mc), "coda_fwd_ms": mf,
             "coda_fwd_tflops": tf(w.fwd_flops, mf), "rounds": rounds, "calls_per_round": n,
@@ -507,13 +518,21 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
         def fwd_u():
             B.coda_fwd_unfused(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y,
                                ws=ws_u, stream=stream)
+        def fwd_f():
+            B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, h=h, r=r, y=y, ws=ws_f,
+                       stream=stream)
         warm(fwd_u)
         ms, k = time_calls(B, stream, barrier, fwd_u, KS, 3)
+        warm(fwd_f)
+        t = alternating(stream, barrier, {"unfused": fwd_u, "fused": fwd_f})
         extras["fwd_unfused"] = {
             "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 3 * KS,
             "kernels_ms": {"gemm0_plain": k[0], "rmsnorm_rows": k[1], "gemm1_plain": k[2]},
+            "alternating_ms": {"unfused": t["unfused"], "coda_fwd": t["fused"]},
             "note": "coda_fwd_unfused: GEMM0 -> RMSNorm kernel (normalised tensor through HBM) "
-                    "-> GEMM1; the fused forward's comparison sequence"}
+                    "-> GEMM1; the fused forward's comparison sequence. alternating_ms: medians of "
+                    "alternating rounds against coda_fwd, the comparison to read (absolute times "
+                    "of the separate extras depend on what ran before them)"}
         del ws_u
 
     if "bwd_swiglu_dgrad" in want:

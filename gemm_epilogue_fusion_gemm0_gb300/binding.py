@@ -64,6 +64,7 @@ EXPORTS = {
                               _sz, _vp]),
     "coda_get_mma_mode": (ctypes.c_int, []),
     "coda_set_fold_rowreduce": (_st, [ctypes.c_int]),
+    "coda_set_split_tail": (_st, [ctypes.c_int]),
     "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
                            _vp, _vp, _vp, _sz, _vp]),
@@ -317,6 +318,11 @@ def coda_set_mma_mode(mode: int) -> None:
 def coda_set_fold_rowreduce(enable: int) -> None:
     """1: r is formed in GEMM1's epilogue (2 launches); 0: separate reduction (default)."""
     _check(_lib.coda_set_fold_rowreduce(int(enable)), "coda_set_fold_rowreduce")
+
+
+def coda_set_split_tail(enable: int) -> None:
+    """1: the forward's CTA-pair GEMMs split their last tiles along K (default); 0: whole tiles."""
+    _check(_lib.coda_set_split_tail(int(enable)), "coda_set_split_tail")
 
 
 def coda_get_mma_mode() -> int:

@@ -185,6 +185,7 @@ DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_fold_rowreduce{0};  // 1: r computed in GEMM1's epilogue (no separate launch)
+std::atomic<int> g_split_tail{1};      // 1: stream-K tail in the forward's CTA-pair GEMMs
 std::atomic<int> g_mma_mode{1};  // 0: single-CTA 128x256 tiles, 1: CTA-pair 256x256 tiles (default)
 cudaEvent_t* g_launch_events = nullptr;  // measurement hook (coda_set_launch_events)
 int g_launch_events_n = 0;
@@ -347,15 +348,79 @@ coda_status_t check_common(int64_t M, int64_t d, int64_t N1) {
   return CODA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Split-tail (stream-K) region of a workspace: partial accumulators, their
+// flags and the launch counter that the flags' tokens come from.
+// ---------------------------------------------------------------------------
+constexpr int kSkMaxPairs = 80;  // no split tail for launches of more CTA pairs
+
+// Partial slots for launches of up to `tiles` CTA-pair tiles: a split tail
+// covers U + R <= 2 U - 1 tiles.
+int64_t sk_slots(int64_t tiles) { return std::min<int64_t>(tiles, 2 * kSkMaxPairs); }
+
+size_t sk_region_bytes(int64_t tiles) {
+  const int64_t slots = sk_slots(tiles);
+  return align256(static_cast<size_t>(slots) * 2 * kSkSlotFloats * 4) +
+         align256(static_cast<size_t>(slots) * 2 * 8) + 256;
+}
+
+struct SkRegion {
+  float* part = nullptr;
+  uint64_t* flags = nullptr;
+  uint64_t* epoch = nullptr;
+  int64_t slots = 0;
+};
+
+SkRegion sk_region(void* base, int64_t tiles) {
+  SkRegion r;
+  r.slots = sk_slots(tiles);
+  char* p = static_cast<char*>(base);
+  r.part = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(r.slots) * 2 * kSkSlotFloats * 4);
+  r.flags = reinterpret_cast<uint64_t*>(p);
+  p += align256(static_cast<size_t>(r.slots) * 2 * 8);
+  r.epoch = reinterpret_cast<uint64_t*>(p);
+  return r;
+}
+
+// Whole tiles for the first W - 1 waves, the last U + R tiles split along K
+// (gemm_pair.cuh).  The split costs a cooperative launch with a grid barrier
+// (2-4 us) and, per pair, a partial written or added and sometimes a wait for
+// a TMEM buffer; it gains the idle share of the last wave, (U - R) / U of a
+// tile.  Measured on GB300 it pays for the llama7b and llama70b GEMM1 (R/U =
+// 0.16, 64 and 128 k-blocks per tile) and loses when the last wave is mostly
+// full (GEMM0 there, R/U = 0.74) or tiles are short (llama1b, 32 k-blocks).  So:
+// split only when R <= U / 2 and a tile has at least 64 k-blocks, with at
+// least two waves and enough slots.
+SkParams plan_split_tail(const SkRegion& reg, int64_t num_tiles, int npairs, int64_t nk) {
+  SkParams sk = kNoSplitTail;
+  if (g_split_tail.load() == 0 || reg.part == nullptr || npairs < 1 || npairs > kSkMaxPairs)
+    return sk;
+  const int64_t W = num_tiles / npairs, R = num_tiles % npairs;
+  if (W < 2 || R == 0 || 2 * R > npairs || nk < 64 || npairs + R > reg.slots) return sk;
+  sk.dp_tiles = static_cast<int>(num_tiles - (npairs + R));
+  sk.part = reg.part;
+  sk.flags = reg.flags;
+  sk.epoch = reg.epoch;
+  return sk;
+}
+
 struct FwdWorkspace {
   __nv_bfloat16* act;  // hg (fused) or hn (unfused), [M, d]
   float* part;         // [nt0][M] (fused only)
+  SkRegion sk;         // split tails of GEMM0 and GEMM1 (fused only)
 };
 
-size_t fwd_ws_bytes(int64_t M, int64_t d, bool fused) {
+// CTA-pair tiles of the forward's larger GEMM (sizes the split-tail region)
+int64_t fwd_pair_tiles(int64_t M, int64_t d, int64_t N1) {
+  return cdiv(M, kPairBM) * std::max(cdiv(d, kBN), cdiv(N1, kBN));
+}
+
+size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t N1, bool fused) {
   const size_t act = align256(static_cast<size_t>(M) * d * 2);
   const size_t part = fused ? align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4) : 0;
-  return act + part;
+  const size_t sk = fused ? sk_region_bytes(fwd_pair_tiles(M, d, N1)) : 0;
+  return act + part + sk;
 }
 
 enum class FwdKind { kFused, kUnfused, kFusedSwiGLU };
@@ -378,7 +443,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   for (const void* p : ptrs)
     if (!aligned16(p)) return CODA_ERR_MISALIGNED;
   if (swiglu && !aligned16(y_out)) return CODA_ERR_MISALIGNED;  // optional, may be null
-  if (workspace == nullptr || workspace_bytes < fwd_ws_bytes(M, d, fused))
+  if (workspace == nullptr || workspace_bytes < fwd_ws_bytes(M, d, N1, fused))
     return CODA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(workspace)) return CODA_ERR_MISALIGNED;
   int sms = 0, max_pairs = 0;
@@ -391,6 +456,10 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   ws.part = fused ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                              align256(static_cast<size_t>(M) * d * 2))
                   : nullptr;
+  if (fused)
+    ws.sk = sk_region(static_cast<char*>(workspace) + align256(static_cast<size_t>(M) * d * 2) +
+                          align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4),
+                      fwd_pair_tiles(M, d, N1));
 
   CUtensorMap mA0, mB0, mA1, mB1;
   bool ok = tmap_2d(&mA0, x, d, M, kBK, kBM);           // x  [M, d]  K-major
@@ -413,9 +482,13 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   p0.hg_out = fused ? ws.act : nullptr;
   p0.part = ws.part;
   const int mtp = static_cast<int>(cdiv(M, kPairBM));
+  const int64_t nkb = cdiv(d, kBK);  // k-blocks of both GEMMs (K = d)
+  const int np0 = std::min(max_pairs, mtp * nt0), np1 = std::min(max_pairs, mtp * nt1);
+  const SkParams sk0 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt0, np0, nkb);
+  const SkParams sk1 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt1, np1, nkb);
   cudaError_t e =
-      pair ? launch(kPairGemm0, 2 * std::min(max_pairs, mtp * nt0), kThreads, kPairGemm0Smem,
-                    stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, tmo)
+      pair ? launch(kPairGemm0, 2 * np0, kThreads, kPairGemm0Smem, stream, sk0.epoch != nullptr,
+                    mA0, mB0, Mi, di, di, kPairGroupM, p0, sk0, tmo)
            : launch(kGemm0, std::min(sms, mt * nt0), kThreads, kGemm0Smem, stream, false, mA0,
                     mB0, Mi, di, di, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
@@ -449,9 +522,8 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     ps.fold = fold;
     ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
-    e = pair ? launch(kPairGemm1Swiglu, 2 * std::min(max_pairs, mtp * nt1), kThreads,
-                      kPairGemm1SwigluSmem, stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM,
-                      ps, tmo)
+    e = pair ? launch(kPairGemm1Swiglu, 2 * np1, kThreads, kPairGemm1SwigluSmem, stream,
+                      sk1.epoch != nullptr, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, sk1, tmo)
              : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kGemm1SwigluSmem,
                       stream, false, mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
   } else {
@@ -459,8 +531,8 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     p1.r = fused ? r_out : nullptr;
     p1.fold = fold;
     p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
-    e = pair ? launch(kPairGemm1, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairGemm1Smem,
-                      stream, false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo)
+    e = pair ? launch(kPairGemm1, 2 * np1, kThreads, kPairGemm1Smem, stream, sk1.epoch != nullptr,
+                      mA1, mB1, Mi, N1i, di, kPairGroupM, p1, sk1, tmo)
              : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kGemm1Smem, stream, false, mA1,
                       mB1, Mi, N1i, di, kGroupM, p1, tmo);
   }
@@ -478,12 +550,12 @@ extern "C" {
 
 size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
-  return fwd_ws_bytes(M, d, true);
+  return fwd_ws_bytes(M, d, N1, true);
 }
 
 size_t coda_fwd_unfused_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
-  return fwd_ws_bytes(M, d, false);
+  return fwd_ws_bytes(M, d, N1, false);
 }
 
 size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
@@ -564,7 +636,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
                                         coda_bwd_dgrad_workspace_bytes(M, d, N1) - 256);
   cudaError_t e =
       pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true, mA, mB,
-                    static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
+                    static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p, kNoSplitTail,
                     g_timeout_ns.load())
            : launch(kDgrad, units, kThreads, kDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
@@ -632,7 +704,7 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   p0.acc_scale = sx * sW0;
   p0.inv_s_hg = 1.0f / s_hg;
   cudaError_t e = launch(kPairGemm0F8, 2 * std::min(max_pairs, mtp * nt0), kThreads,
-                         kPairGemm0F8Smem, stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0,
+                         kPairGemm0F8Smem, stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, kNoSplitTail,
                          tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -651,7 +723,7 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
   p1.scale = s_hg * sW1;
   e = launch(kPairGemm1F8, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairGemm1F8Smem, stream,
-             false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, tmo);
+             false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, kNoSplitTail, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -732,7 +804,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.h2_out = h2;
   p.gpart = gpart;
   cudaError_t e = pair ? launch(kPairDgradFull, 2 * units, kThreads, kPairDgradFullSmem, stream,
-                                true, mDy, mW1, Mi, di, N1i, 1, p, tmo)
+                                true, mDy, mW1, Mi, di, N1i, 1, p, kNoSplitTail, tmo)
                        : launch(kDgradFull, units, kThreads, kDgradFullSmem, stream, true, mDy, mW1,
                                 Mi, di, N1i, 1, p, tmo);
   if (e != cudaSuccess) {
@@ -754,7 +826,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const int mtw = static_cast<int>(cdiv(d, pair ? kPairBM : kBM));
   const int ntw1 = static_cast<int>(cdiv(N1, kBN));
   e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, kPairWgradSmem,
-                    stream, false, mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, tmo)
+                    stream, false, mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, kNoSplitTail, tmo)
            : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kWgradSmem, stream, false, mH2,
                     mDyMN, di, N1i, Mi, kGroupM, pw1, tmo);
   if (e != cudaSuccess) {
@@ -768,7 +840,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   px.y_out = reinterpret_cast<__nv_bfloat16*>(dx_out);
   const int mtx = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
   e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, kPairXgradSmem,
-                    stream, false, mDh, mW0, Mi, di, di, kPairGroupM, px, tmo)
+                    stream, false, mDh, mW0, Mi, di, di, kPairGroupM, px, kNoSplitTail, tmo)
            : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kXgradSmem, stream, false, mDh,
                     mW0, Mi, di, di, kGroupM, px, tmo);
   if (e != cudaSuccess) {
@@ -780,7 +852,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   EpiStoreF32::Params pw0 = {};
   pw0.out = dW0_out;
   e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, kPairWgradSmem,
-                    stream, false, mX, mDhMN, di, di, Mi, kPairGroupM, pw0, tmo)
+                    stream, false, mX, mDhMN, di, di, Mi, kPairGroupM, pw0, kNoSplitTail, tmo)
            : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kWgradSmem, stream, false, mX,
                     mDhMN, di, di, Mi, kGroupM, pw0, tmo);
   if (e != cudaSuccess) {
@@ -847,7 +919,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   cudaError_t e =
       pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads,
                     kPairSwigluBwdSmem, stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM,
-                    p0, tmo)
+                    p0, kNoSplitTail, tmo)
            : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, kSwigluBwdSmem, stream, false,
                     mA0, mB0, Mi, halfi, Douti, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
@@ -871,7 +943,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   p1.s = s_out;
   p1.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
   e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads,
-                    kPairDgradGivenSSmem, stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1,
+                    kPairDgradGivenSSmem, stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, kNoSplitTail,
                     tmo)
            : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kDgradGivenSSmem, stream,
                     false, mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
@@ -922,6 +994,12 @@ coda_status_t coda_set_mma_mode(int mode) {
 }
 
 int coda_get_mma_mode(void) { return g_mma_mode.load(); }
+
+coda_status_t coda_set_split_tail(int enable) {
+  if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
+  g_split_tail.store(enable);
+  return CODA_OK;
+}
 
 coda_status_t coda_set_fold_rowreduce(int enable) {
   if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;

@@ -383,6 +383,7 @@ struct EpiRowScale : EpiDefaultCols {
 template <bool kExtras>
 struct EpiRmsNormBackwardT : EpiDefaultCols {
   static constexpr uint32_t kStageBytesPerWarp = (kExtras ? 2 : 1) * Stage64::kBytes;
+  static constexpr bool kSplitTail = false;  // the row-flag wait needs whole tiles
 
   struct Params {
     const __nv_bfloat16* h;

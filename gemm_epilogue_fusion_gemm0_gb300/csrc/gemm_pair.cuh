@@ -17,6 +17,10 @@
 // accumulator by one arrive on CTA 0's `tempty` barrier (count 2).
 #pragma once
 
+#include <cooperative_groups.h>
+
+#include <type_traits>
+
 #include "gemm.cuh"
 
 namespace coda {
@@ -38,6 +42,129 @@ static_assert(kPairBarBytes + 8 <= 256, "barrier area overflows its reserved 256
 
 static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
+// ---------------------------------------------------------------------------
+// Stream-K tail.  With T tiles on U CTA pairs, T = W U + R (0 < R < U), plain
+// round-robin leaves the last wave R/U full.  Instead:
+//   - tiles [0, dp_tiles), dp_tiles = (W - 1) U, are whole work items, tile t
+//     going to pair t mod U;
+//   - the remaining S = U + R tiles are laid end to end along K (S * nk k-blocks
+//     of kBK) and cut into U contiguous slices, pair i taking
+//     [floor(i S nk / U), floor((i + 1) S nk / U)).
+// Every pair then runs the same number of k-blocks, up to one.  A slice is at
+// least nk long, so a tile is shared by at most two pairs: the owner, whose
+// slice holds the tile's first k-block, and the next pair, whose slice starts
+// inside the tile.  That pair's first item is the tile's tail: its epilogue
+// warps write the fp32 accumulator to a partial slot and publish it with a
+// release flag.  The owner's epilogue waits for the flag, adds the partial into
+// its TMEM accumulator and runs the policy on the sum.  A partial is always its
+// pair's first tail item and waits for nothing but its own data, so the owner's
+// wait always ends.
+// The flag token is *epoch + 1, epoch being a counter in the caller's workspace
+// that the launch advances after a grid-wide barrier (the launch is then
+// cooperative): flags of earlier launches never match, so the slots need no
+// clearing and a launch replayed from a CUDA graph draws a fresh token.
+// Policies whose epilogue waits on other tiles (the data gradient's row flags)
+// are launched without a split tail.
+// ---------------------------------------------------------------------------
+struct SkParams {
+  int dp_tiles;     // tiles handed out whole; >= the tile count: no split tail
+  float* part;      // [S][2 CTAs][128 x 256] fp32 partial accumulators
+  uint64_t* flags;  // [S][2 CTAs]
+  uint64_t* epoch;  // launch counter (any initial value); null when the tail is not split
+};
+
+constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr};
+
+// A policy opts out of the split tail (its epilogue waits on other tiles) with
+// `static constexpr bool kSplitTail = false;`; the kernel then compiles without it.
+template <class E, class = void>
+struct SplitsTail : std::true_type {};
+template <class E>
+struct SplitsTail<E, std::void_t<decltype(E::kSplitTail)>> : std::bool_constant<E::kSplitTail> {};
+
+constexpr int kItemWhole = 0;  // all nk k-blocks of the tile
+constexpr int kItemOwner = 1;  // k-blocks [0, kb1): adds the partial, runs the epilogue
+constexpr int kItemTail = 2;   // k-blocks [kb0, nk): writes the partial
+
+struct WorkItem {
+  int tile, kb0, kb1, kind;
+};
+
+// The split items of one CTA pair, in order (the same sequence in the producer,
+// MMA and epilogue roles, each of which first runs its whole tiles
+// pair, pair + npairs, ... below dp_end).
+struct SplitWork {
+  int nk, sk_base;
+  long long kpos, kend;
+  __device__ __forceinline__ SplitWork(int pair, int npairs, int num_tiles, int dp_end, int nk_)
+      : nk(nk_), sk_base(dp_end) {
+    const long long tot = static_cast<long long>(num_tiles - dp_end) * nk_;
+    kpos = tot * pair / npairs;
+    kend = tot * (pair + 1) / npairs;
+  }
+  __device__ __forceinline__ bool next(WorkItem& w) {
+    if (kpos >= kend) return false;
+    const int s = static_cast<int>(kpos / nk);
+    w.tile = sk_base + s;
+    w.kb0 = static_cast<int>(kpos - static_cast<long long>(s) * nk);
+    w.kb1 = static_cast<int>(min(static_cast<long long>(nk), w.kb0 + (kend - kpos)));
+    w.kind = w.kb0 > 0 ? kItemTail : (w.kb1 < nk ? kItemOwner : kItemWhole);
+    kpos += w.kb1 - w.kb0;
+    return true;
+  }
+};
+
+// Partial slot layout: the 128 x 256 fp32 block of one CTA in float4 units,
+// stored so that a warp's 32 rows of one 16-byte column group are 512
+// contiguous bytes.  Each epilogue thread owns one row and one 128-column half
+// (4 chunks of 32 columns, 8 float4 each).
+constexpr int kSkChunks = kBN / 2 / 32;
+constexpr size_t kSkSlotFloats = 128 * kBN;
+__device__ __forceinline__ size_t sk_part_index4(int half, int ch, int v, int row) {
+  return static_cast<size_t>(((half * kSkChunks + ch) * 8 + v) * 128 + row);
+}
+
+// Tail item: this thread's row and half of the accumulator -> the partial slot.
+__device__ __forceinline__ void sk_write_partial(uint32_t taddr, float4* slot, int half, int row) {
+#pragma unroll 1
+  for (int ch = 0; ch < kSkChunks; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(taddr + half * (kBN / 2) + ch * 32, v);
+    tmem_ld_wait(v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      slot[sk_part_index4(half, ch, j, row)] =
+          make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                      __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+  }
+}
+
+// Owner item: accumulator += partial, in place in TMEM.  The partial's loads
+// are issued before the TMEM read of the same chunk so that the two latencies
+// overlap.
+__device__ __forceinline__ void sk_add_partial(uint32_t taddr, const float4* slot, int half,
+                                               int row) {
+#pragma unroll 1
+  for (int ch = 0; ch < kSkChunks; ++ch) {
+    const uint32_t col = taddr + half * (kBN / 2) + ch * 32;
+    float4 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = __ldcg(slot + sk_part_index4(half, ch, j, row));
+    uint32_t v[32];
+    tmem_ld32(col, v);
+    tmem_ld_wait(v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + q[j].x);
+      v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + q[j].y);
+      v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + q[j].z);
+      v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + q[j].w);
+    }
+    tmem_st32(col, v);
+  }
+  tmem_st_wait();
+}
+
 // plus the policy's store-staging buffers after the barrier area (see cta_smem_bytes)
 template <class Epi>
 __host__ __device__ constexpr uint32_t pair_smem_bytes() {
@@ -51,7 +178,8 @@ template <class Epi, bool kBMNMajor, bool kAMNMajor = false, bool kFp8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
-                              int group_m, const typename Epi::Params ep, uint64_t timeout_ns) {
+                              int group_m, const typename Epi::Params ep, const SkParams sk,
+                              uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -85,6 +213,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int num_tiles = mt * nt;
   const TileMap tmap{mt, nt, group_m};
   const WaitCtl wc{timeout_ns, &g_coda_status, abort_flag};
+  constexpr bool kSplit = SplitsTail<Epi>::value;
+  const int dp_end = kSplit ? min(sk.dp_tiles, num_tiles) : num_tiles;  // whole tiles below
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -117,15 +247,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued_mask = 0, last_par = 0;
       bool ok = true;
-      uint32_t wave = 0;
-      for (int t = pair; ok && t < num_tiles; t += npairs, ++wave) {
+      const auto loads = [&](const WorkItem& w) {
         int mb, nb;
-        tmap.coords(t, mb, nb);
+        tmap.coords(w.tile, mb, nb);
         const int arow = mb * kPairBM + static_cast<int>(rank) * 128;
         const int bcol = nb * kBN + static_cast<int>(rank) * 128;  // K-major B rows
-        const bool reverse = kSerpentineK && (wave & 1u);
-        for (int kbi = 0; kbi < nk; ++kbi) {
-          const int kb = reverse ? nk - 1 - kbi : kbi;
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -162,6 +289,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ph ^= 1u;
           }
         }
+      };
+      for (int t = pair; ok && t < dp_end; t += npairs) loads(WorkItem{t, 0, nk, kItemWhole});
+      if constexpr (kSplit) {
+        SplitWork work(pair, npairs, num_tiles, dp_end, nk);
+        WorkItem w;
+        while (ok && work.next(w)) loads(w);
       }
       if (!ok && leader) {
         // Let every issued copy (of both CTAs) land before the pair can exit.
@@ -184,16 +317,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         uint32_t it = 0;
         bool ok = true;
-        for (int t = pair; ok && t < num_tiles; t += npairs, ++it) {
+        const auto mmas = [&](const WorkItem& w) {
           const uint32_t b = it & 1u;
           const uint32_t aph = (it >> 1) & 1u;
           if (!bounded_wait(bar_tempty + 8u * b, aph ^ 1u, wc, kSiteMmaTmemEmpty)) {
             ok = false;
-            break;
+            return;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * kBN;
-          for (int kb = 0; kb < nk; ++kb) {
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!bounded_wait(bar_full + 8u * s, ph, wc, kSiteMmaFull)) {
               ok = false;
               break;
@@ -213,9 +346,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                           1024)
                             : sdesc_sw128(b0 + k * 32, 16, 1024);
               if constexpr (kFp8)
-                umma_f8_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_f8_pair(d_tmem, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
               else
-                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
             }
             umma_commit_pair_mc(bar_empty + 8u * s, 0x3);
             if (++s == kPairStages) {
@@ -223,8 +356,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ph ^= 1u;
             }
           }
-          if (!ok) break;
+          if (!ok) return;
           umma_commit_pair_mc(bar_tfull + 8u * b, 0x3);
+        };
+        for (int t = pair; ok && t < dp_end; t += npairs, ++it) mmas(WorkItem{t, 0, nk, kItemWhole});
+        if constexpr (kSplit) {
+          SplitWork work(pair, npairs, num_tiles, dp_end, nk);
+          WorkItem w;
+          for (; ok && work.next(w); ++it) mmas(w);
         }
         // Always signal `drain` in both CTAs once every MMA issued here is done.
         umma_commit_pair_mc(bar_drain, 0x3);
@@ -244,28 +383,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     uint32_t it = 0;
-    for (int t = pair; t < num_tiles; t += npairs, ++it) {
+    const auto drain = [&](const WorkItem& w) -> bool {
       const uint32_t b = it & 1u;
       const uint32_t aph = (it >> 1) & 1u;
       int mb, nb;
-      tmap.coords(t, mb, nb);
+      tmap.coords(w.tile, mb, nb);
       const bool ok = bounded_wait(bar_tfull + 8u * b, aph, wc, kSiteEpiTmemFull);
-      if (!epi_all(ok)) break;
+      if (!epi_all(ok)) return false;
       tc_fence_after();
-      TileCtx c;
-      c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
-      c.mb = mb * 2 + static_cast<int>(rank);  // this CTA's 128-row slab
-      c.nb = nb;
-      c.row = row;
-      c.half = half;
-      c.M = M;
-      c.N = N;
-      c.nt = nt;
-      c.stage = base + kPairSmemBar + 256u + static_cast<uint32_t>(warp - 2) * Epi::kStageBytesPerWarp;
-      Epi::apply(ep, wc, c);
+      if (kSplit && w.kind != kItemWhole) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
+        // split tile: this CTA's 128-row half of the tile's partial slot and flag
+        const size_t slot = static_cast<size_t>(w.tile - sk.dp_tiles) * 2 + rank;
+        float4* part = reinterpret_cast<float4*>(sk.part + slot * kSkSlotFloats);
+        uint64_t* flag = sk.flags + slot;
+        if (w.kind == kItemTail) {
+          sk_write_partial(taddr, part, half, row);
+          __threadfence();
+          named_bar_sync(1, kEpiThreads);
+          if (threadIdx.x == kEpiFirstThread) {
+            const uint64_t token = *reinterpret_cast<volatile uint64_t*>(sk.epoch) + 1;
+            st_release_gpu_u64(flag, token);
+          }
+        } else {
+          if (threadIdx.x == kEpiFirstThread) {
+            const uint64_t token = *reinterpret_cast<volatile uint64_t*>(sk.epoch) + 1;
+            flag_wait(flag, token, wc, kSiteSplitTail);
+            __threadfence();
+          }
+          named_bar_sync(1, kEpiThreads);
+          sk_add_partial(taddr, part, half, row);
+          // a policy may read columns another thread just wrote (SwiGLU pairs
+          // column j with j + 128): all stores land before any thread reads
+          tc_fence_before();
+          named_bar_sync(1, kEpiThreads);
+          tc_fence_after();
+        }
+      }
+      if (!kSplit || w.kind != kItemTail) {
+        TileCtx c;
+        c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
+        c.mb = mb * 2 + static_cast<int>(rank);  // this CTA's 128-row slab
+        c.nb = nb;
+        c.row = row;
+        c.half = half;
+        c.M = M;
+        c.N = N;
+        c.nt = nt;
+        c.stage =
+            base + kPairSmemBar + 256u + static_cast<uint32_t>(warp - 2) * Epi::kStageBytesPerWarp;
+        Epi::apply(ep, wc, c);
+      }
       tc_fence_before();
       named_bar_sync(1, kEpiThreads);
       if (threadIdx.x == kEpiFirstThread) mbar_arrive_cluster(mapa_shared(bar_tempty + 8u * b, 0));
+      return true;
+    };
+    bool go = true;
+    for (int t = pair; go && t < dp_end; t += npairs, ++it) go = drain(WorkItem{t, 0, nk, kItemWhole});
+    if constexpr (kSplit) {
+      SplitWork work(pair, npairs, num_tiles, dp_end, nk);
+      WorkItem w;
+      for (; go && work.next(w); ++it) go = drain(w);
     }
   }
 
@@ -276,7 +455,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc_pair(tmem_base, kTmemCols);
   }
-  Epi::at_exit(ep);
+  if (kSplit && sk.epoch != nullptr) {
+    // split tail: every flag of this launch has been read once the grid barrier
+    // is passed; advance the launch counter
+    cooperative_groups::this_grid().sync();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *sk.epoch = *sk.epoch + 1;
+  } else {
+    Epi::at_exit(ep);
+  }
 }
 
 }  // namespace coda

@@ -68,7 +68,10 @@ typedef enum {
 
 /* Bytes of device workspace coda_fwd needs: the bf16 GEMM1 operand
  * hg = h * gamma ([M, d]) and the fp32 partial sums of h^2, two per row and
- * 256-column tile.  Returns 0 for M == 0. */
+ * 256-column tile, then the split-tail region of the two GEMMs: up to
+ * min(T, 160) partial accumulators of 256 x 256 fp32 (T = the larger GEMM's
+ * count of 256 x 256 tiles), one 64-bit flag per 128-row half of each, and a
+ * 256-byte slot holding a launch counter.  Returns 0 for M == 0. */
 CODA_API size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /* Bytes of device workspace coda_bwd_dgrad needs: fp32 partial row
@@ -92,7 +95,16 @@ CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1)
  *   r_out  [M]      fp32 out    (inverse RMS per row; saved for backward)
  *   y_out  [M, N1]  bf16 out
  *   workspace: device memory of at least coda_fwd_workspace_bytes(M, d, N1)
- *   bytes (contents on entry are ignored; clobbered).
+ *   bytes.  Any initial contents work and the call clobbers them, except that
+ *   two calls sharing a workspace must not run concurrently.
+ * Split tail: when a GEMM's 256 x 256 tiles do not fill whole waves of CTA
+ * pairs, its last U + R tiles (U pairs, R tiles past the last full wave) are
+ * shared out along K so that every pair ends together; a tile cut in two is
+ * finished by the pair holding its first K block, which adds the other pair's
+ * fp32 partial (published with a flag whose token comes from the launch
+ * counter in the workspace) before the epilogue.  Such a launch is
+ * cooperative.  Results then differ from the whole-tile order only in fp32
+ * summation order; coda_set_split_tail(0) turns it off.
  */
 CODA_API coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
                        const coda_bf16* gamma, const coda_bf16* W1, float eps,
@@ -258,6 +270,12 @@ CODA_API int coda_get_mma_mode(void);
  * 0 (the default) keeps the separate light auxiliary reduction.  Returns
  * CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_fold_rowreduce(int enable);
+
+/* Forward variant: 1 (the default) splits the tail of the forward's CTA-pair
+ * GEMMs along K when their tiles do not fill whole waves (see coda_fwd); 0
+ * hands out whole tiles only.  Returns CODA_ERR_INVALID_ARG for any other
+ * value.  Process-wide. */
+CODA_API coda_status_t coda_set_split_tail(int enable);
 
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records

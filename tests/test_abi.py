@@ -46,17 +46,30 @@ def test_status_strings(lib):
         assert lib.status_string(code) == name
 
 
+def _split_tail_bytes(M, d, N1):
+    # min(T, 160) slots of 256 x 256 fp32 partials, a u64 flag per 128-row half of each
+    # (rounded up to 256 B), a 256-byte launch-counter slot; T = 256 x 256 tiles of the
+    # larger GEMM
+    tiles = -(-M // 256) * max(-(-d // 256), -(-N1 // 256))
+    slots = min(tiles, 160)
+    return slots * 256 * 256 * 4 + -(-(slots * 16) // 256) * 256 + 256
+
+
 def test_workspace_sizes(lib):
-    # hg [M,d] bf16 + partial sums [2 * ceil(d/256), M] fp32, each rounded up to 256 B
+    # hg [M,d] bf16 + partial sums [2 * ceil(d/256), M] fp32, each rounded up to 256 B,
+    # then the split-tail region
     M, d, N1 = 8192, 4096, 28672
-    assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 32 * M * 4
+    assert _split_tail_bytes(M, d, N1) == 160 * 262144 + 2560 + 256
+    assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 32 * M * 4 + _split_tail_bytes(M, d, N1)
     assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == M * d * 2
     # qpart [2 * 16, M] fp32 + flags [2 * ceil(M/256) * 16] u64 (one per 128-row slab and column
     # tile) + a 256-byte slot for the launch counter
     assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 32 * M * 4 + 64 * 16 * 8 + 256
     assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 2560 + 256 + 256  # 4 slabs x 1 tile
     assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
-    assert lib.coda_fwd_workspace_bytes(300, 328, 776) == 196864 + 4864  # ragged: rounded up
+    assert _split_tail_bytes(300, 328, 776) == 8 * 262144 + 256 + 256  # 2 x 4 tiles
+    assert lib.coda_fwd_workspace_bytes(300, 328, 776) == (  # ragged: rounded up
+        196864 + 4864 + _split_tail_bytes(300, 328, 776))
     assert lib.coda_fwd_workspace_bytes(10, 12, 16) == 0  # d % 8 != 0: unsupported
 
 

@@ -347,6 +347,146 @@ def test_folded_rowreduce_is_bit_identical(B, mode, M, d, N1):
     check_r(f64(fold[1]), ref.r)
 
 
+# ----------------------------------------------------------------------------- split tail (stream-K)
+# 8 x 20 = 160 CTA-pair tiles in both GEMMs: two full waves of 76 pairs plus 8
+# tiles, so the last 84 tiles are shared out along K.  The second shape is ragged
+# in M, d (= K of both GEMMs) and N1.
+SPLIT_SHAPES = [(2048, 5120, 5120), (2000, 5000, 5064)]
+
+
+def fwd_epoch(ws):
+    """The forward's launch counter: the last 8-byte slot of its workspace."""
+    n = ws.numel()
+    return int(ws[n - 256:n - 248].view(torch.int64).item())
+
+
+def split_launches(M, d, N1, pairs):
+    """How many of the forward's two GEMMs split their tail on `pairs` CTA pairs:
+    at least two waves of tiles, a last wave at most half full, at least 64
+    k-blocks of 64 per tile (K = d for both), and at most 160 split tiles."""
+    nk = -(-d // 64)
+    tiles = [-(-M // 256) * -(-d // 256), -(-M // 256) * -(-N1 // 256)]
+    return sum(1 for t in tiles
+               if t // pairs >= 2 and 0 < 2 * (t % pairs) <= pairs and nk >= 64
+               and pairs + t % pairs <= 160)
+
+
+@pytest.mark.parametrize("M,d,N1", SPLIT_SHAPES)
+def test_split_tail_forward_matches_oracle(B, M, d, N1):
+    """The forward with the split tail on (the default) and off: both match the
+    oracle on every row, the split run advances the workspace's launch counter
+    once per split GEMM, and the data gradient taken from the split forward's h
+    and r matches too."""
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=31)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    args = (g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5)
+    ref = oracle.forward(f64(t["x"]), f64(t["W0"]), f64(t["z"]), f64(t["gamma"]), f64(t["W1"]), 1e-5)
+    ws = B.workspace(B.coda_fwd_workspace_bytes(M, d, N1), dev)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        outs = {}
+        for split in (0, 1):
+            B.coda_set_split_tail(split)
+            e0 = fwd_epoch(ws)
+            outs[split] = B.coda_fwd(*args, ws=ws)
+            torch.cuda.synchronize()
+            st, detail = B.coda_get_device_status()
+            assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+            want = split_launches(M, d, N1, pairs) if split else 0
+            assert (fwd_epoch(ws) - e0) % 2 ** 64 == want
+        dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
+        dh = B.coda_bwd_dgrad(dy_cpu.to(dev), g["W1"], outs[1][0], outs[1][1], g["gamma"])
+    finally:
+        B.coda_set_split_tail(1)
+        B.coda_set_mma_mode(old)
+    if pairs == 76:
+        assert split_launches(M, d, N1, pairs) == 2
+    for split, (h, r, y) in outs.items():
+        check("h", f64(h), ref.h, TOL_HY)
+        check_r(f64(r), ref.r)
+        check("y", f64(y), ref.y, TOL_HY)
+    # the split changes only the fp32 summation order of the accumulators
+    assert torch.equal(outs[0][0], outs[1][0]) or check("h", f64(outs[1][0]), f64(outs[0][0]), 1e-3)
+    hG, rG = f64(outs[1][0]), f64(outs[1][1])
+    bref = oracle.backward_dgrad(f64(dy_cpu), f64(t["W1"]), hG, rG, f64(t["gamma"]))
+    check("dh", f64(dh), bref.dh, TOL_DH)
+
+
+def test_split_tail_swiglu_forward_matches_oracle(B):
+    """The SwiGLU forward's GEMM1 (8 x 40 = 320 tiles of 128 gated columns, four
+    waves of 76 pairs plus 16, 64 k-blocks each) with the split tail, against
+    the oracle."""
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        run_swiglu(B, 2048, 4096, 10240, 1e-5, seed=32)
+    finally:
+        B.coda_set_mma_mode(old)
+
+
+def test_split_tail_is_deterministic_and_replays_from_a_cuda_graph(B):
+    """Split-tail forward: repeated eager calls are bitwise identical; a captured
+    call replayed on new inputs (copied into the captured buffers) equals the
+    eager call on those inputs, so no replay consumes a partial that an earlier
+    launch left behind; the launch counter advances by two per replay."""
+    M, d, N1 = SPLIT_SHAPES[1]
+    dev = torch.device("cuda:0")
+    sets = []
+    for seed in (33, 34):
+        t = synth.make_forward_inputs(M, d, N1, seed=seed)
+        sets.append({k: v.to(dev) for k, v in t.items() if k != "_rng"})
+    buf = {k: torch.empty_like(v) for k, v in sets[0].items()}
+    bf = torch.bfloat16
+    h = torch.empty((M, d), dtype=bf, device=dev)
+    r = torch.empty((M,), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N1), dtype=bf, device=dev)
+    ws = B.workspace(B.coda_fwd_workspace_bytes(M, d, N1), dev)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    n_split = split_launches(M, d, N1, pairs)
+
+    def fwd():
+        B.coda_fwd(buf["x"], buf["W0"], buf["z"], buf["gamma"], buf["W1"], 1e-5, h=h, r=r, y=y,
+                   ws=ws, stream=torch.cuda.current_stream())
+
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        for k in buf:
+            buf[k].copy_(sets[0][k])
+        fwd()
+        torch.cuda.synchronize()
+        first = [t.clone() for t in (h, r, y)]
+        fwd()
+        torch.cuda.synchronize()
+        for got, want in zip((h, r, y), first):
+            assert torch.equal(got, want)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fwd()
+        for data in sets[::-1] + sets:
+            for k in buf:
+                buf[k].copy_(data[k])
+            fwd()
+            torch.cuda.synchronize()
+            ref = [t.clone() for t in (h, r, y)]
+            for t in (h, y):
+                t.fill_(float("nan"))
+            r.fill_(-1.0)
+            e0 = fwd_epoch(ws)
+            graph.replay()
+            torch.cuda.synchronize()
+            st, detail = B.coda_get_device_status()
+            assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+            for got, want in zip((h, r, y), ref):
+                assert torch.equal(got, want)
+            assert (fwd_epoch(ws) - e0) % 2 ** 64 == n_split
+    finally:
+        B.coda_set_mma_mode(old)
+
+
 # ----------------------------------------------------------------------------- CUDA graphs
 def test_step_replays_from_a_cuda_graph(B, mode):
     """coda_fwd + coda_bwd_dgrad captured once into a CUDA graph and replayed,
