@@ -732,11 +732,17 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   return CODA_OK;
 }
 
+// CTA-pair tiles of the full backward's largest split-capable GEMM (dW1, dx or
+// dW0), which sizes its split-tail region
+int64_t bwd_pair_tiles(int64_t M, int64_t d, int64_t N1) {
+  return std::max(cdiv(d, kPairBM) * cdiv(std::max(d, N1), kBN), cdiv(M, kPairBM) * cdiv(d, kBN));
+}
+
 size_t coda_bwd_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
   const int64_t slabs = std::max(2 * cdiv(M, kPairBM), cdiv(M, kBM));
   return coda_bwd_dgrad_workspace_bytes(M, d, N1) + align256(static_cast<size_t>(M) * d * 2) +
-         align256(static_cast<size_t>(4 * slabs) * d * 4);
+         align256(static_cast<size_t>(4 * slabs) * d * 4) + sk_region_bytes(bwd_pair_tiles(M, d, N1));
 }
 
 coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16* W0,
@@ -778,6 +784,11 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   char* rest = ws + coda_bwd_dgrad_workspace_bytes(M, d, N1);
   __nv_bfloat16* h2 = reinterpret_cast<__nv_bfloat16*>(rest);
   float* gpart = reinterpret_cast<float*>(rest + align256(static_cast<size_t>(M) * d * 2));
+  const SkRegion skr =
+      sk_region(rest + align256(static_cast<size_t>(M) * d * 2) +
+                    align256(static_cast<size_t>(4 * std::max(2 * cdiv(M, kPairBM), cdiv(M, kBM))) *
+                             d * 4),
+                bwd_pair_tiles(M, d, N1));
 
   const uint32_t bbox = pair ? 128 : kBN;
   CUtensorMap mDy, mW1, mH2, mDyMN, mDh, mW0, mX, mDhMN;
@@ -825,8 +836,11 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   pw1.out = dW1_out;
   const int mtw = static_cast<int>(cdiv(d, pair ? kPairBM : kBM));
   const int ntw1 = static_cast<int>(cdiv(N1, kBN));
-  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * ntw1), kThreads, kPairWgradSmem,
-                    stream, false, mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, kNoSplitTail, tmo)
+  const int64_t nkw = cdiv(M, kBK);  // k-blocks of the weight gradients (K = tokens)
+  const int npw1 = std::min(max_pairs, mtw * ntw1);
+  const SkParams skw1 = plan_split_tail(skr, static_cast<int64_t>(mtw) * ntw1, npw1, nkw);
+  e = pair ? launch(kPairWgrad, 2 * npw1, kThreads, kPairWgradSmem, stream, skw1.epoch != nullptr,
+                    mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, skw1, tmo)
            : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kWgradSmem, stream, false, mH2,
                     mDyMN, di, N1i, Mi, kGroupM, pw1, tmo);
   if (e != cudaSuccess) {
@@ -839,8 +853,10 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   px.r = nullptr;
   px.y_out = reinterpret_cast<__nv_bfloat16*>(dx_out);
   const int mtx = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
-  e = pair ? launch(kPairXgrad, 2 * std::min(max_pairs, mtx * nt), kThreads, kPairXgradSmem,
-                    stream, false, mDh, mW0, Mi, di, di, kPairGroupM, px, kNoSplitTail, tmo)
+  const int npx = std::min(max_pairs, mtx * nt);
+  const SkParams skx = plan_split_tail(skr, static_cast<int64_t>(mtx) * nt, npx, cdiv(d, kBK));
+  e = pair ? launch(kPairXgrad, 2 * npx, kThreads, kPairXgradSmem, stream, skx.epoch != nullptr,
+                    mDh, mW0, Mi, di, di, kPairGroupM, px, skx, tmo)
            : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kXgradSmem, stream, false, mDh,
                     mW0, Mi, di, di, kGroupM, px, tmo);
   if (e != cudaSuccess) {
@@ -851,8 +867,10 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   // 5. dW0 = x^T dh   (K = tokens)
   EpiStoreF32::Params pw0 = {};
   pw0.out = dW0_out;
-  e = pair ? launch(kPairWgrad, 2 * std::min(max_pairs, mtw * nt), kThreads, kPairWgradSmem,
-                    stream, false, mX, mDhMN, di, di, Mi, kPairGroupM, pw0, kNoSplitTail, tmo)
+  const int npw0 = std::min(max_pairs, mtw * nt);
+  const SkParams skw0 = plan_split_tail(skr, static_cast<int64_t>(mtw) * nt, npw0, nkw);
+  e = pair ? launch(kPairWgrad, 2 * npw0, kThreads, kPairWgradSmem, stream, skw0.epoch != nullptr,
+                    mX, mDhMN, di, di, Mi, kPairGroupM, pw0, skw0, tmo)
            : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kWgradSmem, stream, false, mX,
                     mDhMN, di, di, Mi, kGroupM, pw0, tmo);
   if (e != cudaSuccess) {

@@ -235,8 +235,12 @@ CODA_API coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_b
  *   dh_res [M, d] bf16 or NULL                                   (inputs)
  *   dh_out [M, d] bf16 (= dz), dx_out [M, d] bf16, dgamma_out [d] fp32,
  *   dW0_out [d, d] fp32, dW1_out [d, N1] fp32                    (outputs)
- *   workspace: at least coda_bwd_workspace_bytes(M, d, N1) bytes.
- * Launch 1 is cooperative, as in coda_bwd_dgrad.  Conventions as coda_fwd.
+ *   workspace: at least coda_bwd_workspace_bytes(M, d, N1) bytes: the
+ *   coda_bwd_dgrad workspace, h2, the dgamma partials and a split-tail region
+ *   as in coda_fwd, sized for the largest of launches 3-5.
+ * Launch 1 is cooperative, as in coda_bwd_dgrad; launches 3-5 split their tail
+ * (and are then cooperative) under the same conditions as coda_fwd's GEMMs.
+ * Conventions as coda_fwd.
  */
 CODA_API size_t coda_bwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 CODA_API coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16* W0,
@@ -271,10 +275,10 @@ CODA_API int coda_get_mma_mode(void);
  * CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_fold_rowreduce(int enable);
 
-/* Forward variant: 1 (the default) splits the tail of the forward's CTA-pair
- * GEMMs along K when their tiles do not fill whole waves (see coda_fwd); 0
- * hands out whole tiles only.  Returns CODA_ERR_INVALID_ARG for any other
- * value.  Process-wide. */
+/* 1 (the default) splits the tail of the CTA-pair GEMMs of coda_fwd,
+ * coda_fwd_swiglu and coda_bwd (launches 3-5) along K when their tiles do not
+ * fill whole waves (see coda_fwd); 0 hands out whole tiles only.  Returns
+ * CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_split_tail(int enable);
 
 /* Upper bound, in nanoseconds, of every device-side wait launched after this

@@ -46,13 +46,16 @@ def test_status_strings(lib):
         assert lib.status_string(code) == name
 
 
-def _split_tail_bytes(M, d, N1):
+def _split_tail_bytes_for_tiles(tiles):
     # min(T, 160) slots of 256 x 256 fp32 partials, a u64 flag per 128-row half of each
-    # (rounded up to 256 B), a 256-byte launch-counter slot; T = 256 x 256 tiles of the
-    # larger GEMM
-    tiles = -(-M // 256) * max(-(-d // 256), -(-N1 // 256))
+    # (rounded up to 256 B), a 256-byte launch-counter slot
     slots = min(tiles, 160)
     return slots * 256 * 256 * 4 + -(-(slots * 16) // 256) * 256 + 256
+
+
+def _split_tail_bytes(M, d, N1):
+    # the forward's region: T = 256 x 256 tiles of the larger GEMM
+    return _split_tail_bytes_for_tiles(-(-M // 256) * max(-(-d // 256), -(-N1 // 256)))
 
 
 def test_workspace_sizes(lib):
@@ -124,8 +127,11 @@ def test_full_backward_workspace_and_validation(lib):
     E = {v: k for k, v in lib.STATUS_NAMES.items()}
     M, d, N1 = 8192, 4096, 28672
     # dgrad workspace + h2 [M, d] bf16 + dgamma partials [4 * 64 slabs, d] fp32
+    # + a split-tail region sized for the largest of dW1 (d x N1), dx (M x d), dW0 (d x d)
+    tiles = max(-(-d // 256) * -(-max(d, N1) // 256), -(-M // 256) * -(-d // 256))
     assert lib.coda_bwd_workspace_bytes(M, d, N1) == (
-        lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) + M * d * 2 + 4 * 64 * d * 4)
+        lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) + M * d * 2 + 4 * 64 * d * 4
+        + _split_tail_bytes_for_tiles(tiles))
     raw = lib.raw()
 
     def call(res=0, M=128, wsb=1 << 30, dgamma=FAKE):

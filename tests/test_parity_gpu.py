@@ -487,6 +487,41 @@ def test_split_tail_is_deterministic_and_replays_from_a_cuda_graph(B):
         B.coda_set_mma_mode(old)
 
 
+def test_split_tail_full_backward_matches_oracle(B):
+    """coda_bwd at (4040, 4096, 1024): dx (16 x 16 tiles, K = d) and dW0 (16 x 16
+    tiles, K = 4040 tokens, ragged: 64 k-blocks) split their tails, dW1 (16 x 4
+    tiles) does not; every gradient against the oracle, and the backward's
+    split-tail counter (the last 8-byte slot of its workspace) advances once per
+    split launch."""
+    M, d, N1 = 4040, 4096, 1024
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=35)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        h, r, _ = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5)
+        dy = synth.make_grad_output(t["_rng"], M, N1)
+        res = synth.make_residual_grad(t["_rng"], M, d)
+        ws = B.workspace(B.coda_bwd_workspace_bytes(M, d, N1), dev)
+        e0 = fwd_epoch(ws)
+        o = B.coda_bwd(dy.to(dev), g["x"], g["W0"], g["W1"], h, r, g["gamma"], res.to(dev), ws=ws)
+        torch.cuda.synchronize()
+    finally:
+        B.coda_set_mma_mode(old)
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert (fwd_epoch(ws) - e0) % 2 ** 64 == 2
+    ref = oracle.backward_full(f64(dy), f64(t["x"]), f64(t["W0"]), f64(t["W1"]), f64(h.cpu()),
+                               f64(r.cpu()), f64(t["gamma"]), f64(res))
+    check("dh", f64(o["dh"].cpu()), ref.dh, TOL_DH)
+    check("dx", f64(o["dx"].cpu()), ref.dx, TOL_DH)
+    check("dgamma", f64(o["dgamma"].cpu())[None, :], ref.dgamma[None, :], TOL_HY)
+    check("dW0", f64(o["dW0"].cpu()), ref.dW0, TOL_HY)
+    check("dW1", f64(o["dW1"].cpu()), ref.dW1, TOL_HY)
+
+
 # ----------------------------------------------------------------------------- CUDA graphs
 def test_step_replays_from_a_cuda_graph(B, mode):
     """coda_fwd + coda_bwd_dgrad captured once into a CUDA graph and replayed,
