@@ -214,7 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const TileMap tmap{mt, nt, group_m};
   const WaitCtl wc{timeout_ns, &g_coda_status, abort_flag};
   constexpr bool kSplit = SplitsTail<Epi>::value;
-  const int dp_end = kSplit ? min(sk.dp_tiles, num_tiles) : num_tiles;  // whole tiles below
+  // whole tiles below dp_end; a split needs the slots (never planned without them)
+  const int dp_end = (kSplit && sk.part != nullptr) ? min(sk.dp_tiles, num_tiles) : num_tiles;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
