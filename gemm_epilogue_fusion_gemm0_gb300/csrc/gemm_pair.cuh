@@ -15,6 +15,10 @@
 // arms it with both CTAs' bytes); the MMA commit is multicast to the `empty`,
 // `tfull` and `drain` barriers of both CTAs; each CTA's epilogue releases an
 // accumulator by one arrive on CTA 0's `tempty` barrier (count 2).
+//
+// Work: the kernel is persistent; tile t goes to pair t mod (number of pairs),
+// except that a launch may share its last tiles out along K (the split tail
+// below) when whole tiles would leave the last wave of pairs mostly idle.
 #pragma once
 
 #include <cooperative_groups.h>
