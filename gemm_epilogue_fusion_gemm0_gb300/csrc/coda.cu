@@ -185,7 +185,7 @@ DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_fold_rowreduce{0};  // 1: r computed in GEMM1's epilogue (no separate launch)
-std::atomic<int> g_split_tail{1};      // 1: stream-K tail in the forward's CTA-pair GEMMs
+std::atomic<int> g_split_tail{1};      // 1: split tails in the CTA-pair GEMMs that qualify
 std::atomic<int> g_mma_mode{1};  // 0: single-CTA 128x256 tiles, 1: CTA-pair 256x256 tiles (default)
 cudaEvent_t* g_launch_events = nullptr;  // measurement hook (coda_set_launch_events)
 int g_launch_events_n = 0;
