@@ -167,3 +167,26 @@ def test_no_device_is_reported_without_gpu(lib):
     E = {v: k for k, v in lib.STATUS_NAMES.items()}
     assert _fwd(lib) == E["CODA_ERR_NO_DEVICE"]
     assert _bwd(lib) == E["CODA_ERR_NO_DEVICE"]
+
+
+def test_binding_refuses_to_load_without_the_library(tmp_path):
+    """The product path has no CPU fallback: importing the binding from a copy of
+    the package without libcoda.so raises ImportError."""
+    import shutil
+    import subprocess
+    import sys
+
+    pkg = "gemm_epilogue_fusion_gemm0_gb300"
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), pkg)
+    dst = tmp_path / pkg
+    shutil.copytree(src, dst, ignore=shutil.ignore_patterns("*.so", "*.so.tmp", "csrc", "__pycache__"))
+    code = ("import importlib, sys\n"
+            "try:\n"
+            f"    importlib.import_module('{pkg}.binding')\n"
+            "except ImportError as e:\n"
+            "    print('ImportError:', e); sys.exit(0)\n"
+            "sys.exit(1)\n")
+    res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True,
+                         timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert "libcoda.so not found" in res.stdout
