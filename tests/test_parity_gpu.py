@@ -415,6 +415,25 @@ def test_split_tail_forward_matches_oracle(B, M, d, N1):
     check("dh", f64(dh), bref.dh, TOL_DH)
 
 
+# Seeded ragged shapes of two to four waves of CTA-pair tiles and 51 to 92 k-blocks:
+# with 76 pairs some split GEMM0 and/or GEMM1 (2600x5848x7520 both, 1536x4112x7664
+# GEMM1 only, 2600x5744x6272 GEMM0 only) and some split nothing; every one is
+# checked against the oracle on sampled rows, forward and data gradient.
+SWEEP_SHAPES = [(1536, 4504, 6056), (2600, 5848, 7520), (1536, 4112, 7664), (2600, 5744, 6272),
+                (2304, 5544, 6240), (2304, 5600, 5800), (1800, 3208, 6512), (1536, 3648, 5176)]
+
+
+@pytest.mark.parametrize("M,d,N1", SWEEP_SHAPES)
+def test_split_tail_shape_sweep(B, M, d, N1):
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        rows = synth.sample_rows(M, 256, seed=3)
+        run_case(B, M, d, N1, 1e-5, seed=5, rows=rows)
+    finally:
+        B.coda_set_mma_mode(old)
+
+
 def test_split_tail_swiglu_forward_matches_oracle(B):
     """The SwiGLU forward's GEMM1 (8 x 40 = 320 tiles of 128 gated columns, four
     waves of 76 pairs plus 16, 64 k-blocks each) with the split tail, against
