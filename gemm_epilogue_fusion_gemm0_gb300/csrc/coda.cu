@@ -31,6 +31,8 @@ namespace coda {
 // partial sums of squares (fixed summation order over tiles).
 __global__ void rowreduce_rsqrt_kernel(const float* __restrict__ part, int nt, int M, int d,
                                        float eps, float* __restrict__ r) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float s = 0.f;
@@ -41,6 +43,8 @@ __global__ void rowreduce_rsqrt_kernel(const float* __restrict__ part, int nt, i
 // Auxiliary reduction of the backward statistic: s[m] = sum_t spart[t][m]
 // (fixed summation order over tiles).
 __global__ void rowsum_kernel(const float* __restrict__ part, int nt, int M, float* __restrict__ s) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   float acc = 0.f;
@@ -51,6 +55,8 @@ __global__ void rowsum_kernel(const float* __restrict__ part, int nt, int M, flo
 // dgamma[j] = sum_i gpart[i][j] over the per-warp column partials (fixed order).
 __global__ void colsum_kernel(const float* __restrict__ part, int nrows, int d,
                               float* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= d) return;
   float acc = 0.f;
@@ -66,6 +72,8 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const __nv_bfloat16* 
                                                            __nv_bfloat16* __restrict__ hn,
                                                            float* __restrict__ r) {
   __shared__ float warp_sums[8];
+  griddep_launch_dependents();
+  griddep_wait();
   const int m = blockIdx.x;
   if (m >= M) return;
   const __nv_bfloat16* row = h + static_cast<size_t>(m) * d;
@@ -105,6 +113,8 @@ __device__ uint64_t g_selftest_flag = 0;  // never written by anyone
 
 // Watchdog self-test: both waits run out by construction.
 __global__ void watchdog_selftest_kernel(uint64_t timeout_ns) {
+  griddep_launch_dependents();
+  griddep_wait();
   __shared__ __align__(8) uint64_t bar;
   __shared__ uint32_t abort_flag;
   if (threadIdx.x != 0) return;
@@ -330,13 +340,19 @@ cudaError_t launch(void (*kernel)(ExpT...), int grid, int block, size_t smem, cu
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // programmatic dependent launch for every kernel (griddep_wait in ptx.cuh)
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
   if (cooperative) {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<ActT>(args)...);
 }
 

@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  griddep_launch_dependents();
+  griddep_wait();  // prologue done: from here on the preceding kernel's output may be read
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

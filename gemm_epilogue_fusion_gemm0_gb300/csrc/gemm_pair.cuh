@@ -244,6 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  griddep_launch_dependents();
+  griddep_wait();  // prologue done: from here on the preceding kernel's output may be read
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)

@@ -331,6 +331,19 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation: it may start while the preceding kernel in
+// the stream is finishing, runs its prologue (barriers, TMEM, descriptor
+// prefetch; nothing that reads another kernel's output), then waits here until
+// the preceding grid has completed and its writes are visible.  Both are no-ops
+// for a launch without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream start its own prologue (it still waits for
+// this grid to complete before touching memory).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar_cluster, int32_t x, int32_t y) {
