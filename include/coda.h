@@ -32,6 +32,10 @@
  *  - Argument checks happen before anything is enqueued; on any error nothing
  *    is launched.  Device-side failures (a bounded wait that ran out) are
  *    reported later by coda_get_device_status().
+ *  - Every kernel is launched with programmatic stream serialisation: it may
+ *    begin its prologue while the kernel before it in `stream` is finishing,
+ *    and it reads no memory before that kernel has completed.  Stream order is
+ *    kept as for ordinary launches, whatever kernel precedes it.
  *  - Numerics: bf16 operands, fp32 accumulation in tensor memory, fp32
  *    epilogue arithmetic, bf16 round-to-nearest-even stores.
  */
