@@ -541,6 +541,40 @@ def test_split_tail_full_backward_matches_oracle(B):
     check("dW1", f64(o["dW1"].cpu()), ref.dW1, TOL_HY)
 
 
+# ----------------------------------------------------------------------------- stream order
+def test_kernels_see_writes_of_the_preceding_kernel(B):
+    """Every library kernel starts its prologue early (programmatic dependent
+    launch) but must read nothing before the kernel ahead of it in the stream has
+    finished: inputs rewritten by PyTorch kernels just before each call, with no
+    synchronisation in between, give the same results as the same inputs written
+    long before."""
+    M, d, N1 = 640, 512, 1280
+    dev = torch.device("cuda:0")
+    sets = []
+    for seed in (51, 52, 53):
+        t = synth.make_forward_inputs(M, d, N1, seed=seed)
+        dy = synth.make_grad_output(t["_rng"], M, N1)
+        sets.append({**{k: v.to(dev) for k, v in t.items() if k != "_rng"}, "dy": dy.to(dev)})
+    refs = []
+    for data in sets:  # reference: inputs in place long before the calls
+        h, r, y = B.coda_fwd(data["x"], data["W0"], data["z"], data["gamma"], data["W1"], 1e-5)
+        dh = B.coda_bwd_dgrad(data["dy"], data["W1"], h, r, data["gamma"])
+        torch.cuda.synchronize()
+        refs.append((h, r, y, dh))
+    buf = {k: torch.empty_like(v) for k, v in sets[0].items()}
+    for data, ref in zip(sets[::-1] + sets, refs[::-1] + refs):
+        for k in buf:  # device copies on the same stream, right before the calls
+            buf[k].copy_(data[k])
+        h, r, y = B.coda_fwd(buf["x"], buf["W0"], buf["z"], buf["gamma"], buf["W1"], 1e-5)
+        buf["gamma"].copy_(data["gamma"])  # one more kernel between the two calls
+        dh = B.coda_bwd_dgrad(buf["dy"], buf["W1"], h, r, buf["gamma"])
+        torch.cuda.synchronize()
+        for got, want in zip((h, r, y, dh), ref):
+            assert torch.equal(got, want)
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+
+
 # ----------------------------------------------------------------------------- CUDA graphs
 def test_step_replays_from_a_cuda_graph(B, mode):
     """coda_fwd + coda_bwd_dgrad captured once into a CUDA graph and replayed,
