@@ -3,7 +3,8 @@
 Argument marshalling only: torch tensors are checked for device, dtype and
 contiguity and passed as raw device pointers together with the current CUDA
 stream.  Every step of the computation runs in the library's kernels; if the
-library is missing this module raises at import time.
+library is missing this module raises at import time.  A process started with
+CODA_CHECKED_BUILD=1 loads the checked build (libcoda_checked.so) instead.
 """
 
 from __future__ import annotations
@@ -13,17 +14,28 @@ import os
 
 import torch
 
-from .build import LIB_PATH
+from .build import LIB_PATH, LIB_PATH_CHECKED
 
-if not os.path.exists(LIB_PATH):
+LIB = LIB_PATH_CHECKED if os.environ.get("CODA_CHECKED_BUILD") == "1" else LIB_PATH
+
+if not os.path.exists(LIB):
     raise ImportError(
-        f"libcoda.so not found at {LIB_PATH}: build it first "
+        f"{os.path.basename(LIB)} not found at {LIB}: build it first "
         "(python -c 'import __graft_entry__ as g; g.build()')"
     )
 
-_lib = ctypes.CDLL(LIB_PATH)
+_lib = ctypes.CDLL(LIB)
 
 CODA_OK = 0
+CODA_ERR_INVALID_ARG = 1
+CODA_ERR_UNSUPPORTED_SHAPE = 2
+CODA_ERR_MISALIGNED = 3
+CODA_ERR_WORKSPACE_TOO_SMALL = 4
+CODA_ERR_LAUNCH = 5
+CODA_ERR_DEVICE_TIMEOUT = 6
+CODA_ERR_NO_DEVICE = 7
+CODA_ERR_UNSUPPORTED_DEVICE = 8
+CODA_ERR_DEVICE_BOUNDS = 9
 STATUS_NAMES = {
     0: "CODA_OK",
     1: "CODA_ERR_INVALID_ARG",
@@ -34,6 +46,7 @@ STATUS_NAMES = {
     6: "CODA_ERR_DEVICE_TIMEOUT",
     7: "CODA_ERR_NO_DEVICE",
     8: "CODA_ERR_UNSUPPORTED_DEVICE",
+    9: "CODA_ERR_DEVICE_BOUNDS",
 }
 
 _vp, _i64, _sz, _f32, _u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_uint64
@@ -65,6 +78,7 @@ EXPORTS = {
     "coda_get_mma_mode": (ctypes.c_int, []),
     "coda_set_fold_rowreduce": (_st, [ctypes.c_int]),
     "coda_set_split_tail": (_st, [ctypes.c_int]),
+    "coda_set_col_plan": (_st, [ctypes.c_int]),
     "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
                            _vp, _vp, _vp, _sz, _vp]),
@@ -323,6 +337,12 @@ def coda_set_fold_rowreduce(enable: int) -> None:
 def coda_set_split_tail(enable: int) -> None:
     """1: the forward's CTA-pair GEMMs split their last tiles along K (default); 0: whole tiles."""
     _check(_lib.coda_set_split_tail(int(enable)), "coda_set_split_tail")
+
+
+def coda_set_col_plan(enable: int) -> None:
+    """1: the CTA-pair data gradients may use narrower column tiles that spread evenly over
+    the pairs; 0: 256-column tiles (default)."""
+    _check(_lib.coda_set_col_plan(int(enable)), "coda_set_col_plan")
 
 
 def coda_get_mma_mode() -> int:

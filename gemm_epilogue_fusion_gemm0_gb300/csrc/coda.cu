@@ -9,10 +9,14 @@
 // Backward data gradient (section "反向传播的 GEMM-Epilogue 结构"):
 //   launch 1  GEMM dy @ W1^T with EpiRmsNormBackward    -> grad_h (cooperative launch)
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -173,6 +177,31 @@ constexpr uint32_t kPairDgradGivenSSmem = pair_smem_bytes<EpiRmsNormBackwardGive
 }  // namespace coda
 
 // ---------------------------------------------------------------------------
+// Data gradient without any allocation: scratch in a static device array.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) at the
+// point where they run the backward: code inside a custom allocator or
+// memory-pool callback, runtimes that forbid allocation while a step is in
+// flight because it could synchronise the device or fragment a pre-sized
+// pool, and embedders whose device memory is fully reserved up front.  For
+// them this entry point takes only inputs and outputs; the partial row
+// statistics and completion flags that coda_bwd_dgrad keeps in the caller's
+// workspace live instead in the fixed array below, which every GPU that
+// loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocPartials = 2 * CODA_NOALLOC_MAX_PARTIALS;  // fp32, two per (row, column tile)
+constexpr size_t kNoAllocFlags = CODA_NOALLOC_MAX_TILES;        // u64 per output tile
+constexpr size_t kNoAllocFlagOffset = kNoAllocPartials * sizeof(float);
+constexpr size_t kNoAllocEpochOffset = kNoAllocFlagOffset + kNoAllocFlags * sizeof(uint64_t);
+constexpr size_t kNoAllocBytes = kNoAllocEpochOffset + 256;
+
+// 4 MiB of partials + 128 KiB of flags + a 256-byte slot with the launch
+// counter and its arrival word.  The flags need no clearing: each launch
+// publishes counter + 1 and its last block to finish advances the counter, so
+// values left by an earlier call never match (the array starts zeroed).
+static __device__ __align__(256) unsigned char g_noalloc_dgrad_scratch[kNoAllocBytes];
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 namespace {
@@ -188,6 +217,7 @@ struct DevState {
   coda_status_t status = CODA_OK;
   int sms = 0;
   int max_pairs = 0;  // co-resident clusters of two for the CTA-pair kernels
+  void* noalloc_scratch = nullptr;  // device address of g_noalloc_dgrad_scratch on this device
 };
 
 std::mutex g_mu;
@@ -209,7 +239,12 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
+// First use of the library on the current device (once per device, under a
+// lock): checks the device, sets the kernels' shared-memory limits (which loads
+// the library's device code on this device, the static scratch array of the
+// no-allocation entry point included) and looks up the device address of that
+// array, so that whichever entry point runs first on a device does both.
+coda_status_t device_setup(int* sms, int* max_pairs = nullptr, void** noalloc_scratch = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -293,6 +328,15 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
           ok = false;
         }
       }
+      if (ok) {
+        // In host code the array's name is only a host-side stand-in: its device
+        // address on this device comes from the runtime.
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_dgrad_scratch) == cudaSuccess && p != nullptr)
+          s.noalloc_scratch = p;
+        else
+          ok = false;
+      }
       if (!ok) {
         cudaGetLastError();
         s.status = CODA_ERR_LAUNCH;
@@ -302,6 +346,7 @@ coda_status_t device_setup(int* sms, int* max_pairs = nullptr) {
   }
   *sms = s.sms;
   if (max_pairs) *max_pairs = s.max_pairs;
+  if (noalloc_scratch) *noalloc_scratch = s.noalloc_scratch;
   return s.status;
 }
 
@@ -418,6 +463,7 @@ SkParams plan_split_tail(const SkRegion& reg, int64_t num_tiles, int npairs, int
   sk.part = reg.part;
   sk.flags = reg.flags;
   sk.epoch = reg.epoch;
+  sk.slots = static_cast<int>(reg.slots);
   return sk;
 }
 
@@ -504,7 +550,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   const SkParams sk1 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt1, np1, nkb);
   cudaError_t e =
       pair ? launch(kPairGemm0, 2 * np0, kThreads, kPairGemm0Smem, stream, sk0.epoch != nullptr,
-                    mA0, mB0, Mi, di, di, kPairGroupM, p0, sk0, tmo)
+                    mA0, mB0, Mi, di, di, kPairGroupM, p0, sk0, kNoColPlan, tmo)
            : launch(kGemm0, std::min(sms, mt * nt0), kThreads, kGemm0Smem, stream, false, mA0,
                     mB0, Mi, di, di, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
@@ -539,7 +585,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     ps.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     ps.a_out = reinterpret_cast<__nv_bfloat16*>(a_out);
     e = pair ? launch(kPairGemm1Swiglu, 2 * np1, kThreads, kPairGemm1SwigluSmem, stream,
-                      sk1.epoch != nullptr, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, sk1, tmo)
+                      sk1.epoch != nullptr, mA1, mB1, Mi, N1i, di, kPairGroupM, ps, sk1, kNoColPlan, tmo)
              : launch(kGemm1Swiglu, std::min(sms, mt * nt1), kThreads, kGemm1SwigluSmem,
                       stream, false, mA1, mB1, Mi, N1i, di, kGroupM, ps, tmo);
   } else {
@@ -548,7 +594,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
     p1.fold = fold;
     p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
     e = pair ? launch(kPairGemm1, 2 * np1, kThreads, kPairGemm1Smem, stream, sk1.epoch != nullptr,
-                      mA1, mB1, Mi, N1i, di, kPairGroupM, p1, sk1, tmo)
+                      mA1, mB1, Mi, N1i, di, kPairGroupM, p1, sk1, kNoColPlan, tmo)
              : launch(kGemm1, std::min(sms, mt * nt1), kThreads, kGemm1Smem, stream, false, mA1,
                       mB1, Mi, N1i, di, kGroupM, p1, tmo);
   }
@@ -558,6 +604,111 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   }
   after_launch(k_launch, stream);
   return CODA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Column plans for the CTA-pair data gradient (gemm_pair.cuh, ColPlan).
+// ---------------------------------------------------------------------------
+std::atomic<int> g_col_plan{0};  // 1: the data gradients may use narrower column tiles
+
+// Most column tiles per row block the data-gradient workspace is sized for.
+int64_t dgrad_max_col_tiles(int64_t d) { return 2 * cdiv(d, kBN); }
+
+// The data gradient's workspace: qpart [2 * max tiles][M] fp32, then flags
+// [slabs][max tiles] (a launch uses the first slabs * nt), then the 256-byte slot
+// of the launch counter.
+struct DgradWs {
+  float* qpart;
+  uint64_t* flags;
+  uint64_t* epoch;
+};
+
+size_t dgrad_ws_bytes(int64_t M, int64_t d) {
+  const int64_t slabs = 2 * cdiv(M, kPairBM), nt = dgrad_max_col_tiles(d);
+  return align256(static_cast<size_t>(2 * nt) * M * 4) +
+         align256(static_cast<size_t>(slabs) * nt * 8) + 256;
+}
+
+DgradWs dgrad_ws(void* base, int64_t M, int64_t d) {
+  char* p = static_cast<char*>(base);
+  DgradWs w;
+  w.qpart = reinterpret_cast<float*>(p);
+  w.flags = reinterpret_cast<uint64_t*>(
+      p + align256(static_cast<size_t>(2 * dgrad_max_col_tiles(d)) * M * 4));
+  w.epoch = reinterpret_cast<uint64_t*>(p + dgrad_ws_bytes(M, d) - 256);
+  return w;
+}
+
+// Largest per-pair load of a plan with tiles handed out round-robin in
+// row-major order, in units of one 256-column tile; `c` is the fixed cost of a
+// tile in the same unit.
+double plan_load(const ColPlan& cp, int mt, int npairs, double c, std::vector<double>& load) {
+  load.assign(npairs, 0.0);
+  int64_t t = 0;
+  for (int mb = 0; mb < mt; ++mb)
+    for (int j = 0; j < cp.nt; ++j, ++t) {
+      int n0, width;
+      cp.tile(mb, j, n0, width);
+      load[t % npairs] += width / 256.0 + c;
+    }
+  return *std::max_element(load.begin(), load.end());
+}
+
+struct PlanKey {
+  int64_t mt, d, K;
+  int npairs;
+  bool operator<(const PlanKey& o) const {
+    return std::tie(mt, d, K, npairs) < std::tie(o.mt, o.d, o.K, o.npairs);
+  }
+};
+std::mutex g_plan_mu;
+std::map<PlanKey, ColPlan> g_plan_cache;
+
+// The column plan for a data gradient of mt 256-row blocks, d output columns
+// and K = N1 on `npairs` CTA pairs: among 256-column tiles and every tiling
+// into nt tiles (ceil(d/256) <= nt <= 2 ceil(d/256), at most npairs, so that a
+// row block's tiles can all be in flight at once) of widths w and w + 16
+// (128 <= w, w + 16 <= 256), each with its best rotation, the one whose
+// largest per-pair load is smallest.  A tile's fixed cost (pipeline fill,
+// drain, epilogue not hidden) is taken as 2 us against a pair's 256-column
+// tile time 2 * 256 * 256 * K / (25 TFLOP/s); a plan must beat the 256-column
+// tiling by 0.5 % to be taken.  Memoised per shape and pair count.
+ColPlan plan_dgrad_cols(int64_t mt, int64_t d, int64_t K, int npairs) {
+  if (g_col_plan.load() == 0 || npairs < 2) return kNoColPlan;
+  const PlanKey key{mt, d, K, npairs};
+  {
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    auto it = g_plan_cache.find(key);
+    if (it != g_plan_cache.end()) return it->second;
+  }
+  const double c = 2e-6 / (2.0 * 256 * 256 * static_cast<double>(K) / 25e12);
+  std::vector<double> load;
+  const int nt0 = static_cast<int>(cdiv(d, kBN));
+  ColPlan uni = {nt0, kBN, 0, 0, 128};
+  const double base = plan_load(uni, static_cast<int>(mt), npairs, c, load);
+  ColPlan best = kNoColPlan;
+  double best_load = base * (1.0 - 0.005);
+  const int nt_hi = static_cast<int>(std::min<int64_t>(dgrad_max_col_tiles(d), npairs));
+  for (int nt = nt0; nt <= nt_hi; ++nt) {
+    int w = static_cast<int>(d / nt) / 16 * 16;
+    int nl = static_cast<int>(cdiv(d - static_cast<int64_t>(nt) * w, 16));
+    if (nl >= nt) {
+      w += 16;
+      nl = 0;
+    }
+    if (w < 128 || w + (nl > 0 ? 16 : 0) > kBN) continue;
+    for (int rot = 0; rot < (nl > 0 ? nt : 1); ++rot) {
+      const ColPlan cp = {nt, w, nl, rot, (w + (nl > 0 ? 16 : 0)) / 2};
+      const double l = plan_load(cp, static_cast<int>(mt), npairs, c, load);
+      if (l < best_load - 1e-9) {
+        best_load = l;
+        best = cp;
+      }
+    }
+  }
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plan_cache[key] = best;
+  return best;
 }
 
 }  // namespace
@@ -576,11 +727,10 @@ size_t coda_fwd_unfused_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
 
 size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
-  // one flag per (128-row slab, column tile); CTA-pair tiles cover 2 * ceil(M/256) slabs;
-  // then the launch epoch (8 bytes in a 256-byte slot)
-  const int64_t slabs = 2 * cdiv(M, kPairBM), nt = cdiv(d, kBN);
-  return align256(static_cast<size_t>(2 * nt) * M * 4) +
-         align256(static_cast<size_t>(slabs) * nt * 8) + 256;
+  // one flag per (128-row slab, column tile); CTA-pair tiles cover 2 * ceil(M/256) slabs
+  // and a column plan cuts a row block into at most twice ceil(d/256) tiles; then the
+  // launch counter's 256-byte slot
+  return dgrad_ws_bytes(M, d);
 }
 
 coda_status_t coda_fwd(const coda_bf16* x, const coda_bf16* W0, const coda_bf16* z,
@@ -630,30 +780,30 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
 
   // Row-major tile order; every column tile of a row block must be in flight
   // at once (at most one wave per row block), see EpiRmsNormBackward.
-  const int nt = static_cast<int>(cdiv(d, kBN));
   const int mt = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
+  const ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
+  const int nt = cp.nt > 0 ? cp.nt : static_cast<int>(cdiv(d, kBN));
   const int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
   if (nt > units) return CODA_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap mA, mB;
   bool ok = tmap_2d(&mA, dy, N1, M, kBK, kBM);                  // dy [M, N1] K-major (K = N1)
-  ok &= tmap_2d(&mB, W1, N1, d, kBK, pair ? 128 : kBN);         // W1 [d(N), N1(K)] K-major
+  ok &= tmap_2d(&mB, W1, N1, d, kBK, pair ? cp.b_rows : kBN);   // W1 [d(N), N1(K)] K-major
   if (!ok) return CODA_ERR_LAUNCH;
 
+  const DgradWs dw = dgrad_ws(workspace, M, d);
   EpiRmsNormBackward::Params p = {};
   p.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p.r = r;
   p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
-  p.qpart = reinterpret_cast<float*>(workspace);
-  p.flags = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
-                                        align256(static_cast<size_t>(2 * nt) * M * 4));
-  p.epoch = reinterpret_cast<uint64_t*>(static_cast<char*>(workspace) +
-                                        coda_bwd_dgrad_workspace_bytes(M, d, N1) - 256);
+  p.qpart = dw.qpart;
+  p.flags = dw.flags;
+  p.epoch = dw.epoch;
   cudaError_t e =
       pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p, kNoSplitTail,
-                    g_timeout_ns.load())
+                    cp, g_timeout_ns.load())
            : launch(kDgrad, units, kThreads, kDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                     g_timeout_ns.load());
@@ -721,7 +871,7 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   p0.inv_s_hg = 1.0f / s_hg;
   cudaError_t e = launch(kPairGemm0F8, 2 * std::min(max_pairs, mtp * nt0), kThreads,
                          kPairGemm0F8Smem, stream, false, mA0, mB0, Mi, di, di, kPairGroupM, p0, kNoSplitTail,
-                         tmo);
+                         kNoColPlan, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -739,7 +889,7 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   p1.y_out = reinterpret_cast<__nv_bfloat16*>(y_out);
   p1.scale = s_hg * sW1;
   e = launch(kPairGemm1F8, 2 * std::min(max_pairs, mtp * nt1), kThreads, kPairGemm1F8Smem, stream,
-             false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, kNoSplitTail, tmo);
+             false, mA1, mB1, Mi, N1i, di, kPairGroupM, p1, kNoSplitTail, kNoColPlan, tmo);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return CODA_ERR_LAUNCH;
@@ -787,16 +937,17 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const uint64_t tmo = g_timeout_ns.load();
   const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
 
-  const int nt = static_cast<int>(cdiv(d, kBN));
+  const int nt = static_cast<int>(cdiv(d, kBN));  // 256-column tiles of the GEMMs with N = d
   const int mt = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
-  const int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
-  if (nt > units) return CODA_ERR_UNSUPPORTED_SHAPE;
+  // launch 1 (the data gradient) may cut its row blocks into a column plan's tiles
+  const ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
+  const int nt1 = cp.nt > 0 ? cp.nt : nt;
+  const int units = pair ? std::min(max_pairs, mt * nt1) : std::min(sms, mt * nt1);
+  if (nt1 > units) return CODA_ERR_UNSUPPORTED_SHAPE;
   const int slabs = pair ? 2 * mt : mt;
 
   char* ws = static_cast<char*>(workspace);
-  float* qpart = reinterpret_cast<float*>(ws);
-  uint64_t* flags =
-      reinterpret_cast<uint64_t*>(ws + align256(static_cast<size_t>(2 * nt) * M * 4));
+  const DgradWs dw = dgrad_ws(ws, M, d);
   char* rest = ws + coda_bwd_dgrad_workspace_bytes(M, d, N1);
   __nv_bfloat16* h2 = reinterpret_cast<__nv_bfloat16*>(rest);
   float* gpart = reinterpret_cast<float*>(rest + align256(static_cast<size_t>(M) * d * 2));
@@ -809,7 +960,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const uint32_t bbox = pair ? 128 : kBN;
   CUtensorMap mDy, mW1, mH2, mDyMN, mDh, mW0, mX, mDhMN;
   bool ok = tmap_2d(&mDy, dy, N1, M, kBK, kBM);     // dy [M, N1] K-major (dgrad)
-  ok &= tmap_2d(&mW1, W1, N1, d, kBK, bbox);        // W1 [d(N), N1(K)] K-major
+  ok &= tmap_2d(&mW1, W1, N1, d, kBK, pair ? cp.b_rows : kBN);  // W1 [d(N), N1(K)] K-major
   ok &= tmap_2d(&mH2, h2, d, M, 64, kBK);           // h2^T: [M(K), d(M)] MN-major A
   ok &= tmap_2d(&mDyMN, dy, N1, M, 64, kBK);        // dy: [M(K), N1(N)] MN-major B
   ok &= tmap_2d(&mDh, dh_out, d, M, kBK, kBM);      // dh [M, d] K-major A
@@ -824,14 +975,14 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p.r = r;
   p.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
-  p.qpart = qpart;
-  p.flags = flags;
-  p.epoch = reinterpret_cast<uint64_t*>(ws + coda_bwd_dgrad_workspace_bytes(M, d, N1) - 256);
+  p.qpart = dw.qpart;
+  p.flags = dw.flags;
+  p.epoch = dw.epoch;
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
   cudaError_t e = pair ? launch(kPairDgradFull, 2 * units, kThreads, kPairDgradFullSmem, stream,
-                                true, mDy, mW1, Mi, di, N1i, 1, p, kNoSplitTail, tmo)
+                                true, mDy, mW1, Mi, di, N1i, 1, p, kNoSplitTail, cp, tmo)
                        : launch(kDgradFull, units, kThreads, kDgradFullSmem, stream, true, mDy, mW1,
                                 Mi, di, N1i, 1, p, tmo);
   if (e != cudaSuccess) {
@@ -856,7 +1007,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const int npw1 = std::min(max_pairs, mtw * ntw1);
   const SkParams skw1 = plan_split_tail(skr, static_cast<int64_t>(mtw) * ntw1, npw1, nkw);
   e = pair ? launch(kPairWgrad, 2 * npw1, kThreads, kPairWgradSmem, stream, skw1.epoch != nullptr,
-                    mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, skw1, tmo)
+                    mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, skw1, kNoColPlan, tmo)
            : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kWgradSmem, stream, false, mH2,
                     mDyMN, di, N1i, Mi, kGroupM, pw1, tmo);
   if (e != cudaSuccess) {
@@ -872,7 +1023,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const int npx = std::min(max_pairs, mtx * nt);
   const SkParams skx = plan_split_tail(skr, static_cast<int64_t>(mtx) * nt, npx, cdiv(d, kBK));
   e = pair ? launch(kPairXgrad, 2 * npx, kThreads, kPairXgradSmem, stream, skx.epoch != nullptr,
-                    mDh, mW0, Mi, di, di, kPairGroupM, px, skx, tmo)
+                    mDh, mW0, Mi, di, di, kPairGroupM, px, skx, kNoColPlan, tmo)
            : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kXgradSmem, stream, false, mDh,
                     mW0, Mi, di, di, kGroupM, px, tmo);
   if (e != cudaSuccess) {
@@ -886,7 +1037,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const int npw0 = std::min(max_pairs, mtw * nt);
   const SkParams skw0 = plan_split_tail(skr, static_cast<int64_t>(mtw) * nt, npw0, nkw);
   e = pair ? launch(kPairWgrad, 2 * npw0, kThreads, kPairWgradSmem, stream, skw0.epoch != nullptr,
-                    mX, mDhMN, di, di, Mi, kPairGroupM, pw0, skw0, tmo)
+                    mX, mDhMN, di, di, Mi, kPairGroupM, pw0, skw0, kNoColPlan, tmo)
            : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kWgradSmem, stream, false, mX,
                     mDhMN, di, di, Mi, kGroupM, pw0, tmo);
   if (e != cudaSuccess) {
@@ -953,7 +1104,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   cudaError_t e =
       pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads,
                     kPairSwigluBwdSmem, stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM,
-                    p0, kNoSplitTail, tmo)
+                    p0, kNoSplitTail, kNoColPlan, tmo)
            : launch(kSwigluBwd, std::min(sms, mt * nts), kThreads, kSwigluBwdSmem, stream, false,
                     mA0, mB0, Mi, halfi, Douti, kGroupM, p0, tmo);
   if (e != cudaSuccess) {
@@ -978,7 +1129,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   p1.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
   e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads,
                     kPairDgradGivenSSmem, stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, kNoSplitTail,
-                    tmo)
+                    kNoColPlan, tmo)
            : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kDgradGivenSSmem, stream,
                     false, mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
   if (e != cudaSuccess) {
@@ -1013,7 +1164,8 @@ coda_status_t coda_get_device_status(cudaStream_t stream, uint32_t* detail) {
     }
   }
   if (detail) *detail = v;
-  return v ? CODA_ERR_DEVICE_TIMEOUT : CODA_OK;
+  if (v == 0) return CODA_OK;
+  return (v & 0x200u) ? CODA_ERR_DEVICE_BOUNDS : CODA_ERR_DEVICE_TIMEOUT;
 }
 
 void coda_set_launch_events(cudaEvent_t* events, int n) {
@@ -1032,6 +1184,12 @@ int coda_get_mma_mode(void) { return g_mma_mode.load(); }
 coda_status_t coda_set_split_tail(int enable) {
   if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
   g_split_tail.store(enable);
+  return CODA_OK;
+}
+
+coda_status_t coda_set_col_plan(int enable) {
+  if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
+  g_col_plan.store(enable);
   return CODA_OK;
 }
 
@@ -1054,6 +1212,7 @@ const char* coda_status_string(coda_status_t s) {
     case CODA_ERR_DEVICE_TIMEOUT: return "CODA_ERR_DEVICE_TIMEOUT";
     case CODA_ERR_NO_DEVICE: return "CODA_ERR_NO_DEVICE";
     case CODA_ERR_UNSUPPORTED_DEVICE: return "CODA_ERR_UNSUPPORTED_DEVICE";
+    case CODA_ERR_DEVICE_BOUNDS: return "CODA_ERR_DEVICE_BOUNDS";
   }
   return "CODA_ERR_UNKNOWN";
 }
@@ -1072,58 +1231,6 @@ coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t stream) {
 
 }  // extern "C"
 
-// ---------------------------------------------------------------------------
-// Data gradient without any allocation: scratch in a static device array.
-//
-// Some callers cannot call cudaMalloc (or any allocating routine) at the
-// point where they run the backward: code inside a custom allocator or
-// memory-pool callback, runtimes that forbid allocation while a step is in
-// flight because it could synchronise the device or fragment a pre-sized
-// pool, and embedders whose device memory is fully reserved up front.  For
-// them this entry point takes only inputs and outputs; the partial row
-// statistics and completion flags that coda_bwd_dgrad keeps in the caller's
-// workspace live instead in the fixed array below, which every GPU that
-// loads this library holds until the process exits.
-// ---------------------------------------------------------------------------
-constexpr size_t kNoAllocPartials = 2 * CODA_NOALLOC_MAX_PARTIALS;  // fp32, two per (row, column tile)
-constexpr size_t kNoAllocFlags = CODA_NOALLOC_MAX_TILES;        // u64 per output tile
-constexpr size_t kNoAllocFlagOffset = kNoAllocPartials * sizeof(float);
-constexpr size_t kNoAllocEpochOffset = kNoAllocFlagOffset + kNoAllocFlags * sizeof(uint64_t);
-constexpr size_t kNoAllocBytes = kNoAllocEpochOffset + 256;
-
-// 4 MiB of partials + 128 KiB of flags + the launch epoch.  The flags need no
-// clearing: each launch publishes epoch + 1 and then advances the epoch, so
-// values left by an earlier call never match (the array starts zeroed).
-static __device__ __align__(256) unsigned char g_noalloc_dgrad_scratch[kNoAllocBytes];
-
-namespace {
-
-std::mutex g_noalloc_mu;
-void* g_noalloc_scratch_addr[kMaxDevices] = {};
-
-// Device address of the static array on the current device, looked up once per
-// device (the name itself is only a host-side stand-in in host code).
-coda_status_t noalloc_scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    return CODA_ERR_NO_DEVICE;
-  }
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_dgrad_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return CODA_ERR_LAUNCH;
-    }
-    g_noalloc_scratch_addr[dev] = p;
-  }
-  *out = g_noalloc_scratch_addr[dev];
-  return CODA_OK;
-}
-
-}  // namespace
-
 extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_bf16* W1,
                                                 const coda_bf16* h, const float* r,
                                                 const coda_bf16* gamma, int64_t M, int64_t d,
@@ -1141,10 +1248,8 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
       static_cast<uint64_t>(mt64) * static_cast<uint64_t>(nt64) > kNoAllocFlags)
     return CODA_ERR_UNSUPPORTED_SHAPE;  // larger than the static scratch
   int sms = 0;
-  st = device_setup(&sms);
-  if (st != CODA_OK) return st;
   void* scratch = nullptr;
-  st = noalloc_scratch_address(&scratch);
+  st = device_setup(&sms, nullptr, &scratch);
   if (st != CODA_OK) return st;
 
   const int mt = static_cast<int>(mt64);

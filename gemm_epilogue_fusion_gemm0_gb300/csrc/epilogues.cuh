@@ -20,7 +20,6 @@
 // (per-tile sums of squares / of grad_h2 * gamma * h).
 #pragma once
 
-#include <cooperative_groups.h>
 #include <cuda_fp8.h>
 
 #include "gemm.cuh"
@@ -37,7 +36,7 @@ struct Chunk8 {
 struct EpiDefaultCols {
   static __host__ __device__ __forceinline__ int num_col_tiles(int N) { return (N + kBN - 1) / kBN; }
   static __device__ __forceinline__ int b_col(int nb, int j, int /*N*/) { return nb * kBN + 64 * j; }
-  // run by every thread of the grid after the block's last tile (nothing by default)
+  // run by one thread of each block once all the block's threads are done (nothing by default)
   template <class P>
   static __device__ __forceinline__ void at_exit(const P&) {}
 };
@@ -135,7 +134,7 @@ struct Stage {
   // (staged row i at src + i * pitch bytes) into registers.  Issued a chunk
   // ahead, its latency overlaps the work on the current chunk.
   static __device__ __forceinline__ void fetch(uint4 (&v)[kGroups], const void* src, size_t pitch,
-                                               int rows, int valid) {
+                                               int rows, int valid, const Span& sp = Span{}) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t g = lane % kGroups;
     const char* s = static_cast<const char*>(src);
@@ -143,7 +142,8 @@ struct Stage {
     for (uint32_t i = 0; i < kGroups; ++i) {
       const uint32_t r = i * kRowsPerPass + lane / kGroups;
       v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid)
+      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid &&
+          checked(in_span(sp, s + r * pitch + 16u * g, 16), kChkLoad))
         v[i] = __ldg(reinterpret_cast<const uint4*>(s + r * pitch + 16u * g));
     }
   }
@@ -161,7 +161,7 @@ struct Stage {
 
   // global block -> staging buffer (fetch, then deposit)
   static __device__ __forceinline__ void load(uint32_t buf, const void* src, size_t pitch,
-                                              int rows, int valid) {
+                                              int rows, int valid, const Span& sp = Span{}) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t g = lane % kGroups;
     const char* s = static_cast<const char*>(src);
@@ -170,7 +170,8 @@ struct Stage {
     for (uint32_t i = 0; i < kGroups; ++i) {
       const uint32_t r = i * kRowsPerPass + lane / kGroups;
       v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid)
+      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid &&
+          checked(in_span(sp, s + r * pitch + 16u * g, 16), kChkLoad))
         v[i] = __ldg(reinterpret_cast<const uint4*>(s + r * pitch + 16u * g));
     }
 #pragma unroll
@@ -182,7 +183,7 @@ struct Stage {
 
   // staging buffer -> global block (staged row i at dst + i * pitch bytes)
   static __device__ __forceinline__ void flush(uint32_t buf, void* dst, size_t pitch, int rows,
-                                               int valid) {
+                                               int valid, const Span& sp = Span{}) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t g = lane % kGroups;
     char* d = static_cast<char*>(dst);
@@ -190,7 +191,8 @@ struct Stage {
     for (uint32_t i = 0; i < kGroups; ++i) {
       const uint32_t r = i * kRowsPerPass + lane / kGroups;
       const uint4 v = ld_shared_v4(at(buf, r, g));
-      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid)
+      if (static_cast<int>(r) < rows && static_cast<int>(16u * g) < valid &&
+          checked(in_span(sp, d + r * pitch + 16u * g, 16), kChkStore))
         *reinterpret_cast<uint4*>(d + r * pitch + 16u * g) = v;
     }
   }
@@ -212,6 +214,19 @@ struct WarpRows {
 // Bytes of the 32 columns starting at n0 that lie below column `limit`.
 __device__ __forceinline__ int valid_bytes(int n0, int limit, int esize) {
   return max(0, min(32, limit - n0)) * esize;
+}
+
+// Zeroes the accumulator values of the 32-column chunk starting at output
+// column n0 that lie at or past `nend`.  A tile narrower than 256 columns is
+// computed by an MMA of that width, which leaves the rest of its TMEM
+// accumulator untouched (stale), so every reduction over a chunk masks it.
+// Warp-uniform: n0 and nend are the same for the whole warp.
+__device__ __forceinline__ void mask_chunk(uint32_t (&v)[32], int n0, int nend) {
+  if (n0 + 32 > nend) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (n0 + i >= nend) v[i] = 0u;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -242,28 +257,29 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
     const size_t pitch = static_cast<size_t>(c.N) * 2;
     const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
-    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    const int nbase = c.n0 + c.half * kHalfCols;
     const size_t rbase = static_cast<size_t>(wr.row0) * c.N;
     uint4 zf[Stage64::kGroups];  // the next chunk's z block, in flight during this chunk
-    Stage64::fetch(zf, p.z + rbase + nbase, pitch, wr.rows, valid_bytes(nbase, c.N, 2));
+    Stage64::fetch(zf, p.z + rbase + nbase, pitch, wr.rows, valid_bytes(nbase, c.nend, 2), span(p.z, c.M, pitch));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
-      const int valid = valid_bytes(n0, c.N, 2);
+      const int n0 = c.n0 + col;
+      const int valid = valid_bytes(n0, c.nend, 2);
       const size_t off = rbase + n0;
       Stage64::deposit(buf0, zf);
       if (ch + 1 < kHalfChunks)
-        Stage64::fetch(zf, p.z + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.N, 2));
+        Stage64::fetch(zf, p.z + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.nend, 2), span(p.z, c.M, pitch));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
+      mask_chunk(v, n0, c.nend);
       __syncwarp();
       uint32_t zr[16], hw[16], hgw[16];
       Stage64::get(buf0, zr);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zr[4 * g + e]);
@@ -277,11 +293,13 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
       Stage64::put(buf0, hw);
       if (fused) Stage64::put(buf1, hgw);
       __syncwarp();
-      Stage64::flush(buf0, p.h_out + off, pitch, wr.rows, valid);
-      if (fused) Stage64::flush(buf1, p.hg_out + off, pitch, wr.rows, valid);
+      Stage64::flush(buf0, p.h_out + off, pitch, wr.rows, valid, span(p.h_out, c.M, pitch));
+      if (fused) Stage64::flush(buf1, p.hg_out + off, pitch, wr.rows, valid, span(p.hg_out, c.M, pitch));
       __syncwarp();
     }
-    if (m < c.M && p.part != nullptr) p.part[partial_index(c, m)] = ss;
+    if (m < c.M && p.part != nullptr &&
+        checked(partial_index(c, m) < static_cast<size_t>(2 * c.nt) * c.M, kChkPartial))
+      p.part[partial_index(c, m)] = ss;
   }
 };
 
@@ -301,14 +319,14 @@ struct EpiStoreF32 : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
+      const int n0 = c.n0 + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
       Stage128::put(c.stage, v);
       __syncwarp();
       Stage128::flush(c.stage, p.out + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
-                      valid_bytes(n0, c.N, 4));
+                      valid_bytes(n0, c.nend, 4), span(p.out, c.M, pitch));
       __syncwarp();
     }
   }
@@ -343,7 +361,7 @@ struct EpiRowScale : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
+      const int n0 = c.n0 + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
@@ -354,7 +372,7 @@ struct EpiRowScale : EpiDefaultCols {
       Stage64::put(c.stage, yw);
       __syncwarp();
       Stage64::flush(c.stage, p.y_out + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
-                     valid_bytes(n0, c.N, 2));
+                     valid_bytes(n0, c.nend, 2), span(p.y_out, c.M, pitch));
       __syncwarp();
     }
   }
@@ -373,10 +391,10 @@ struct EpiRowScale : EpiDefaultCols {
 // row-major order with at most gridDim.x column tiles per row; then every wait
 // depends only on tiles with smaller index and cannot deadlock.
 // The token is epoch + 1, epoch being a counter in the caller's workspace that
-// the launch reads and, once every block is done (a grid-wide barrier: the
-// launch is cooperative), advances by one.  Flags left by an earlier launch hold
-// an older token, so the workspace never needs clearing, and a launch replayed
-// from a CUDA graph draws a fresh token each time.
+// the launch reads and that the last of its blocks to finish advances by one
+// (launch_exit).  Flags left by an earlier launch hold an older token, so the
+// workspace never needs clearing, and a launch replayed from a CUDA graph draws
+// a fresh token each time.
 // ---------------------------------------------------------------------------
 // kExtras: the full backward's additions (dh_res, h2, dgamma partials) are
 // compiled in; the plain data gradient leaves them out and keeps fewer registers.
@@ -399,12 +417,9 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
     float* gpart;                 // [4 * slabs][d] per-warp column partials of dgamma
   };
 
-  // Every block has finished its tiles once the grid barrier is passed, so no
-  // flag of this launch is read any more: advance the epoch.
-  static __device__ __forceinline__ void at_exit(const Params& p) {
-    cooperative_groups::this_grid().sync();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.epoch = *p.epoch + 1;
-  }
+  // This block reads no flag any more: count it out of the launch; the last
+  // block to finish advances the epoch.
+  static __device__ __forceinline__ void at_exit(const Params& p) { launch_exit(p.epoch); }
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
                                                const TileCtx& c) {
@@ -418,34 +433,35 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
     // Without the extras there are registers to spare: the next chunk's h block
     // is fetched while the current one is processed (the last fetch of pass 1
     // brings pass 2's first block).
-    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    const int nbase = c.n0 + c.half * kHalfCols;
     uint4 hf[Stage64::kGroups];
     if constexpr (!kExtras)
       Stage64::fetch(hf, p.h + static_cast<size_t>(wr.row0) * c.N + nbase, pitch, wr.rows,
-                     valid_bytes(nbase, c.N, 2));
+                     valid_bytes(nbase, c.nend, 2), span(p.h, c.M, pitch));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
+      const int n0 = c.n0 + col;
       if constexpr (!kExtras) {
         Stage64::deposit(buf0, hf);
         const int nn = ch + 1 < kHalfChunks ? n0 + 32 : nbase;
         Stage64::fetch(hf, p.h + static_cast<size_t>(wr.row0) * c.N + nn, pitch, wr.rows,
-                       valid_bytes(nn, c.N, 2));
+                       valid_bytes(nn, c.nend, 2), span(p.h, c.M, pitch));
       } else {
         Stage64::load(buf0, p.h + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
-                      valid_bytes(n0, c.N, 2));
+                      valid_bytes(n0, c.nend, 2), span(p.h, c.M, pitch));
       }
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
+      mask_chunk(v, n0, c.nend);
       __syncwarp();
       uint32_t hr[16];
       Stage64::get(buf0, hr);
       __syncwarp();  // every lane has its row before the buffer is refilled
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           qp = fmaf(__uint_as_float(v[g * 8 + 2 * e]) * bf16lo(gg.w[e]), bf16lo(hr[4 * g + e]), qp);
@@ -454,12 +470,15 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
         }
       }
     }
-    if (row_ok) p.qpart[partial_index(c, m)] = qp;
+    if (row_ok && checked(partial_index(c, m) < static_cast<size_t>(2 * c.nt) * c.M, kChkPartial))
+      p.qpart[partial_index(c, m)] = qp;
 
     // Publish this tile's partials, then wait for the whole row block.
     named_bar_sync(1, kEpiThreads);
     uint64_t* row_flags = p.flags + static_cast<size_t>(c.mb) * c.nt;
-    if (threadIdx.x == kEpiFirstThread) {
+    // 128-row slabs the flags cover: two per 256-row block (CTA-pair tiles)
+    const bool flags_ok = checked(c.mb < 2 * ((c.M + 255) / 256) && c.nb < c.nt, kChkFlag);
+    if (threadIdx.x == kEpiFirstThread && flags_ok) {
       const uint64_t token = *reinterpret_cast<volatile uint64_t*>(p.epoch) + 1;
       __threadfence();
       st_release_gpu_u64(row_flags + c.nb, token);
@@ -481,20 +500,21 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
-      const int valid = valid_bytes(n0, c.N, 2);
+      const int n0 = c.n0 + col;
+      const int valid = valid_bytes(n0, c.nend, 2);
       const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
       if constexpr (!kExtras) {
         Stage64::deposit(buf0, hf);
         if (ch + 1 < kHalfChunks)
-          Stage64::fetch(hf, p.h + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.N, 2));
+          Stage64::fetch(hf, p.h + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.nend, 2), span(p.h, c.M, pitch));
       } else {
-        Stage64::load(buf0, p.h + off, pitch, wr.rows, valid);
-        if (res) Stage64::load(buf1, p.dh_res + off, pitch, wr.rows, valid);
+        Stage64::load(buf0, p.h + off, pitch, wr.rows, valid, span(p.h, c.M, pitch));
+        if (res) Stage64::load(buf1, p.dh_res + off, pitch, wr.rows, valid, span(p.dh_res, c.M, pitch));
       }
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
+      mask_chunk(v, n0, c.nend);
       __syncwarp();
       uint32_t hr[16], rs[16], dw[16], h2w[16];
       Stage64::get(buf0, hr);
@@ -504,7 +524,7 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
       float t[32];  // r * h * grad_h2: this row's contribution to dgamma (kExtras)
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float a0 = __uint_as_float(v[g * 8 + 2 * e]);
@@ -526,8 +546,8 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
       Stage64::put(buf0, dw);
       if (kExtras && p.h2_out != nullptr) Stage64::put(buf1, h2w);
       __syncwarp();
-      Stage64::flush(buf0, p.dh_out + off, pitch, wr.rows, valid);
-      if (kExtras && p.h2_out != nullptr) Stage64::flush(buf1, p.h2_out + off, pitch, wr.rows, valid);
+      Stage64::flush(buf0, p.dh_out + off, pitch, wr.rows, valid, span(p.dh_out, c.M, pitch));
+      if (kExtras && p.h2_out != nullptr) Stage64::flush(buf1, p.h2_out + off, pitch, wr.rows, valid, span(p.h2_out, c.M, pitch));
       __syncwarp();
       if (kExtras && p.gpart != nullptr) {
         // Column sums over the warp's 32 rows: butterfly reduction; lane k ends
@@ -544,7 +564,9 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
           }
         }
         const int slab_warp = c.mb * 4 + (c.row >> 5);
-        if (n0 + lane < c.N) p.gpart[static_cast<size_t>(slab_warp) * c.N + n0 + lane] = t[0];
+        if (n0 + lane < c.nend &&
+            checked(slab_warp < 8 * ((c.M + 255) / 256), kChkColPartial))
+          p.gpart[static_cast<size_t>(slab_warp) * c.N + n0 + lane] = t[0];
       }
     }
   }
@@ -625,13 +647,13 @@ struct EpiRowScaleSwiGLU {
       if (p.y_out != nullptr) Stage64::put(buf1, gw);
       __syncwarp();
       Stage64::flush(buf0, p.a_out + static_cast<size_t>(wr.row0) * half + o0, a_pitch, wr.rows,
-                     valid);
-      if (p.y_out != nullptr) Stage64::flush(buf1, p.y_out + y_off, y_pitch, wr.rows, valid);
+                     valid, span(p.a_out, c.M, a_pitch));
+      if (p.y_out != nullptr) Stage64::flush(buf1, p.y_out + y_off, y_pitch, wr.rows, valid, span(p.y_out, c.M, y_pitch));
       __syncwarp();
       if (p.y_out != nullptr) {
         Stage64::put(buf0, uw);
         __syncwarp();
-        Stage64::flush(buf0, p.y_out + y_off + half, y_pitch, wr.rows, valid);
+        Stage64::flush(buf0, p.y_out + y_off + half, y_pitch, wr.rows, valid, span(p.y_out, c.M, y_pitch));
         __syncwarp();
       }
     }
@@ -667,14 +689,15 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int j0 = c.nb * kBN + col;
-      const int valid = valid_bytes(j0, half, 2);
+      const int j0 = c.n0 + col;
+      const int valid = valid_bytes(j0, c.nend, 2);
       const size_t off = static_cast<size_t>(wr.row0) * (2 * static_cast<size_t>(half)) + j0;
-      Stage64::load(buf0, p.y + off, pitch, wr.rows, valid);
-      Stage64::load(buf1, p.y + off + half, pitch, wr.rows, valid);
+      Stage64::load(buf0, p.y + off, pitch, wr.rows, valid, span(p.y, c.M, pitch));
+      Stage64::load(buf1, p.y + off + half, pitch, wr.rows, valid, span(p.y, c.M, pitch));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
+      mask_chunk(v, j0, c.nend);
       __syncwarp();
       uint32_t gr[16], ur[16], dgw[16], duw[16];
       Stage64::get(buf0, gr);
@@ -699,11 +722,12 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
       Stage64::put(buf0, dgw);
       Stage64::put(buf1, duw);
       __syncwarp();
-      Stage64::flush(buf0, p.dy_out + off, pitch, wr.rows, valid);
-      Stage64::flush(buf1, p.dy_out + off + half, pitch, wr.rows, valid);
+      Stage64::flush(buf0, p.dy_out + off, pitch, wr.rows, valid, span(p.dy_out, c.M, pitch));
+      Stage64::flush(buf1, p.dy_out + off + half, pitch, wr.rows, valid, span(p.dy_out, c.M, pitch));
       __syncwarp();
     }
-    if (m < c.M) p.spart[partial_index(c, m)] = ss;
+    if (m < c.M && checked(partial_index(c, m) < static_cast<size_t>(2 * c.nt) * c.M, kChkPartial))
+      p.spart[partial_index(c, m)] = ss;
   }
 };
 
@@ -733,10 +757,10 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
-      const int valid = valid_bytes(n0, c.N, 2);
+      const int n0 = c.n0 + col;
+      const int valid = valid_bytes(n0, c.nend, 2);
       const size_t off = static_cast<size_t>(wr.row0) * c.N + n0;
-      Stage64::load(c.stage, p.h + off, pitch, wr.rows, valid);
+      Stage64::load(c.stage, p.h + off, pitch, wr.rows, valid, span(p.h, c.M, pitch));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
@@ -745,7 +769,7 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
       Stage64::get(c.stage, hr);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
@@ -757,7 +781,7 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
       }
       Stage64::put(c.stage, dw);
       __syncwarp();
-      Stage64::flush(c.stage, p.dh_out + off, pitch, wr.rows, valid);
+      Stage64::flush(c.stage, p.dh_out + off, pitch, wr.rows, valid, span(p.dh_out, c.M, pitch));
       __syncwarp();
     }
   }
@@ -794,28 +818,29 @@ struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
     const size_t pitch = static_cast<size_t>(c.N) * 2;
     const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
-    const int nbase = c.nb * kBN + c.half * kHalfCols;
+    const int nbase = c.n0 + c.half * kHalfCols;
     const size_t rbase = static_cast<size_t>(wr.row0) * c.N;
     uint4 zf[Stage64::kGroups];  // the next chunk's z block, in flight during this chunk
-    Stage64::fetch(zf, p.z + rbase + nbase, pitch, wr.rows, valid_bytes(nbase, c.N, 2));
+    Stage64::fetch(zf, p.z + rbase + nbase, pitch, wr.rows, valid_bytes(nbase, c.nend, 2), span(p.z, c.M, pitch));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
-      const int valid = valid_bytes(n0, c.N, 2);
+      const int n0 = c.n0 + col;
+      const int valid = valid_bytes(n0, c.nend, 2);
       const size_t off = rbase + n0;
       Stage64::deposit(buf0, zf);
       if (ch + 1 < kHalfChunks)
-        Stage64::fetch(zf, p.z + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.N, 2));
+        Stage64::fetch(zf, p.z + off + 32, pitch, wr.rows, valid_bytes(n0 + 32, c.nend, 2), span(p.z, c.M, pitch));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
+      mask_chunk(v, n0, c.nend);
       __syncwarp();
       uint32_t zr[16], hw[16], qw[8];
       Stage64::get(buf0, zr);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.N);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
         float q[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -834,11 +859,12 @@ struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
       Stage64::put(buf0, hw);
       Stage32::put(buf1, qw);
       __syncwarp();
-      Stage64::flush(buf0, p.h_out + off, pitch, wr.rows, valid);
-      Stage32::flush(buf1, p.hq_out + off, static_cast<size_t>(c.N), wr.rows, valid / 2);
+      Stage64::flush(buf0, p.h_out + off, pitch, wr.rows, valid, span(p.h_out, c.M, pitch));
+      Stage32::flush(buf1, p.hq_out + off, static_cast<size_t>(c.N), wr.rows, valid / 2, span(p.hq_out, c.M, c.N));
       __syncwarp();
     }
-    if (m < c.M) p.part[partial_index(c, m)] = ss;
+    if (m < c.M && checked(partial_index(c, m) < static_cast<size_t>(2 * c.nt) * c.M, kChkPartial))
+      p.part[partial_index(c, m)] = ss;
   }
 };
 
@@ -859,7 +885,7 @@ struct EpiRowScaleFp8 : EpiDefaultCols {
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
-      const int n0 = c.nb * kBN + col;
+      const int n0 = c.n0 + col;
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
@@ -870,7 +896,7 @@ struct EpiRowScaleFp8 : EpiDefaultCols {
       Stage64::put(c.stage, yw);
       __syncwarp();
       Stage64::flush(c.stage, p.y_out + static_cast<size_t>(wr.row0) * c.N + n0, pitch, wr.rows,
-                     valid_bytes(n0, c.N, 2));
+                     valid_bytes(n0, c.nend, 2), span(p.y_out, c.M, pitch));
       __syncwarp();
     }
   }

@@ -30,6 +30,65 @@ namespace coda {
 
 __device__ uint32_t g_coda_status = 0;  // device status word (see WaitSite)
 
+// ---------------------------------------------------------------------------
+// Checked build (compiled with -DCODA_CHECKED, libcoda_checked.so): every
+// global access of the epilogues is checked against the extent of the tensor
+// it belongs to, every TMA box start against its tensor map's extent and the
+// 16-byte alignment of its innermost coordinate, and every index into the
+// workspace (partial sums, completion flags, split-tail slots) against the
+// size the host gave it.  A failed check records 0x200 | site in the status
+// word (first failure wins; coda_get_device_status reports
+// CODA_ERR_DEVICE_BOUNDS) and skips the access; a failed TMA check also makes
+// the producer leave its role like a wait that ran out.  Nothing traps.  In the
+// normal build every check compiles to nothing.
+// ---------------------------------------------------------------------------
+#ifdef CODA_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+enum CheckSite : uint32_t {
+  kChkTmaA = 1,        // A operand box start
+  kChkTmaB = 2,        // B operand box start
+  kChkLoad = 3,        // epilogue operand load (z, h, dh_res, saved y)
+  kChkStore = 4,       // epilogue output store
+  kChkPartial = 5,     // per-tile partial sum (sum of squares, q, s)
+  kChkFlag = 6,        // row-block completion flag
+  kChkSplitSlot = 7,   // split-tail partial slot or its flag
+  kChkColPartial = 8,  // column partial of dgamma
+};
+
+__device__ __forceinline__ bool checked(bool ok, uint32_t site) {
+  if (!kChecked || ok) return true;
+  atomicCAS(&g_coda_status, 0u, 0x200u | site);
+  return false;
+}
+
+// The bytes of one tensor, for the checked build's address checks (an empty
+// span checks nothing).
+struct Span {
+  const char* base;
+  size_t bytes;
+};
+
+__device__ __forceinline__ Span span(const void* base, int rows, size_t row_bytes) {
+  return Span{static_cast<const char*>(base), static_cast<size_t>(rows) * row_bytes};
+}
+
+// [p, p + n) lies inside the span
+__device__ __forceinline__ bool in_span(const Span& s, const void* p, size_t n) {
+  const char* c = static_cast<const char*>(p);
+  return s.base == nullptr || (c >= s.base && c + n <= s.base + s.bytes);
+}
+
+// A TMA box start: the innermost coordinate x (elements of `esize` bytes) on a
+// 16-byte boundary, both coordinates non-negative and less than one tile (256)
+// past their extent (a load may start past the edge; it reads the fill value).
+__device__ __forceinline__ bool tma_start_ok(int x, int y, int x_ext, int y_ext, int esize) {
+  return x >= 0 && y >= 0 && (x * esize) % 16 == 0 && x < x_ext + 256 && y < y_ext + 256;
+}
+
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
@@ -89,11 +148,12 @@ struct TileMap {
 // Epilogue context handed to the policy for one output tile.
 struct TileCtx {
   uint32_t taddr;  // TMEM address of this thread's lane, column 0 of the tile
-  int mb, nb;      // tile coordinates
+  int mb, nb;      // tile coordinates (nb: column tile index inside the row block)
+  int n0, nend;    // the tile's output columns are [n0, nend); nend <= n0 + 256 and <= N
   int row;         // row inside the tile (0..127) owned by this thread
   int half;        // which 128-column half of the tile this thread drains (0, 1)
   int M, N;        // problem size (N = output columns)
-  int nt;          // number of column tiles
+  int nt;          // number of column tiles per row block
   uint32_t stage;  // this warp's store-staging buffer (shared address), if the policy has one
 };
 
@@ -188,6 +248,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t full = bar_full + 8u * s;
+          if constexpr (kChecked) {
+            const bool a_ok = kAMNMajor ? tma_start_ok(mb * kBM, kb * kBK, M, K, 2)
+                                        : tma_start_ok(kb * kBK, mb * kBM, K, M, 2);
+            bool b_ok = true;
+            if constexpr (kBMNMajor) {
+              for (int j = 0; j < kBN / 64; ++j)
+                b_ok = b_ok && tma_start_ok(Epi::b_col(nb, j, N), kb * kBK, N, K, 2);
+            } else {
+              b_ok = tma_start_ok(kb * kBK, nb * kBN, K, N, 2);
+            }
+            if (!checked(a_ok, kChkTmaA) || !checked(b_ok, kChkTmaB)) {
+              *wc.abort_flag = 1u;
+              ok = false;
+              break;
+            }
+          }
           mbar_arrive_expect_tx(full, kStageBytes);
           const uint32_t a_dst = sA + s * kAStageBytes;
           const uint32_t b_dst = sB + s * kBStageBytes;
@@ -298,6 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
       c.mb = mb;
       c.nb = nb;
+      c.n0 = nb * kBN;
+      c.nend = min(N, c.n0 + kBN);
       c.row = row;
       c.half = half;
       c.M = M;
@@ -317,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  Epi::at_exit(ep);
+  if (threadIdx.x == 0) Epi::at_exit(ep);  // every thread of the block is done (barrier above)
 }
 
 }  // namespace coda

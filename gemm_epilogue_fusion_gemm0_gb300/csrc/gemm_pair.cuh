@@ -21,8 +21,6 @@
 // below) when whole tiles would leave the last wave of pairs mostly idle.
 #pragma once
 
-#include <cooperative_groups.h>
-
 #include <type_traits>
 
 #include "gemm.cuh"
@@ -64,9 +62,10 @@ static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared mem
 // pair's first tail item and waits for nothing but its own data, so the owner's
 // wait always ends.
 // The flag token is *epoch + 1, epoch being a counter in the caller's workspace
-// that the launch advances after a grid-wide barrier (the launch is then
-// cooperative): flags of earlier launches never match, so the slots need no
-// clearing and a launch replayed from a CUDA graph draws a fresh token.
+// that the last block of the launch to finish advances (launch_exit): flags of
+// earlier launches never match, so the slots need no clearing and a launch
+// replayed from a CUDA graph draws a fresh token.  The owner's wait needs the
+// other pair resident, so such a launch is cooperative.
 // Policies whose epilogue waits on other tiles (the data gradient's row flags)
 // are launched without a split tail.
 // ---------------------------------------------------------------------------
@@ -75,9 +74,10 @@ struct SkParams {
   float* part;      // [S][2 CTAs][128 x 256] fp32 partial accumulators
   uint64_t* flags;  // [S][2 CTAs]
   uint64_t* epoch;  // launch counter (any initial value); null when the tail is not split
+  int slots;        // S, the partial slots the workspace holds
 };
 
-constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr};
+constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr, 0};
 
 // A policy opts out of the split tail (its epilogue waits on other tiles) with
 // `static constexpr bool kSplitTail = false;`; the kernel then compiles without it.
@@ -169,6 +169,41 @@ __device__ __forceinline__ void sk_add_partial(uint32_t taddr, const float4* slo
   tmem_st_wait();
 }
 
+// ---------------------------------------------------------------------------
+// Column plan: tiles narrower than 256 columns, so that a launch's tiles spread
+// evenly over the CTA pairs.  With 256-column tiles a row block of d columns has
+// ceil(d / 256) tiles, and T tiles on U pairs leave the last wave (T mod U) / U
+// full: at d = 4096 and 32 row blocks, 512 tiles run 6.74 waves in the time of
+// 7.  A plan cuts every row block into nt tiles instead, nt - nl of them w
+// columns wide and nl of them w + 16 (w a multiple of 16, at most 240), laid out
+// from column 0 in tile order: tile j of row block mb is wide iff
+// (j + mb * rot) mod nt < nl, so the wide tiles move to other pairs from one row
+// block to the next (tile t goes to pair t mod U).  The MMA of a tile has that
+// width (N of tcgen05.mma .cta_group::2 is any multiple of 16 up to 256), each
+// CTA loads b_rows rows of B (half the widest tile) and the epilogue masks the
+// columns past the tile.  Only for K-major B operands in bf16 (the data
+// gradients: B = W1 read as [d, N1]).  nt == 0: the policy's own tiling.
+// ---------------------------------------------------------------------------
+struct ColPlan {
+  int nt;      // column tiles per row block (0: no plan)
+  int w;       // width of a narrow tile (multiple of 16)
+  int nl;      // wide tiles (w + 16 columns) per row block
+  int rot;     // rotation of the wide tiles from one row block to the next
+  int b_rows;  // rows of B each CTA loads per stage (the B tensor map's box)
+  // wide tiles among the positions [0, x) of the periodic pattern
+  __host__ __device__ __forceinline__ int wide_before(int x) const {
+    return (x / nt) * nl + min(x % nt, nl);
+  }
+  // first column and width of tile j of row block mb
+  __host__ __device__ __forceinline__ void tile(int mb, int j, int& n0, int& width) const {
+    const int s = static_cast<int>((static_cast<long long>(mb) * rot) % nt);
+    width = ((j + s) % nt < nl) ? w + 16 : w;
+    n0 = j * w + 16 * (wide_before(s + j) - wide_before(s));
+  }
+};
+
+constexpr ColPlan kNoColPlan = {0, kBN, 0, 0, 128};
+
 // plus the policy's store-staging buffers after the barrier area (see cta_smem_bytes)
 template <class Epi>
 __host__ __device__ constexpr uint32_t pair_smem_bytes() {
@@ -183,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_epilogue_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
                               int group_m, const typename Epi::Params ep, const SkParams sk,
-                              uint64_t timeout_ns) {
+                              const ColPlan cplan, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -210,7 +245,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const int npairs = gridDim.x >> 1;
   const int mt = (M + kPairBM - 1) / kPairBM;
-  const int nt = Epi::num_col_tiles(N);
+  // a column plan applies to bf16 K-major B without a split tail (see ColPlan)
+  constexpr bool kPlanCapable = !kBMNMajor && !kAMNMajor && !kFp8 && !SplitsTail<Epi>::value;
+  const bool planned = kPlanCapable && cplan.nt > 0;
+  const int nt = planned ? cplan.nt : Epi::num_col_tiles(N);
+  // first output column and width of tile (mb, nb)
+  const auto geometry = [&](int mb, int nb, int& n0, int& width) {
+    if (planned) {
+      cplan.tile(mb, nb, n0, width);
+    } else {
+      n0 = nb * kBN;
+      width = kBN;
+    }
+  };
   static_assert(!(kFp8 && kAMNMajor), "FP8 path: A must be K-major");
   constexpr int kKE = kFp8 ? 128 : kBK;  // K elements per stage (128-byte rows)
   const int nk = (K + kKE - 1) / kKE;
@@ -254,11 +301,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued_mask = 0, last_par = 0;
       bool ok = true;
+      // bytes one CTA's copies bring per stage (a plan's B box has b_rows rows of 128 bytes)
+      const uint32_t stage_bytes =
+          planned ? kPairAStageBytes + static_cast<uint32_t>(cplan.b_rows) * 128u : kPairStageBytes;
       const auto loads = [&](const WorkItem& w) {
         int mb, nb;
         tmap.coords(w.tile, mb, nb);
         const int arow = mb * kPairBM + static_cast<int>(rank) * 128;
-        const int bcol = nb * kBN + static_cast<int>(rank) * 128;  // K-major B rows
+        int n0, width;
+        geometry(mb, nb, n0, width);
+        const int bcol = n0 + static_cast<int>(rank) * (width / 2);  // K-major B rows
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
@@ -266,7 +318,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t full_local = bar_full + 8u * s;
           const uint32_t full_leader = mapa_shared(full_local, 0);
-          if (leader) mbar_arrive_expect_tx(full_local, 2u * kPairStageBytes);
+          if constexpr (kChecked) {
+            constexpr int es = kFp8 ? 1 : 2;
+            const bool a_ok = kAMNMajor ? tma_start_ok(arow, kb * kBK, M, K, es)
+                                        : tma_start_ok(kb * kKE, arow, K, M, es);
+            bool b_ok;
+            if constexpr (kFp8 && kBMNMajor) {
+              b_ok = tma_start_ok(Epi::b_col(nb, 2 * static_cast<int>(rank), N), kb * kKE, N, K, es);
+            } else if constexpr (kBMNMajor) {
+              const int j0 = 2 * static_cast<int>(rank);
+              b_ok = tma_start_ok(Epi::b_col(nb, j0, N), kb * kBK, N, K, es) &&
+                     tma_start_ok(Epi::b_col(nb, j0 + 1, N), kb * kBK, N, K, es);
+            } else {
+              b_ok = tma_start_ok(kb * kKE, bcol, K, N, es);
+            }
+            if (!checked(a_ok, kChkTmaA) || !checked(b_ok, kChkTmaB)) {
+              *wc.abort_flag = 1u;
+              ok = false;
+              break;
+            }
+          }
+          if (leader) mbar_arrive_expect_tx(full_local, 2u * stage_bytes);
           const uint32_t a_dst = sA + s * kPairAStageBytes;
           const uint32_t b_dst = sB + s * kPairBStageBytes;
           if constexpr (kAMNMajor) {
@@ -318,8 +390,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (CTA 0 only)
     if (lane == 0) {
       if (leader) {
-        constexpr uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPairBM, kBN, false, kBMNMajor)
-                                        : idesc_bf16_f32(kPairBM, kBN, kAMNMajor, kBMNMajor);
+        constexpr uint32_t idesc_full = kFp8 ? idesc_e4m3_f32(kPairBM, kBN, false, kBMNMajor)
+                                             : idesc_bf16_f32(kPairBM, kBN, kAMNMajor, kBMNMajor);
         int s = 0;
         uint32_t ph = 0;
         uint32_t it = 0;
@@ -333,6 +405,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * kBN;
+          uint32_t idesc = idesc_full;
+          if (planned) {  // N of the MMA = the tile's width
+            int mb, nb, n0, width;
+            tmap.coords(w.tile, mb, nb);
+            geometry(mb, nb, n0, width);
+            idesc = idesc_bf16_f32(kPairBM, width, kAMNMajor, kBMNMajor);
+          }
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!bounded_wait(bar_full + 8u * s, ph, wc, kSiteMmaFull)) {
               ok = false;
@@ -404,6 +483,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const size_t slot = static_cast<size_t>(w.tile - sk.dp_tiles) * 2 + rank;
         float4* part = reinterpret_cast<float4*>(sk.part + slot * kSkSlotFloats);
         uint64_t* flag = sk.flags + slot;
+        if constexpr (kChecked) {
+          if (!epi_all(checked(sk.part != nullptr && w.tile >= sk.dp_tiles &&
+                                   slot < 2 * static_cast<size_t>(sk.slots),
+                               kChkSplitSlot)))
+            return false;  // leave the role (every epilogue thread agrees)
+        }
         if (w.kind == kItemTail) {
           sk_write_partial(taddr, part, half, row);
           __threadfence();
@@ -432,6 +517,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
         c.mb = mb * 2 + static_cast<int>(rank);  // this CTA's 128-row slab
         c.nb = nb;
+        int width;
+        geometry(mb, nb, c.n0, width);
+        c.nend = min(N, c.n0 + width);
         c.row = row;
         c.half = half;
         c.M = M;
@@ -462,13 +550,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc_pair(tmem_base, kTmemCols);
   }
-  if (kSplit && sk.epoch != nullptr) {
-    // split tail: every flag of this launch has been read once the grid barrier
-    // is passed; advance the launch counter
-    cooperative_groups::this_grid().sync();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *sk.epoch = *sk.epoch + 1;
-  } else {
-    Epi::at_exit(ep);
+  // Both CTAs are past their last flag access (cluster barrier above): count
+  // this block out of the launch (the last one advances the launch counter).
+  if (threadIdx.x == 0) {
+    if (kSplit && sk.epoch != nullptr)
+      launch_exit(sk.epoch);
+    else
+      Epi::at_exit(ep);
   }
 }
 

@@ -1,9 +1,15 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA, tcgen05 (TMEM + MMA).
 //
-// Every wait in this library goes through bounded_wait()/flag_wait(): it gives
-// up after a host-set number of nanoseconds, records a code in the library's
-// device status word and returns false, so a protocol bug ends the kernel
-// instead of hanging the GPU.
+// Every wait of the kernels' own protocols (mbarrier phases, completion flags
+// written by other blocks) goes through bounded_wait()/flag_wait(): it gives up
+// after a host-set number of nanoseconds, records a code in the library's device
+// status word and returns false, so a protocol bug ends the kernel instead of
+// hanging the GPU.  The end of a launch is not a wait: each block counts itself
+// out with one atomic and the last one advances the launch counter
+// (launch_exit below).  The one wait not bounded here is
+// griddepcontrol.wait (programmatic dependent launch), which ends when the
+// preceding kernel in the stream completes; every kernel of this library
+// completes because all its other waits are bounded.
 #pragma once
 
 #include <cstdint>
@@ -140,6 +146,78 @@ __device__ __forceinline__ bool flag_wait(const uint64_t* p, uint64_t token, con
       record_failure(c, site);
       return false;
     }
+  }
+}
+
+// 128-bit compare-and-swap at GPU scope (acquire-release): {lo, hi} at p becomes
+// {n_lo, n_hi} if it held {e_lo, e_hi}.  Returns true on success; `o_lo`,
+// `o_hi` receive the value found.
+__device__ __forceinline__ bool cas128_gpu(uint64_t* p, uint64_t e_lo, uint64_t e_hi,
+                                           uint64_t n_lo, uint64_t n_hi, uint64_t& o_lo,
+                                           uint64_t& o_hi) {
+  asm volatile(
+      "{\n\t.reg .b128 d, e, n;\n\t"
+      "mov.b128 e, {%2, %3};\n\t"
+      "mov.b128 n, {%4, %5};\n\t"
+      "atom.acq_rel.gpu.global.cas.b128 d, [%6], e, n;\n\t"
+      "mov.b128 {%0, %1}, d;\n\t}"
+      : "=l"(o_lo), "=l"(o_hi)
+      : "l"(e_lo), "l"(e_hi), "l"(n_lo), "l"(n_hi), "l"(p)
+      : "memory");
+  return o_lo == e_lo && o_hi == e_hi;
+}
+
+__device__ __forceinline__ uint64_t atom_add_acq_rel_gpu_u64(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+
+// End of a launch whose blocks exchange flags tagged with a token taken from a
+// launch counter (the data gradient's row flags, the split tail's partial
+// flags).  `slot` is a 256-byte, 16-byte aligned slot of the caller's
+// workspace, any initial contents:
+//   slot[0]           launch counter; this launch's token is slot[0] + 1
+//   slot[1]           kSlotReady once slot[2] has been prepared by a launch
+//   slot[2]           blocks of the current launch that have finished (0 at its start)
+//   slot[4], slot[5]  {token, blocks finished}: the count of a first launch
+// Called by one thread per block once every thread of the block is done with
+// the launch's flags.  The block that completes the count (gridDim.x) prepares
+// slot[2] for the next launch and stores the token as the new launch counter,
+// after which no flag of this launch is read any more.  Nothing waits.  In
+// steady state each block adds 1 to slot[2] (one atomic).  On a slot not yet
+// prepared (a fresh workspace) the count goes through a 128-bit
+// compare-and-swap on {token, count} that any contents cannot fool (a token
+// that does not match restarts the count); every failed compare-and-swap means
+// another block got in, so that loop runs at most gridDim.x + 1 times.  Only the
+// last block writes slot[1], after every block has read it, so all blocks of a
+// launch take the same path.
+constexpr uint64_t kSlotReady = 0xC0DA5107C0DA5107ull;
+
+__device__ __forceinline__ void launch_exit(uint64_t* slot) {
+  volatile uint64_t* vs = reinterpret_cast<volatile uint64_t*>(slot);
+  const uint64_t token = vs[0] + 1;
+  bool last = false;
+  if (vs[1] == kSlotReady) {
+    last = atom_add_acq_rel_gpu_u64(slot + 2, 1) == gridDim.x - 1;
+  } else {
+    uint64_t e_lo = vs[4], e_hi = vs[5];
+    for (uint32_t i = 0; i <= gridDim.x; ++i) {
+      const uint64_t n_hi = (e_lo == token) ? e_hi + 1 : 1;
+      uint64_t o_lo, o_hi;
+      if (cas128_gpu(slot + 4, e_lo, e_hi, token, n_hi, o_lo, o_hi)) {
+        last = n_hi == gridDim.x;
+        break;
+      }
+      e_lo = o_lo;
+      e_hi = o_hi;
+    }
+  }
+  if (last) {
+    vs[2] = 0;
+    vs[1] = kSlotReady;
+    st_release_gpu_u64(slot, token);
   }
 }
 

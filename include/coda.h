@@ -67,7 +67,8 @@ typedef enum {
   CODA_ERR_LAUNCH = 5,             /* a CUDA launch or tensor-map encode failed */
   CODA_ERR_DEVICE_TIMEOUT = 6,     /* a bounded device-side wait ran out */
   CODA_ERR_NO_DEVICE = 7,          /* no CUDA device is current */
-  CODA_ERR_UNSUPPORTED_DEVICE = 8  /* the current device is not compute capability 10.3 */
+  CODA_ERR_UNSUPPORTED_DEVICE = 8, /* the current device is not compute capability 10.3 */
+  CODA_ERR_DEVICE_BOUNDS = 9       /* checked build only: a device-side bounds or alignment check failed */
 } coda_status_t;
 
 /* Bytes of device workspace coda_fwd needs: the bf16 GEMM1 operand
@@ -79,12 +80,17 @@ typedef enum {
 CODA_API size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /* Bytes of device workspace coda_bwd_dgrad needs: fp32 partial row
- * statistics (two per row and 256-column tile) and one 64-bit completion flag
- * per 128-row slab and column tile. */
+ * statistics (two per row and column tile), one 64-bit completion flag per
+ * 128-row slab and column tile, and a 256-byte slot holding the launch counter
+ * and its arrival word. */
 CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /*
- * Forward of the chain (the method's three steps, see the file header):
+ * Forward of the chain, the method's three steps ("CODA：将 Transformer 块重写为
+ * GEMM-Epilogue 程序以消除显存瓶颈", blog.hotdry.top, section
+ * "GEMM-Residual-RMSNorm-GEMM 重参数化": GEMM0 does the residual add and the
+ * gamma scaling and emits partial sums of squares, a light auxiliary pass forms
+ * the inverse RMS r, and GEMM1's epilogue multiplies its output rows by r):
  *   1. GEMM0 epilogue: h = x @ W0 + z (fp32), stores h and hg = h * gamma as
  *      bf16, and writes partial sums of h^2 (fp32, taken before rounding h;
  *      two per row and 256-column tile).
@@ -164,7 +170,11 @@ CODA_API coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t*
                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * Data gradient through the RMSNorm branch, as one GEMM-epilogue program:
+ * Data gradient through the RMSNorm branch, as one GEMM-epilogue program
+ * ("CODA：将 Transformer 块重写为 GEMM-Epilogue 程序以消除显存瓶颈",
+ * blog.hotdry.top, section "反向传播的 GEMM-Epilogue 结构": the backward keeps
+ * the GEMM-epilogue shape, and the row statistic s = sum_cols(grad_h2 * h2) =
+ * sum_cols(grad_y * y) is accumulated in a GEMM's epilogue):
  *   grad_h2 = grad_y @ W1^T  accumulated in tensor memory, then in the epilogue
  *   q[m]    = sum_j grad_h2[m,j] * gamma[j] * h[m,j]  (so s = r * q equals
  *             sum_j grad_h2 * h2 = sum_n grad_y * y), completed across the
@@ -182,7 +192,11 @@ CODA_API coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t*
  *   workspace needs no clearing (any initial contents work), and a call
  *   captured in a CUDA graph draws a fresh token at every replay.  Two calls
  *   that share a workspace must not run concurrently.
- * The kernel is a cooperative launch (all its blocks are resident at once).
+ * The kernel is a cooperative launch (all its blocks are resident at once):
+ * every column tile of a row block must be in flight together, so d is limited
+ * to 256 * (CTA pairs resident on the device) columns, 19456 on a 152-SM GB300
+ * (256 * SMs with coda_set_mma_mode(0)); larger d returns
+ * CODA_ERR_UNSUPPORTED_SHAPE without launching.  coda_bwd has the same limit.
  */
 CODA_API coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const coda_bf16* h,
                              const float* r, const coda_bf16* gamma,
@@ -256,10 +270,15 @@ CODA_API coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const c
                                 size_t workspace_bytes, cudaStream_t stream);
 
 /* Synchronises `stream`, then reports and clears the library's device-side
- * status word: CODA_OK, or CODA_ERR_DEVICE_TIMEOUT if a bounded wait in any
- * kernel of this library ran out since the last call.  If `detail` is not
- * NULL it receives the raw code (0 = none; otherwise which wait gave up).
- * Returns CODA_ERR_LAUNCH if the stream itself reports a CUDA error. */
+ * status word: CODA_OK, CODA_ERR_DEVICE_TIMEOUT if a bounded wait in any
+ * kernel of this library ran out since the last call (raw code 0x100 | which
+ * wait), or, in the checked build (libcoda_checked.so, compiled with
+ * -DCODA_CHECKED: every epilogue global access, TMA box start and workspace
+ * index checked on the device), CODA_ERR_DEVICE_BOUNDS if a check failed and
+ * its access was skipped (raw code 0x200 | which check).  The first failure
+ * since the last call is kept.  If `detail` is not NULL it receives the raw
+ * code (0 = none).  Returns CODA_ERR_LAUNCH if the stream itself reports a
+ * CUDA error. */
 CODA_API coda_status_t coda_get_device_status(cudaStream_t stream, uint32_t* detail);
 
 /* Tile shape of the tensor-core GEMMs used by every following call:
@@ -284,6 +303,19 @@ CODA_API coda_status_t coda_set_fold_rowreduce(int enable);
  * fill whole waves (see coda_fwd); 0 hands out whole tiles only.  Returns
  * CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_split_tail(int enable);
+
+/* 1 lets the CTA-pair data gradients (coda_bwd_dgrad and launch 1 of coda_bwd)
+ * cut each 256-row block into tiles narrower than 256 columns (two widths w and
+ * w + 16, multiples of 16 between 128 and 256, at most 2 * ceil(d / 256) tiles)
+ * when that spreads the tiles more evenly over the CTA pairs than 256-column
+ * tiles do: at d = 4096 and M = 8192, 19 tiles per row block fill 8 whole waves
+ * of 76 pairs where 16 tiles leave the seventh wave 74 % full.  The plan is
+ * chosen per shape and device on the host; results differ from 256-column tiles
+ * only in fp32 summation order.  Measured on GB300 it is slower at every Llama
+ * shape (narrower tiles re-read the grad_y rows once per tile), so 0, 256-column
+ * tiles, is the default.  Returns CODA_ERR_INVALID_ARG for any other value.
+ * Process-wide. */
+CODA_API coda_status_t coda_set_col_plan(int enable);
 
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records
@@ -352,9 +384,15 @@ CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t 
  *    ceil(M/128) * ceil(d/256) <= CODA_NOALLOC_MAX_TILES, otherwise it returns
  *    CODA_ERR_UNSUPPORTED_SHAPE without launching (e.g. M = 32768 rows at
  *    d = 4096, or 16384 rows at d = 8192, fit).
- *  - The first call on each device looks up the device address of the array
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - The library's device code, this array with it, is loaded on a device by
+ *    the first call of any entry point on that device (CUDA loads modules
+ *    lazily), and that first call also looks up the array's device address
+ *    (cudaGetSymbolAddress) with the device current.  Loading the module
+ *    reserves device memory for the array and the kernels, so the guarantee
+ *    that a call allocates nothing holds from the second library call on a
+ *    device on: make one call of any entry point that launches work (this one
+ *    included) on each device outside the region where allocation is
+ *    forbidden, and before any stream capture.
  *  - Every call uses the same array.  Nothing in it needs clearing (each
  *    launch tags its flags with a fresh token from a launch counter kept in
  *    the array), but calls whose kernels

@@ -65,10 +65,12 @@ def test_workspace_sizes(lib):
     assert _split_tail_bytes(M, d, N1) == 160 * 262144 + 2560 + 256
     assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 32 * M * 4 + _split_tail_bytes(M, d, N1)
     assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == M * d * 2
-    # qpart [2 * 16, M] fp32 + flags [2 * ceil(M/256) * 16] u64 (one per 128-row slab and column
-    # tile) + a 256-byte slot for the launch counter
-    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 32 * M * 4 + 64 * 16 * 8 + 256
-    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 2560 + 256 + 256  # 4 slabs x 1 tile
+    # qpart [2 * 32, M] fp32 + flags [2 * ceil(M/256) * 32] u64 (one per 128-row slab and column
+    # tile, for up to 2 * ceil(d/256) = 32 column tiles per row block) + a 256-byte slot for the
+    # launch counter
+    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 64 * M * 4 + 64 * 32 * 8 + 256
+    # 2 * 2 x 300 fp32 = 4800 -> 4864; 4 slabs x 2 tiles x 8 = 64 -> 256; + 256
+    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 4864 + 256 + 256
     assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
     assert _split_tail_bytes(300, 328, 776) == 8 * 262144 + 256 + 256  # 2 x 4 tiles
     assert lib.coda_fwd_workspace_bytes(300, 328, 776) == (  # ragged: rounded up

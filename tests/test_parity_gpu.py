@@ -196,7 +196,7 @@ def test_watchdog_reports_timeout_and_context_survives(B):
     assert B.coda_get_device_status()[0] == B.CODA_OK
     assert B.coda_watchdog_selftest(20_000_000) == B.CODA_OK  # 20 ms per wait
     st, detail = B.coda_get_device_status()
-    assert st == 6 and detail == 0x107, (st, hex(detail))  # first wait (mbarrier) ran out
+    assert st == B.CODA_ERR_DEVICE_TIMEOUT and detail == 0x107, (st, hex(detail))  # mbarrier wait ran out
     assert B.coda_get_device_status() == (B.CODA_OK, 0)  # cleared
     run_case(B, 128, 256, 512, 1e-5)  # the context is still usable
 
@@ -206,11 +206,50 @@ def test_watchdog_reports_timeout_and_context_survives(B):
 def test_llama_shapes_sampled_rows(B, mode, name):
     w = synth.WORKLOADS[name]
     rows = synth.sample_rows(w.M, 512, seed=1)
-    # The data gradient runs on the same shapes: saved h, r from this forward
-    # and dy drawn after the forward inputs from the same generator (llama7b is
-    # the backward workload; llama70b has 32 column tiles per row block in the
-    # cross-tile statistic).
-    run_case(B, w.M, w.d, w.N1, w.eps, seed=0, rows=rows, bwd=(name != "llama1b"))
+    # The data gradient runs on the same shapes, as the benchmark times it:
+    # saved h, r from this forward and dy drawn after the forward inputs from the
+    # same generator (llama7b is the backward workload; llama1b has 8 column
+    # tiles per row block and 3.4 waves of tiles, llama70b 32 column tiles per
+    # row block in the cross-tile statistic).
+    run_case(B, w.M, w.d, w.N1, w.eps, seed=0, rows=rows, bwd=True)
+
+
+# ----------------------------------------------------------------------------- column plans
+# Shapes whose CTA-pair data gradient cuts its row blocks into narrower tiles:
+# two widths with the wide ones rotating from row block to row block (2048 x
+# 4096: 19 tiles of 208 and 224 columns), ragged everywhere (2000 x 5000 x
+# 5064: 28 tiles; 3000 x 2600: 12 tiles that end past d), and 50 tiles per row
+# block (768 x 7168).
+PLAN_SHAPES = [(2048, 4096, 4096), (2000, 5000, 5064), (3000, 2600, 1000), (768, 7168, 512)]
+
+
+@pytest.mark.parametrize("M,d,N1", PLAN_SHAPES)
+def test_dgrad_column_plans_match_oracle(B, M, d, N1):
+    """The data gradient with the column plan (coda_set_col_plan(1)) and with
+    256-column tiles (the default), both against the oracle on the same saved h, r,
+    on a seeded sample of rows (rows 0, 127, 128 and M - 1 among them; every
+    column of those rows, so every column tile of every plan)."""
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=5)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    h, r, _ = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5)
+    dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
+    dy = dy_cpu.to(dev)
+    got = {}
+    for plan in (1, 0):
+        B.coda_set_col_plan(plan)
+        try:
+            got[plan] = B.coda_bwd_dgrad(dy, g["W1"], h, r, g["gamma"])
+        finally:
+            B.coda_set_col_plan(0)
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    rows = synth.sample_rows(M, 256, seed=2)
+    idx = torch.as_tensor(rows)
+    bref = oracle.backward_dgrad(f64(dy_cpu[idx]), f64(t["W1"]), f64(h.cpu()[idx]),
+                                 f64(r.cpu()[idx]), f64(t["gamma"]))
+    for plan, dh in got.items():
+        check(f"dh (plan {plan})", f64(dh.cpu()[idx]), bref.dh, TOL_DH)
 
 
 # ----------------------------------------------------------------------------- SwiGLU forward
@@ -615,8 +654,10 @@ def test_step_replays_from_a_cuda_graph(B, mode):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step()
-    nt = (d + 255) // 256
-    flags = ws_b[((2 * nt * M * 4 + 255) // 256) * 256:].view(torch.int64)
+    ntmax = 2 * ((d + 255) // 256)  # the workspace holds up to 2 ceil(d/256) column tiles
+    # 128-row slabs: two per 256-row block of CTA-pair tiles, else one per 128-row tile
+    slabs = 2 * ((M + 255) // 256) if mode == 1 else (M + 127) // 128
+    flags = ws_b[((2 * ntmax * M * 4 + 255) // 256) * 256:][: slabs * ntmax * 8].view(torch.int64)
     for data in sets:
         for k in buf:
             buf[k].copy_(data[k])
@@ -636,8 +677,10 @@ def test_step_replays_from_a_cuda_graph(B, mode):
             assert torch.equal(got, want)
         e2 = epoch()
         assert (e2 - e0) % 2 ** 64 == 2  # the counter starts at whatever the workspace held
-        used = flags[: ((M + 127) // 128) * nt]
-        assert torch.all(used == e2), "every flag holds the last replay's token"
+        # the launch used the first slabs * nt flags, nt its column tiles per row block
+        k = int((flags == e2).sum())
+        assert k > 0 and k % slabs == 0 and k // slabs >= (d + 255) // 256, k
+        assert torch.all(flags[:k] == e2), "every flag holds the last replay's token"
 
 
 @pytest.mark.parametrize("entry", ["fwd_swiglu", "bwd_swiglu_dgrad", "bwd", "fwd_fp8"])
