@@ -216,7 +216,7 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    w = WORKLOAD
+    w = synth.WORKLOADS[args.workload]
     t = synth.make_forward_inputs(w.M, w.d, w.N1, seed=0)
     dy = synth.make_grad_output(t["_rng"], w.M, w.N1)
     x, z, dy64, W0, W1, g = oracle_setup(t, dy)
@@ -298,32 +298,39 @@ def alternating(stream, barrier, calls, rounds=6, n=20):
     return {k: statistics.median(v) for k, v in out.items()}
 
 
-def fp8_peak(dev, peaks, n=8192, sustain_s=4.0):
+def fp8_peak(dev, peaks, shapes=((8192, 8192, 8192),), sustain_s=4.0):
     """Dense E4M3 GEMM throughput on this GPU, measured the way the bf16 peaks
-    are: torch._scaled_mm (cuBLASLt) on n x n x n E4M3 operands with bf16
-    output, best of 10 single calls (burst) and back to back for `sustain_s`
-    seconds (sustained).  Falls back to twice the measured bf16 figures (the
-    nominal dense ratio) if the library call is unavailable, and says so."""
+    are: torch._scaled_mm (cuBLASLt) on E4M3 operands with bf16 output, best of
+    10 single calls (burst) at each (M, K, N) of `shapes`, the fastest shape then
+    back to back for `sustain_s` seconds (sustained).  Falls back to twice the
+    measured bf16 figures (the nominal dense ratio) if the library call is
+    unavailable, and says so."""
     try:
-        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
-        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)  # [N, K] row-major
         one = torch.ones((), dtype=torch.float32, device=dev)
+        best, best_mm, per_shape = 0.0, None, {}
+        for (m, k, n) in shapes:
+            a = torch.randn(m, k, device=dev).to(torch.float8_e4m3fn)
+            b = torch.randn(n, k, device=dev).to(torch.float8_e4m3fn)  # [N, K] row-major
 
-        def mm():
-            return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            def mm(a=a, b=b):
+                return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
 
-        for _ in range(3):
-            mm()
-        torch.cuda.synchronize()
-        flops = 2.0 * n ** 3
-        best = float("inf")
-        for _ in range(10):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            mm()
-            e1.record()
+            for _ in range(3):
+                mm()
             torch.cuda.synchronize()
-            best = min(best, e0.elapsed_time(e1))
+            t_best = float("inf")
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                mm()
+                e1.record()
+                torch.cuda.synchronize()
+                t_best = min(t_best, e0.elapsed_time(e1))
+            tf = 2.0 * m * k * n / (t_best * 1e-3) / 1e12
+            per_shape[f"{m}x{k}x{n}"] = tf
+            if tf > best:
+                best, best_mm, flops = tf, mm, 2.0 * m * k * n
+        mm = best_mm
         calls, t0 = 0, time.perf_counter()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -335,9 +342,11 @@ def fp8_peak(dev, peaks, n=8192, sustain_s=4.0):
         e1.record()
         torch.cuda.synchronize()
         sus = flops * calls / (e0.elapsed_time(e1) * 1e-3) / 1e12
-        return ({"burst": flops / (best * 1e-3) / 1e12, "sustained": sus},
-                f"measured in this run: torch._scaled_mm E4M3 x E4M3 -> bf16, {n}^3, best of 10 "
-                f"(burst) and back to back for {sustain_s:.0f} s (sustained)")
+        shown = ", ".join(f"{k2} {v:.0f}" for k2, v in per_shape.items())
+        return ({"burst": best, "sustained": sus, "per_shape_burst": per_shape},
+                f"measured in this run: torch._scaled_mm E4M3 x E4M3 -> bf16 (M x K x N: burst "
+                f"TFLOP/s {shown}), the fastest shape's best of 10 (burst) and back to back for "
+                f"{sustain_s:.0f} s (sustained)")
     except Exception as exc:  # noqa: BLE001 (reported in the line)
         return ({"burst": 2.0 * peaks["bf16_tflops"], "sustained": 2.0 * peaks["bf16_tflops_sustained"]},
                 f"2 x the bf16 peaks (nominal dense ratio): torch._scaled_mm unavailable ({exc!r:.120})")
@@ -345,16 +354,21 @@ def fp8_peak(dev, peaks, n=8192, sustain_s=4.0):
 
 def col_plan_ab(B, stream, barrier, call):
     """Medians of alternating rounds of `call` (a data gradient) with 256-column
-    tiles (the default) and with the column plan (coda_set_col_plan(1))."""
-    def planned():
-        B.coda_set_col_plan(1)
-        try:
-            call()
-        finally:
-            B.coda_set_col_plan(0)
-    planned()
+    tiles (the default) and with the column plans (coda_set_col_plan(1): widths
+    in steps of 16; coda_set_col_plan(2): widths that are multiples of 64)."""
+    def planned(mode):
+        def f():
+            B.coda_set_col_plan(mode)
+            try:
+                call()
+            finally:
+                B.coda_set_col_plan(0)
+        return f
+    p16, p64 = planned(1), planned(2)
+    p16()
+    p64()
     call()
-    return alternating(stream, barrier, {"col_plan": planned, "tiles_256": call})
+    return alternating(stream, barrier, {"col_plan_16": p16, "col_plan_64": p64, "tiles_256": call})
 
 
 def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
@@ -438,7 +452,8 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
 
     if "fwd_fp8" in want:
         # F4: the forward with FP8 (E4M3) GEMM operands
-        p8, p8_src = fp8_peak(dev, peaks)
+        # the library's E4M3 rate at a square shape and at both GEMMs of this workload
+        p8, p8_src = fp8_peak(dev, peaks, shapes=((8192, 8192, 8192), (M, d, d), (M, d, N1)))
         t8 = synth.make_fp8_forward_inputs(M, d, N1, seed=rank)
         f8 = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t8.items()}
         ws8 = B.workspace(B.coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
@@ -457,6 +472,7 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
             "kernels_ms": {"gemm0_fp8": k[0], "rowreduce": k[1], "gemm1_fp8": k[2]},
             "kernels_tflops": {"gemm0_fp8": g0, "gemm1_fp8": g1},
             "fp8_peak_tflops": pk, "fp8_peak_sustained_tflops": p8["sustained"],
+            "fp8_peak_per_shape_burst_tflops": p8.get("per_shape_burst"),
             "fp8_peak_source": p8_src,
             "frac_of_fp8_peak": tf(w.fwd_flops, ms) / pk,
             "kernels_frac_of_fp8_peak": {"gemm0_fp8": g0 / pk, "gemm1_fp8": g1 / pk},
@@ -688,7 +704,7 @@ def run_coda(args):
     if args.mma_mode is not None:
         B.coda_set_mma_mode(args.mma_mode)
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = WORKLOAD
+    w = synth.WORKLOADS[args.workload]
     M, d, N1, eps = w.M, w.d, w.N1, w.eps
     t = synth.make_forward_inputs(M, d, N1, seed=rank)
     dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
@@ -945,7 +961,8 @@ def run_coda(args):
             "M": M, "d": d, "N1": N1, "eps": eps, "step": "coda_fwd + coda_bwd_dgrad",
             "parallelism": f"replicas x{world} (rows sharded, no collective)",
             "mma": ["cta_group::1 128x256 tiles", "cta_group::2 256x256 tiles"][B.coda_get_mma_mode()],
-            "l2": "no flush: inputs larger than L2 (W1 235 MB, dy 470 MB; ~1.6 GB touched per step)",
+            "l2": f"no flush: inputs larger than L2 (W1 {d * N1 * 2 / 1e6:.0f} MB, dy "
+                  f"{M * N1 * 2 / 1e6:.0f} MB per step)",
             "kernel_times": f"CUDA events around every launch of {len(sampled)} of the {K} timed steps "
                             "(steps 5, 15, ...; the others launch back to back under programmatic "
                             "dependent launch)",
@@ -983,6 +1000,9 @@ def main():
     ap.add_argument("--extras", default="all",
                     help="widened paths timed after the step: 'all', 'none' or a comma list of "
                          + ", ".join(EXTRAS))
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default=WORKLOAD.name,
+                    help="the step's shapes (default llama7b, the metric's workload; the others "
+                         "for profiling at other sizes)")
     ap.add_argument("--mma-mode", type=int, choices=[0, 1], default=None,
                     help="0: single-CTA tiles, 1: CTA-pair tiles (library default)")
     args = ap.parse_args()

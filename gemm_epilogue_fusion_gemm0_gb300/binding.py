@@ -340,8 +340,8 @@ def coda_set_split_tail(enable: int) -> None:
 
 
 def coda_set_col_plan(enable: int) -> None:
-    """1: the CTA-pair data gradients may use narrower column tiles that spread evenly over
-    the pairs; 0: 256-column tiles (default)."""
+    """1 (2): the CTA-pair data gradients may use narrower column tiles, widths in steps of
+    16 (64), that spread evenly over the pairs; 0: 256-column tiles (default)."""
     _check(_lib.coda_set_col_plan(int(enable)), "coda_set_col_plan")
 
 

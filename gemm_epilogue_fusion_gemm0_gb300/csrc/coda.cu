@@ -609,7 +609,9 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
 // ---------------------------------------------------------------------------
 // Column plans for the CTA-pair data gradient (gemm_pair.cuh, ColPlan).
 // ---------------------------------------------------------------------------
-std::atomic<int> g_col_plan{0};  // 1: the data gradients may use narrower column tiles
+// 0: 256-column tiles; 1 (2): the data gradients may use narrower column tiles
+// whose widths are multiples of 16 (of 64)
+std::atomic<int> g_col_plan{0};
 
 // Most column tiles per row block the data-gradient workspace is sized for.
 int64_t dgrad_max_col_tiles(int64_t d) { return 2 * cdiv(d, kBN); }
@@ -667,15 +669,18 @@ std::map<PlanKey, ColPlan> g_plan_cache;
 // The column plan for a data gradient of mt 256-row blocks, d output columns
 // and K = N1 on `npairs` CTA pairs: among 256-column tiles and every tiling
 // into nt tiles (ceil(d/256) <= nt <= 2 ceil(d/256), at most npairs, so that a
-// row block's tiles can all be in flight at once) of widths w and w + 16
-// (128 <= w, w + 16 <= 256), each with its best rotation, the one whose
-// largest per-pair load is smallest.  A tile's fixed cost (pipeline fill,
-// drain, epilogue not hidden) is taken as 2 us against a pair's 256-column
-// tile time 2 * 256 * 256 * K / (25 TFLOP/s); a plan must beat the 256-column
-// tiling by 0.5 % to be taken.  Memoised per shape and pair count.
+// row block's tiles can all be in flight at once) of widths w and w + step
+// (step 16 or 64 as the switch says, w a multiple of step, 128 <= w,
+// w + step <= 256), each with its best rotation, the one whose largest
+// per-pair load is smallest.  A tile's fixed cost (pipeline fill, drain,
+// epilogue not hidden) is taken as 2 us against a pair's 256-column tile time
+// 2 * 256 * 256 * K / (25 TFLOP/s); a plan must beat the 256-column tiling by
+// 0.5 % to be taken.  Memoised per shape, pair count and step.
 ColPlan plan_dgrad_cols(int64_t mt, int64_t d, int64_t K, int npairs) {
-  if (g_col_plan.load() == 0 || npairs < 2) return kNoColPlan;
-  const PlanKey key{mt, d, K, npairs};
+  const int mode = g_col_plan.load();
+  if (mode == 0 || npairs < 2) return kNoColPlan;
+  const int step = mode == 2 ? 64 : 16;
+  const PlanKey key{mt, d, K, npairs * 4 + mode};
   {
     std::lock_guard<std::mutex> lock(g_plan_mu);
     auto it = g_plan_cache.find(key);
@@ -684,21 +689,21 @@ ColPlan plan_dgrad_cols(int64_t mt, int64_t d, int64_t K, int npairs) {
   const double c = 2e-6 / (2.0 * 256 * 256 * static_cast<double>(K) / 25e12);
   std::vector<double> load;
   const int nt0 = static_cast<int>(cdiv(d, kBN));
-  ColPlan uni = {nt0, kBN, 0, 0, 128};
+  ColPlan uni = {nt0, kBN, 0, 0, 128, step};
   const double base = plan_load(uni, static_cast<int>(mt), npairs, c, load);
   ColPlan best = kNoColPlan;
   double best_load = base * (1.0 - 0.005);
   const int nt_hi = static_cast<int>(std::min<int64_t>(dgrad_max_col_tiles(d), npairs));
   for (int nt = nt0; nt <= nt_hi; ++nt) {
-    int w = static_cast<int>(d / nt) / 16 * 16;
-    int nl = static_cast<int>(cdiv(d - static_cast<int64_t>(nt) * w, 16));
+    int w = static_cast<int>(d / nt) / step * step;
+    int nl = static_cast<int>(cdiv(d - static_cast<int64_t>(nt) * w, step));
     if (nl >= nt) {
-      w += 16;
+      w += step;
       nl = 0;
     }
-    if (w < 128 || w + (nl > 0 ? 16 : 0) > kBN) continue;
+    if (w < 128 || w + (nl > 0 ? step : 0) > kBN) continue;
     for (int rot = 0; rot < (nl > 0 ? nt : 1); ++rot) {
-      const ColPlan cp = {nt, w, nl, rot, (w + (nl > 0 ? 16 : 0)) / 2};
+      const ColPlan cp = {nt, w, nl, rot, (w + (nl > 0 ? step : 0)) / 2, step};
       const double l = plan_load(cp, static_cast<int>(mt), npairs, c, load);
       if (l < best_load - 1e-9) {
         best_load = l;
@@ -1188,7 +1193,7 @@ coda_status_t coda_set_split_tail(int enable) {
 }
 
 coda_status_t coda_set_col_plan(int enable) {
-  if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
+  if (enable < 0 || enable > 2) return CODA_ERR_INVALID_ARG;
   g_col_plan.store(enable);
   return CODA_OK;
 }

@@ -175,8 +175,8 @@ __device__ __forceinline__ void sk_add_partial(uint32_t taddr, const float4* slo
 // ceil(d / 256) tiles, and T tiles on U pairs leave the last wave (T mod U) / U
 // full: at d = 4096 and 32 row blocks, 512 tiles run 6.74 waves in the time of
 // 7.  A plan cuts every row block into nt tiles instead, nt - nl of them w
-// columns wide and nl of them w + 16 (w a multiple of 16, at most 240), laid out
-// from column 0 in tile order: tile j of row block mb is wide iff
+// columns wide and nl of them w + step (w and step multiples of 16, w + step at
+// most 256), laid out from column 0 in tile order: tile j of row block mb is wide iff
 // (j + mb * rot) mod nt < nl, so the wide tiles move to other pairs from one row
 // block to the next (tile t goes to pair t mod U).  The MMA of a tile has that
 // width (N of tcgen05.mma .cta_group::2 is any multiple of 16 up to 256), each
@@ -187,9 +187,10 @@ __device__ __forceinline__ void sk_add_partial(uint32_t taddr, const float4* slo
 struct ColPlan {
   int nt;      // column tiles per row block (0: no plan)
   int w;       // width of a narrow tile (multiple of 16)
-  int nl;      // wide tiles (w + 16 columns) per row block
+  int nl;      // wide tiles (w + step columns) per row block
   int rot;     // rotation of the wide tiles from one row block to the next
   int b_rows;  // rows of B each CTA loads per stage (the B tensor map's box)
+  int step;    // a wide tile's extra columns (multiple of 16)
   // wide tiles among the positions [0, x) of the periodic pattern
   __host__ __device__ __forceinline__ int wide_before(int x) const {
     return (x / nt) * nl + min(x % nt, nl);
@@ -197,12 +198,12 @@ struct ColPlan {
   // first column and width of tile j of row block mb
   __host__ __device__ __forceinline__ void tile(int mb, int j, int& n0, int& width) const {
     const int s = static_cast<int>((static_cast<long long>(mb) * rot) % nt);
-    width = ((j + s) % nt < nl) ? w + 16 : w;
-    n0 = j * w + 16 * (wide_before(s + j) - wide_before(s));
+    width = ((j + s) % nt < nl) ? w + step : w;
+    n0 = j * w + step * (wide_before(s + j) - wide_before(s));
   }
 };
 
-constexpr ColPlan kNoColPlan = {0, kBN, 0, 0, 128};
+constexpr ColPlan kNoColPlan = {0, kBN, 0, 0, 128, 16};
 
 // plus the policy's store-staging buffers after the barrier area (see cta_smem_bytes)
 template <class Epi>

@@ -304,17 +304,17 @@ CODA_API coda_status_t coda_set_fold_rowreduce(int enable);
  * CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_split_tail(int enable);
 
-/* 1 lets the CTA-pair data gradients (coda_bwd_dgrad and launch 1 of coda_bwd)
- * cut each 256-row block into tiles narrower than 256 columns (two widths w and
- * w + 16, multiples of 16 between 128 and 256, at most 2 * ceil(d / 256) tiles)
- * when that spreads the tiles more evenly over the CTA pairs than 256-column
- * tiles do: at d = 4096 and M = 8192, 19 tiles per row block fill 8 whole waves
- * of 76 pairs where 16 tiles leave the seventh wave 74 % full.  The plan is
- * chosen per shape and device on the host; results differ from 256-column tiles
- * only in fp32 summation order.  Measured on GB300 it is slower at every Llama
- * shape (narrower tiles re-read the grad_y rows once per tile), so 0, 256-column
- * tiles, is the default.  Returns CODA_ERR_INVALID_ARG for any other value.
- * Process-wide. */
+/* 1 or 2 lets the CTA-pair data gradients (coda_bwd_dgrad and launch 1 of
+ * coda_bwd) cut each 256-row block into tiles narrower than 256 columns (two
+ * widths w and w + step, between 128 and 256, at most 2 * ceil(d / 256) tiles;
+ * 1: w and step multiples of 16, 2: multiples of 64) when that spreads the tiles
+ * more evenly over the CTA pairs than 256-column tiles do: at d = 4096 and
+ * M = 8192, 19 tiles per row block fill 8 whole waves of 76 pairs where 16 tiles
+ * leave the seventh wave 74 % full.  The plan is chosen per shape and device on
+ * the host; results differ from 256-column tiles only in fp32 summation order.
+ * Measured on GB300 both are slower at every Llama shape (more tiles per row
+ * block read the grad_y rows more often), so 0, 256-column tiles, is the
+ * default.  Returns CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_col_plan(int enable);
 
 /* Upper bound, in nanoseconds, of every device-side wait launched after this

@@ -225,8 +225,9 @@ PLAN_SHAPES = [(2048, 4096, 4096), (2000, 5000, 5064), (3000, 2600, 1000), (768,
 
 @pytest.mark.parametrize("M,d,N1", PLAN_SHAPES)
 def test_dgrad_column_plans_match_oracle(B, M, d, N1):
-    """The data gradient with the column plan (coda_set_col_plan(1)) and with
-    256-column tiles (the default), both against the oracle on the same saved h, r,
+    """The data gradient with the column plans (coda_set_col_plan(1): widths in
+    steps of 16; coda_set_col_plan(2): multiples of 64) and with 256-column tiles
+    (the default), each against the oracle on the same saved h, r,
     on a seeded sample of rows (rows 0, 127, 128 and M - 1 among them; every
     column of those rows, so every column tile of every plan)."""
     dev = torch.device("cuda:0")
@@ -236,7 +237,7 @@ def test_dgrad_column_plans_match_oracle(B, M, d, N1):
     dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
     dy = dy_cpu.to(dev)
     got = {}
-    for plan in (1, 0):
+    for plan in (1, 2, 0):
         B.coda_set_col_plan(plan)
         try:
             got[plan] = B.coda_bwd_dgrad(dy, g["W1"], h, r, g["gamma"])
