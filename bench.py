@@ -353,9 +353,11 @@ def fp8_peak(dev, peaks, shapes=((8192, 8192, 8192),), sustain_s=4.0):
 
 
 def col_plan_ab(B, stream, barrier, call):
-    """Medians of alternating rounds of `call` (a data gradient) with 256-column
-    tiles (the default) and with the column plans (coda_set_col_plan(1): widths
-    in steps of 16; coda_set_col_plan(2): widths that are multiples of 64)."""
+    """Medians of alternating rounds of `call` (a data gradient) with the
+    defaults (256-column tiles, every other wave loading K backwards) against K
+    loaded forwards in every wave (coda_set_serpentine_k(0)) and against the
+    column plans (coda_set_col_plan(1): widths in steps of 16; (2): multiples
+    of 64)."""
     def planned(mode):
         def f():
             B.coda_set_col_plan(mode)
@@ -364,11 +366,18 @@ def col_plan_ab(B, stream, barrier, call):
             finally:
                 B.coda_set_col_plan(0)
         return f
+
+    def k_forward():
+        B.coda_set_serpentine_k(0)
+        try:
+            call()
+        finally:
+            B.coda_set_serpentine_k(1)
     p16, p64 = planned(1), planned(2)
-    p16()
-    p64()
-    call()
-    return alternating(stream, barrier, {"col_plan_16": p16, "col_plan_64": p64, "tiles_256": call})
+    for f in (p16, p64, k_forward, call):
+        f()
+    return alternating(stream, barrier, {"col_plan_16": p16, "col_plan_64": p64,
+                                         "k_forward": k_forward, "default": call})
 
 
 def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
@@ -437,8 +446,8 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
         extras["other_llama_shapes"] = by_w
 
     if "dgrad_col_plan" in want:
-        # the data gradient with 256-column tiles (the default) against narrower
-        # column tiles spread evenly over the pairs, alternating rounds at this workload
+        # the data gradient as by default against its K-forward and column-plan
+        # variants, alternating rounds at this workload
         ws_b = B.workspace(B.coda_bwd_dgrad_workspace_bytes(M, d, N1), dev)
 
         def bwd():
@@ -446,8 +455,9 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
         t = col_plan_ab(B, stream, barrier, bwd)
         extras["dgrad_col_plan"] = {
             "alternating_ms": t, "tflops": {k: tf(w.bwd_flops, v) for k, v in t.items()},
-            "note": "coda_bwd_dgrad with 256-column tiles (default) against the column plan "
-                    "(coda_set_col_plan(1)), medians of alternating rounds"}
+            "note": "coda_bwd_dgrad as by default (256-column tiles, every other wave loading K "
+                    "backwards) against K forwards in every wave and against the column plans "
+                    "(coda_set_col_plan(1), (2)), medians of alternating rounds"}
         del ws_b
 
     if "fwd_fp8" in want:

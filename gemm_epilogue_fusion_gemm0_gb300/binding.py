@@ -79,6 +79,7 @@ EXPORTS = {
     "coda_set_fold_rowreduce": (_st, [ctypes.c_int]),
     "coda_set_split_tail": (_st, [ctypes.c_int]),
     "coda_set_col_plan": (_st, [ctypes.c_int]),
+    "coda_set_serpentine_k": (_st, [ctypes.c_int]),
     "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
                            _vp, _vp, _vp, _sz, _vp]),
@@ -343,6 +344,12 @@ def coda_set_col_plan(enable: int) -> None:
     """1 (2): the CTA-pair data gradients may use narrower column tiles, widths in steps of
     16 (64), that spread evenly over the pairs; 0: 256-column tiles (default)."""
     _check(_lib.coda_set_col_plan(int(enable)), "coda_set_col_plan")
+
+
+def coda_set_serpentine_k(enable: int) -> None:
+    """1: the CTA-pair data gradients load every other wave's K blocks backwards (default);
+    0: forwards."""
+    _check(_lib.coda_set_serpentine_k(int(enable)), "coda_set_serpentine_k")
 
 
 def coda_get_mma_mode() -> int:

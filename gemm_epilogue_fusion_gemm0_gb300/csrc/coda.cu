@@ -612,6 +612,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
 // 0: 256-column tiles; 1 (2): the data gradients may use narrower column tiles
 // whose widths are multiples of 16 (of 64)
 std::atomic<int> g_col_plan{0};
+std::atomic<int> g_dgrad_kserp{1};  // 1: the data gradients load every other wave's K backwards
 
 // Most column tiles per row block the data-gradient workspace is sized for.
 int64_t dgrad_max_col_tiles(int64_t d) { return 2 * cdiv(d, kBN); }
@@ -786,7 +787,8 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   // Row-major tile order; every column tile of a row block must be in flight
   // at once (at most one wave per row block), see EpiRmsNormBackward.
   const int mt = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
-  const ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
+  ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
+  cp.kserp = g_dgrad_kserp.load();
   const int nt = cp.nt > 0 ? cp.nt : static_cast<int>(cdiv(d, kBN));
   const int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
   if (nt > units) return CODA_ERR_UNSUPPORTED_SHAPE;
@@ -945,7 +947,8 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const int nt = static_cast<int>(cdiv(d, kBN));  // 256-column tiles of the GEMMs with N = d
   const int mt = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
   // launch 1 (the data gradient) may cut its row blocks into a column plan's tiles
-  const ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
+  ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
+  cp.kserp = g_dgrad_kserp.load();
   const int nt1 = cp.nt > 0 ? cp.nt : nt;
   const int units = pair ? std::min(max_pairs, mt * nt1) : std::min(sms, mt * nt1);
   if (nt1 > units) return CODA_ERR_UNSUPPORTED_SHAPE;
@@ -1195,6 +1198,12 @@ coda_status_t coda_set_split_tail(int enable) {
 coda_status_t coda_set_col_plan(int enable) {
   if (enable < 0 || enable > 2) return CODA_ERR_INVALID_ARG;
   g_col_plan.store(enable);
+  return CODA_OK;
+}
+
+coda_status_t coda_set_serpentine_k(int enable) {
+  if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
+  g_dgrad_kserp.store(enable);
   return CODA_OK;
 }
 

@@ -183,6 +183,11 @@ __device__ __forceinline__ void sk_add_partial(uint32_t taddr, const float4* slo
 // CTA loads b_rows rows of B (half the widest tile) and the epilogue masks the
 // columns past the tile.  Only for K-major B operands in bf16 (the data
 // gradients: B = W1 read as [d, N1]).  nt == 0: the policy's own tiling.
+// kserp (with or without nt) reverses the K order of every other wave of
+// tiles: the pairs of one wave walk K in step, so the wave that follows starts
+// on the K slices of B that the previous one read last, which the L2 may still
+// hold.  Only the load order changes; the MMA accumulates the k-blocks in the
+// order they arrive, so results differ only in fp32 summation order.
 // ---------------------------------------------------------------------------
 struct ColPlan {
   int nt;      // column tiles per row block (0: no plan)
@@ -191,6 +196,7 @@ struct ColPlan {
   int rot;     // rotation of the wide tiles from one row block to the next
   int b_rows;  // rows of B each CTA loads per stage (the B tensor map's box)
   int step;    // a wide tile's extra columns (multiple of 16)
+  int kserp;   // 1: tiles of odd waves (tile / pairs odd) load K backwards (any nt)
   // wide tiles among the positions [0, x) of the periodic pattern
   __host__ __device__ __forceinline__ int wide_before(int x) const {
     return (x / nt) * nl + min(x % nt, nl);
@@ -203,7 +209,7 @@ struct ColPlan {
   }
 };
 
-constexpr ColPlan kNoColPlan = {0, kBN, 0, 0, 128, 16};
+constexpr ColPlan kNoColPlan = {0, kBN, 0, 0, 128, 16, 0};
 
 // plus the policy's store-staging buffers after the barrier area (see cta_smem_bytes)
 template <class Epi>
@@ -312,7 +318,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int n0, width;
         geometry(mb, nb, n0, width);
         const int bcol = n0 + static_cast<int>(rank) * (width / 2);  // K-major B rows
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
+        // serpentine K order: whole tiles of odd waves walk K backwards (see ColPlan)
+        const bool rev = kPlanCapable && cplan.kserp != 0 && w.kind == kItemWhole &&
+                         ((w.tile / npairs) & 1) != 0;
+        for (int ki = w.kb0; ki < w.kb1; ++ki) {
+          const int kb = rev ? w.kb0 + w.kb1 - 1 - ki : ki;
           if (!bounded_wait(bar_empty + 8u * s, ph ^ 1u, wc, kSiteProducerEmpty)) {
             ok = false;
             break;

@@ -317,6 +317,16 @@ CODA_API coda_status_t coda_set_split_tail(int enable);
  * default.  Returns CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_col_plan(int enable);
 
+/* 1 (the default) makes the CTA-pair data gradients (coda_bwd_dgrad and launch
+ * 1 of coda_bwd) load the K blocks of every other wave of tiles in reverse
+ * order, so that a wave starts on the slices of W1 that the wave before it read
+ * last, which the L2 still holds (each wave streams all of W1, 235 MB at
+ * llama7b, through the 129 MB L2).  Measured on GB300: 1.3-1.7 % faster at the
+ * llama1b and llama7b shapes, 4.8 % at llama70b.  Results differ only in fp32
+ * summation order.  0 loads K forwards.  Returns CODA_ERR_INVALID_ARG for any
+ * other value.  Process-wide. */
+CODA_API coda_status_t coda_set_serpentine_k(int enable);
+
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records
  * CODA_ERR_DEVICE_TIMEOUT and lets its kernel finish without hanging. */
