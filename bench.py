@@ -353,11 +353,11 @@ def fp8_peak(dev, peaks, shapes=((8192, 8192, 8192),), sustain_s=4.0):
 
 
 def col_plan_ab(B, stream, barrier, call):
-    """Medians of alternating rounds of `call` (a data gradient) with the
-    defaults (256-column tiles, every other wave loading K backwards) against K
-    loaded forwards in every wave (coda_set_serpentine_k(0)) and against the
-    column plans (coda_set_col_plan(1): widths in steps of 16; (2): multiples
-    of 64)."""
+    """Per-call medians, calls interleaved one by one (see interleaved), of
+    `call` (a data gradient) as by default against K loaded forwards in every
+    wave (coda_set_serpentine_k(0)), K loaded backwards in every other wave
+    ((1)) and the column plans (coda_set_col_plan(1): widths in steps of 16;
+    (2): multiples of 64)."""
     def planned(mode):
         def f():
             B.coda_set_col_plan(mode)
@@ -367,17 +367,41 @@ def col_plan_ab(B, stream, barrier, call):
                 B.coda_set_col_plan(0)
         return f
 
-    def k_forward():
-        B.coda_set_serpentine_k(0)
-        try:
-            call()
-        finally:
-            B.coda_set_serpentine_k(1)
-    p16, p64 = planned(1), planned(2)
-    for f in (p16, p64, k_forward, call):
+    def k_order(serp):
+        def f():
+            old = B.coda_get_serpentine_k()
+            B.coda_set_serpentine_k(serp)
+            try:
+                call()
+            finally:
+                B.coda_set_serpentine_k(old)
+        return f
+    forms = {"col_plan_16": planned(1), "col_plan_64": planned(2), "k_forward": k_order(0),
+             "k_serpentine": k_order(1), "default": call}
+    for f in forms.values():
         f()
-    return alternating(stream, barrier, {"col_plan_16": p16, "col_plan_64": p64,
-                                         "k_forward": k_forward, "default": call})
+    return interleaved(stream, barrier, forms)
+
+
+def interleaved(stream, barrier, calls, n=40, seed=0):
+    """Median ms per call of each callable in `calls`, every call timed on its
+    own with CUDA events, the forms interleaved call by call in a fresh random
+    order each cycle (n cycles), so that neighbouring calls of different forms
+    see the same clock and power state and no form always follows the same
+    other form."""
+    names = list(calls)
+    rng = np.random.default_rng(seed)
+    evs = {k: [] for k in names}
+    barrier()
+    for _ in range(n):
+        for k in rng.permutation(names):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            calls[k]()
+            b.record(stream)
+            evs[k].append((a, b))
+    barrier()
+    return {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in evs.items()}
 
 
 def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
@@ -441,7 +465,7 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
             b_ms, _ = time_calls(B, stream, barrier, bwd_w, KW, 1)
             by_w[wn] = {"shape": [Mw, dw, Nw], "fwd_ms": f_ms, "fwd_tflops": tf(ww.fwd_flops, f_ms),
                         "dgrad_ms": b_ms, "dgrad_tflops": tf(ww.bwd_flops, b_ms), "calls": KW,
-                        "dgrad_col_plan_alternating_ms": col_plan_ab(B, stream, barrier, bwd_w)}
+                        "dgrad_variants_interleaved_ms": col_plan_ab(B, stream, barrier, bwd_w)}
             del gw, dyw, outw, wsw, wsb, dhw
         extras["other_llama_shapes"] = by_w
 
@@ -454,10 +478,10 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
             B.coda_bwd_dgrad(dy, g["W1"], h, r, g["gamma"], dh=dh, ws=ws_b, stream=stream)
         t = col_plan_ab(B, stream, barrier, bwd)
         extras["dgrad_col_plan"] = {
-            "alternating_ms": t, "tflops": {k: tf(w.bwd_flops, v) for k, v in t.items()},
-            "note": "coda_bwd_dgrad as by default (256-column tiles, every other wave loading K "
-                    "backwards) against K forwards in every wave and against the column plans "
-                    "(coda_set_col_plan(1), (2)), medians of alternating rounds"}
+            "interleaved_ms": t, "tflops": {k: tf(w.bwd_flops, v) for k, v in t.items()},
+            "note": "coda_bwd_dgrad as by default against K forwards in every wave and against "
+                    "the column plans (coda_set_col_plan(1), (2)), medians of calls interleaved one "
+                    "by one in a random order per cycle"}
         del ws_b
 
     if "fwd_fp8" in want:
@@ -626,16 +650,25 @@ def run_extras(B, args, w, g, dy, h, r, y, dh, ws_f, stream, barrier, rank):
                        stream=stream)
         warm(fwd_u)
         ms, k = time_calls(B, stream, barrier, fwd_u, KS, 3)
+        def fwd_f_whole():  # the fused forward with whole tiles only, as the unfused one runs
+            B.coda_set_split_tail(0)
+            try:
+                fwd_f()
+            finally:
+                B.coda_set_split_tail(1)
         warm(fwd_f)
-        t = alternating(stream, barrier, {"unfused": fwd_u, "fused": fwd_f})
+        warm(fwd_f_whole)
+        t = interleaved(stream, barrier, {"unfused": fwd_u, "fused": fwd_f, "fused_whole": fwd_f_whole})
         extras["fwd_unfused"] = {
             "ms": ms, "tflops": tf(w.fwd_flops, ms), "calls": KS, "gpu_launches": 3 * KS,
             "kernels_ms": {"gemm0_plain": k[0], "rmsnorm_rows": k[1], "gemm1_plain": k[2]},
-            "alternating_ms": {"unfused": t["unfused"], "coda_fwd": t["fused"]},
+            "interleaved_ms": {"unfused": t["unfused"], "coda_fwd": t["fused"],
+                               "coda_fwd_whole_tiles": t["fused_whole"]},
             "note": "coda_fwd_unfused: GEMM0 -> RMSNorm kernel (normalised tensor through HBM) "
-                    "-> GEMM1; the fused forward's comparison sequence. alternating_ms: medians of "
-                    "alternating rounds against coda_fwd, the comparison to read (absolute times "
-                    "of the separate extras depend on what ran before them)"}
+                    "-> GEMM1 (whole tiles); the fused forward's comparison sequence. "
+                    "interleaved_ms: per-call medians of calls interleaved one by one in a random "
+                    "order per cycle with coda_fwd with and without its split tail, the comparison "
+                    "to read (absolute times of the separate extras depend on what ran before them)"}
         del ws_u
 
     if "bwd_swiglu_dgrad" in want:

@@ -80,6 +80,7 @@ EXPORTS = {
     "coda_set_split_tail": (_st, [ctypes.c_int]),
     "coda_set_col_plan": (_st, [ctypes.c_int]),
     "coda_set_serpentine_k": (_st, [ctypes.c_int]),
+    "coda_get_serpentine_k": (ctypes.c_int, []),
     "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
                            _vp, _vp, _vp, _sz, _vp]),
@@ -347,9 +348,13 @@ def coda_set_col_plan(enable: int) -> None:
 
 
 def coda_set_serpentine_k(enable: int) -> None:
-    """1: the CTA-pair data gradients load every other wave's K blocks backwards (default);
-    0: forwards."""
+    """1: the CTA-pair data gradients load every other wave's K blocks backwards; 0: forwards
+    (default)."""
     _check(_lib.coda_set_serpentine_k(int(enable)), "coda_set_serpentine_k")
+
+
+def coda_get_serpentine_k() -> int:
+    return int(_lib.coda_get_serpentine_k())
 
 
 def coda_get_mma_mode() -> int:

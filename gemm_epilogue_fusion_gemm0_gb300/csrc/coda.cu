@@ -612,7 +612,7 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
 // 0: 256-column tiles; 1 (2): the data gradients may use narrower column tiles
 // whose widths are multiples of 16 (of 64)
 std::atomic<int> g_col_plan{0};
-std::atomic<int> g_dgrad_kserp{1};  // 1: the data gradients load every other wave's K backwards
+std::atomic<int> g_dgrad_kserp{0};  // 1: the data gradients load every other wave's K backwards
 
 // Most column tiles per row block the data-gradient workspace is sized for.
 int64_t dgrad_max_col_tiles(int64_t d) { return 2 * cdiv(d, kBN); }
@@ -1206,6 +1206,8 @@ coda_status_t coda_set_serpentine_k(int enable) {
   g_dgrad_kserp.store(enable);
   return CODA_OK;
 }
+
+int coda_get_serpentine_k(void) { return g_dgrad_kserp.load(); }
 
 coda_status_t coda_set_fold_rowreduce(int enable) {
   if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;

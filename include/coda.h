@@ -317,15 +317,17 @@ CODA_API coda_status_t coda_set_split_tail(int enable);
  * default.  Returns CODA_ERR_INVALID_ARG for any other value.  Process-wide. */
 CODA_API coda_status_t coda_set_col_plan(int enable);
 
-/* 1 (the default) makes the CTA-pair data gradients (coda_bwd_dgrad and launch
- * 1 of coda_bwd) load the K blocks of every other wave of tiles in reverse
- * order, so that a wave starts on the slices of W1 that the wave before it read
- * last, which the L2 still holds (each wave streams all of W1, 235 MB at
- * llama7b, through the 129 MB L2).  Measured on GB300: 1.3-1.7 % faster at the
- * llama1b and llama7b shapes, 4.8 % at llama70b.  Results differ only in fp32
- * summation order.  0 loads K forwards.  Returns CODA_ERR_INVALID_ARG for any
- * other value.  Process-wide. */
+/* 1 makes the CTA-pair data gradients (coda_bwd_dgrad and launch 1 of
+ * coda_bwd) load the K blocks of every other wave of tiles in reverse order, so
+ * that a wave starts on the slices of W1 that the wave before it read last
+ * (each wave streams all of W1, 235 MB at llama7b, through the 129 MB L2).
+ * Results differ only in fp32 summation order.  Measured on GB300 with calls
+ * of both orders interleaved one by one, it makes no difference (within
+ * +-0.5 % at the llama1b, llama7b and llama70b shapes), so 0, K forwards, is
+ * the default.  Returns CODA_ERR_INVALID_ARG for any other value.
+ * coda_get_serpentine_k returns the current setting.  Process-wide. */
 CODA_API coda_status_t coda_set_serpentine_k(int enable);
+CODA_API int coda_get_serpentine_k(void);
 
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records
