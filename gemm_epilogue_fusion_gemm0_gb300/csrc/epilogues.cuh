@@ -74,9 +74,10 @@ __device__ __forceinline__ void stg8(__nv_bfloat16* p, const uint32_t (&w)[4]) {
   *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// p[n .. n + 8), or zeros at or past `limit` (the end of the row)
-__device__ __forceinline__ Chunk8 ldg8_or0(const __nv_bfloat16* p, int n, int limit) {
-  return n < limit ? ldg8(p + n) : Chunk8{{0u, 0u, 0u, 0u}};
+// p[n .. n + 8), or zeros at or past `limit` (the end of the tile's columns);
+// p holds `total` elements (checked in the checked build)
+__device__ __forceinline__ Chunk8 ldg8_or0(const __nv_bfloat16* p, int n, int limit, int total) {
+  return n < limit && checked(n + 8 <= total, kChkLoad) ? ldg8(p + n) : Chunk8{{0u, 0u, 0u, 0u}};
 }
 
 // ---------------------------------------------------------------------------
@@ -279,7 +280,7 @@ struct EpiResidualGammaSumsq : EpiDefaultCols {
       Stage64::get(buf0, zr);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend, c.N);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float h0 = __uint_as_float(v[g * 8 + 2 * e]) + bf16lo(zr[4 * g + e]);
@@ -461,7 +462,7 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
       __syncwarp();  // every lane has its row before the buffer is refilled
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend, c.N);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           qp = fmaf(__uint_as_float(v[g * 8 + 2 * e]) * bf16lo(gg.w[e]), bf16lo(hr[4 * g + e]), qp);
@@ -524,7 +525,7 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
       float t[32];  // r * h * grad_h2: this row's contribution to dgamma (kExtras)
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend, c.N);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float a0 = __uint_as_float(v[g * 8 + 2 * e]);
@@ -769,7 +770,7 @@ struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
       Stage64::get(c.stage, hr);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend, c.N);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float d0 = rr * bf16lo(gg.w[e]) * __uint_as_float(v[g * 8 + 2 * e]) -
@@ -840,7 +841,7 @@ struct EpiResidualGammaSumsqFp8 : EpiDefaultCols {
       Stage64::get(buf0, zr);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend);
+        const Chunk8 gg = ldg8_or0(p.gamma, n0 + g * 8, c.nend, c.N);
         float q[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -32,9 +32,10 @@ __device__ uint32_t g_coda_status = 0;  // device status word (see WaitSite)
 
 // ---------------------------------------------------------------------------
 // Checked build (compiled with -DCODA_CHECKED, libcoda_checked.so): every
-// global access of the epilogues is checked against the extent of the tensor
-// it belongs to, every TMA box start against its tensor map's extent and the
-// 16-byte alignment of its innermost coordinate, and every index into the
+// staged load and store of a rank-2 tensor in the epilogues is checked against
+// the extent of the tensor it belongs to (and every vector load of gamma
+// against its length), every TMA box start against its tensor map's extent and
+// the 16-byte alignment of its innermost coordinate, and every index into the
 // workspace (partial sums, completion flags, split-tail slots) against the
 // size the host gave it.  A failed check records 0x200 | site in the status
 // word (first failure wins; coda_get_device_status reports

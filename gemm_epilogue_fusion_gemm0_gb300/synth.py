@@ -86,6 +86,19 @@ def make_grad_output(rng_or_seed, M: int, N1: int) -> torch.Tensor:
     return to_bf16(_normal(rng, (M, N1), 1e-2))
 
 
+def make_dgrad_inputs(M: int, d: int, N1: int, seed: int = 0) -> dict:
+    """bf16 CPU tensors for a data gradient on its own, without running a
+    forward: h [M, d] ~ N(0, 2) (the spread of x @ W0 + z with the forward's
+    distributions), W1 [d, N1] ~ N(0, 1/d), gamma [d] = 1 + N(0, 0.1) and
+    dy [M, N1] ~ N(0, 1e-2), drawn in that order from default_rng(seed)."""
+    rng = np.random.default_rng(seed)
+    h = to_bf16(_normal(rng, (M, d), 2.0))
+    W1 = to_bf16(_normal(rng, (d, N1), 1.0 / d))
+    gamma = to_bf16(1.0 + _normal(rng, (d,), 0.1))
+    dy = to_bf16(_normal(rng, (M, N1), 1e-2))
+    return {"h": h, "W1": W1, "gamma": gamma, "dy": dy}
+
+
 def make_residual_grad(rng, M: int, d: int) -> torch.Tensor:
     """bf16 CPU tensor dh_res [M, d] ~ N(0, 1e-2): the gradient reaching h
     through the residual stream; drawn after dy from the same generator."""

@@ -273,8 +273,8 @@ CODA_API coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const c
  * status word: CODA_OK, CODA_ERR_DEVICE_TIMEOUT if a bounded wait in any
  * kernel of this library ran out since the last call (raw code 0x100 | which
  * wait), or, in the checked build (libcoda_checked.so, compiled with
- * -DCODA_CHECKED: every epilogue global access, TMA box start and workspace
- * index checked on the device), CODA_ERR_DEVICE_BOUNDS if a check failed and
+ * -DCODA_CHECKED: every staged epilogue load and store, gamma load, TMA box
+ * start and workspace index checked on the device), CODA_ERR_DEVICE_BOUNDS if a check failed and
  * its access was skipped (raw code 0x200 | which check).  The first failure
  * since the last call is kept.  If `detail` is not NULL it receives the raw
  * code (0 = none).  Returns CODA_ERR_LAUNCH if the stream itself reports a

@@ -2,8 +2,8 @@
 
 Run by tests/test_checked_build.py in a child process with
 CODA_CHECKED_BUILD=1, so that the binding loads the library compiled with
--DCODA_CHECKED: every epilogue global access, TMA box start and workspace
-index is checked on the device, and a failed check records
+-DCODA_CHECKED: every staged epilogue load and store, gamma load, TMA box
+start and workspace index is checked on the device, and a failed check records
 CODA_ERR_DEVICE_BOUNDS in the status word instead of touching memory.  Every
 case below compares with the fp64 oracle (the parity tests' own helpers and
 tolerances) and then requires a clean status word.  Prints one line per case

@@ -1,10 +1,10 @@
 """The checked build (libcoda_checked.so, compiled with -DCODA_CHECKED).
 
-Every global access of the epilogues is checked against its tensor's extent,
-every TMA box start against its tensor map's extent and the 16-byte alignment
-of its innermost coordinate, and every workspace index against its size; a
-failed check records CODA_ERR_DEVICE_BOUNDS and skips the access, it never
-traps.  The GPU test runs the small, ragged, split-tail, column-plan and
+Every staged load and store of the epilogues (and every gamma load) is checked
+against its tensor's extent, every TMA box start against its tensor map's
+extent and the 16-byte alignment of its innermost coordinate, and every
+workspace index against its size; a failed check records
+CODA_ERR_DEVICE_BOUNDS and skips the access, it never traps.  The GPU test runs the small, ragged, split-tail, column-plan and
 no-allocation parity cases against that library in a child process (the
 binding picks the library when the process starts) and requires every case to
 match the oracle with a clean status word.  The CPU test checks that the

@@ -770,6 +770,38 @@ def test_entry_points_replay_from_a_cuda_graph(B, entry):
         assert torch.equal(v, ref[k]), k
 
 
+# ----------------------------------------------------------------------------- the dgrad's column-tile ceiling
+def test_dgrad_at_the_column_tile_ceiling(B, mode):
+    """The cross-tile data gradient needs every column tile of a row block in
+    flight together: d up to 256 x (resident CTA pairs) in CTA-pair mode, 256 x
+    SMs in single-CTA mode.  At that d it matches the oracle (h and r given, r
+    from the oracle's own RMS of h); 8 columns more are refused before any
+    launch with CODA_ERR_UNSUPPORTED_SHAPE."""
+    dev = torch.device("cuda:0")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = sms // 2 if mode == 1 else sms
+    M, d, N1, eps = (256 if mode == 1 else 128), 256 * units, 512, 1e-5
+    t = synth.make_dgrad_inputs(M, d, N1, seed=7)
+    r = oracle.inverse_rms(oracle.mean_square(f64(t["h"])), eps).astype(np.float32)
+    g = {k: v.to(dev) for k, v in t.items()}
+    rg = torch.from_numpy(r).to(dev)
+    dh = B.coda_bwd_dgrad(g["dy"], g["W1"], g["h"], rg, g["gamma"])
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    bref = oracle.backward_dgrad(f64(t["dy"]), f64(t["W1"]), f64(t["h"]), r.astype(np.float64),
+                                 f64(t["gamma"]))
+    check("dh", f64(dh), bref.dh, TOL_DH)
+    # one 8-column step past the ceiling: refused, nothing launched
+    d2 = d + 8
+    h2 = torch.zeros((M, d2), dtype=torch.bfloat16, device=dev)
+    W2 = torch.zeros((d2, N1), dtype=torch.bfloat16, device=dev)
+    gm2 = torch.ones((d2,), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(B.CodaError) as e:
+        B.coda_bwd_dgrad(g["dy"], W2, h2, rg, gm2)
+    assert e.value.status == B.CODA_ERR_UNSUPPORTED_SHAPE
+    assert B.coda_get_device_status() == (B.CODA_OK, 0)
+
+
 # ----------------------------------------------------------------------------- element offsets past 2^31
 def test_large_batch_element_offsets_past_int32(B, mode):
     """81920 tokens at the llama7b widths: y and dy hold 2.35e9 elements, more

@@ -64,3 +64,18 @@ def test_device_generator_shapes_determinism_and_distributions():
     assert abs(std["W0"] - 256 ** -0.5) < 0.003 and abs(std["W1"] - 256 ** -0.5) < 0.003
     assert abs(std["dy"] - 0.1) < 0.003
     assert abs(float(a["gamma"].float().mean()) - 1.0) < 0.06 and abs(std["gamma"] - 0.1 ** 0.5) < 0.06
+
+
+def test_dgrad_input_generator():
+    """make_dgrad_inputs: shapes, dtypes, seeding and the stated distributions."""
+    a = synth.make_dgrad_inputs(512, 256, 384, seed=9)
+    b = synth.make_dgrad_inputs(512, 256, 384, seed=9)
+    shapes = {"h": (512, 256), "W1": (256, 384), "gamma": (256,), "dy": (512, 384)}
+    for k, shp in shapes.items():
+        assert tuple(a[k].shape) == shp and a[k].dtype == torch.bfloat16, k
+        assert torch.equal(a[k], b[k]), k
+    f = lambda k: a[k].to(torch.float64).numpy()
+    assert abs(f("h").std() - 2.0 ** 0.5) < 0.03 and abs(f("h").mean()) < 0.03
+    assert abs(f("W1").std() - (1 / 256) ** 0.5) < 0.003
+    assert abs(f("gamma").mean() - 1.0) < 0.08
+    assert abs(f("dy").std() - 0.1) < 0.003
