@@ -687,35 +687,20 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
     const size_t pitch = 2 * static_cast<size_t>(half) * 2;
     const uint32_t buf0 = c.stage, buf1 = c.stage + Stage64::kBytes;
     float ss = 0.f;
-    // The saved g and u blocks of a chunk are fetched together, and the next
-    // chunk's while the current one is processed, so their global-load
-    // latencies overlap instead of adding up.
-    const size_t rbase = static_cast<size_t>(wr.row0) * (2 * static_cast<size_t>(half));
-    const int jbase = c.n0 + c.half * kHalfCols;
-    uint4 gf[Stage64::kGroups], uf[Stage64::kGroups];
-    Stage64::fetch(gf, p.y + rbase + jbase, pitch, wr.rows, valid_bytes(jbase, c.nend, 2),
-                   span(p.y, c.M, pitch));
-    Stage64::fetch(uf, p.y + rbase + jbase + half, pitch, wr.rows, valid_bytes(jbase, c.nend, 2),
-                   span(p.y, c.M, pitch));
 #pragma unroll 1
     for (int ch = 0; ch < kHalfChunks; ++ch) {
       const int col = c.half * kHalfCols + ch * 32;
       const int j0 = c.n0 + col;
       const int valid = valid_bytes(j0, c.nend, 2);
-      const size_t off = rbase + j0;
-      Stage64::deposit(buf0, gf);
-      Stage64::deposit(buf1, uf);
-      if (ch + 1 < kHalfChunks) {
-        const int vn = valid_bytes(j0 + 32, c.nend, 2);
-        Stage64::fetch(gf, p.y + off + 32, pitch, wr.rows, vn, span(p.y, c.M, pitch));
-        Stage64::fetch(uf, p.y + off + 32 + half, pitch, wr.rows, vn, span(p.y, c.M, pitch));
-      }
+      const size_t off = static_cast<size_t>(wr.row0) * (2 * static_cast<size_t>(half)) + j0;
+      Stage64::load(buf0, p.y + off, pitch, wr.rows, valid, span(p.y, c.M, pitch));
+      Stage64::load(buf1, p.y + off + half, pitch, wr.rows, valid, span(p.y, c.M, pitch));
       uint32_t v[32];
       tmem_ld32(c.taddr + col, v);
       tmem_ld_wait(v);
       mask_chunk(v, j0, c.nend);
       __syncwarp();
-      uint32_t gr[16], ur[16];  // g, u in; dg, du out (in place)
+      uint32_t gr[16], ur[16], dgw[16], duw[16];
       Stage64::get(buf0, gr);
       Stage64::get(buf1, ur);
 #pragma unroll
@@ -732,11 +717,11 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
           ss = fmaf(dgv[k], g, ss);  // da is zero past the last row and column
           ss = fmaf(duv[k], u, ss);
         }
-        gr[e] = pack_bf16x2(dgv[0], dgv[1]);
-        ur[e] = pack_bf16x2(duv[0], duv[1]);
+        dgw[e] = pack_bf16x2(dgv[0], dgv[1]);
+        duw[e] = pack_bf16x2(duv[0], duv[1]);
       }
-      Stage64::put(buf0, gr);
-      Stage64::put(buf1, ur);
+      Stage64::put(buf0, dgw);
+      Stage64::put(buf1, duw);
       __syncwarp();
       Stage64::flush(buf0, p.dy_out + off, pitch, wr.rows, valid, span(p.dy_out, c.M, pitch));
       Stage64::flush(buf1, p.dy_out + off + half, pitch, wr.rows, valid, span(p.dy_out, c.M, pitch));
