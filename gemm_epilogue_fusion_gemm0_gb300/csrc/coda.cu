@@ -445,8 +445,9 @@ SkRegion sk_region(void* base, int64_t tiles) {
 }
 
 // Whole tiles for the first W - 1 waves, the last U + R tiles split along K
-// (gemm_pair.cuh).  The split costs a cooperative launch with a grid barrier
-// (2-4 us) and, per pair, a partial written or added and sometimes a wait for
+// (gemm_pair.cuh).  The split costs a cooperative launch (measured at 2-4 us
+// when it still ended with a grid barrier) and, per pair, a partial written or
+// added and sometimes a wait for
 // a TMEM buffer; it gains the idle share of the last wave, (U - R) / U of a
 // tile.  Measured on GB300 it pays for the llama7b and llama70b GEMM1 (R/U =
 // 0.16, 64 and 128 k-blocks per tile) and loses when the last wave is mostly

@@ -770,6 +770,37 @@ def test_entry_points_replay_from_a_cuda_graph(B, entry):
         assert torch.equal(v, ref[k]), k
 
 
+# ----------------------------------------------------------------------------- workspace with any contents
+def test_dgrad_workspace_with_random_contents(B, mode):
+    """The data gradient on a workspace filled with random bytes: the first
+    launch counts its blocks out through the 128-bit compare-and-swap (no
+    marker yet), leaves the marker and a zeroed count in the launch counter's
+    slot and advances the counter by one; the second uses the prepared count.
+    Both match the oracle."""
+    dev = torch.device("cuda:0")
+    M, d, N1 = 640, 512, 1280
+    t = synth.make_forward_inputs(M, d, N1, seed=17)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    h, r, _ = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5)
+    dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
+    dy = dy_cpu.to(dev)
+    nb = B.coda_bwd_dgrad_workspace_bytes(M, d, N1)
+    gen = torch.Generator(device="cpu").manual_seed(99)
+    ws = torch.randint(0, 256, (nb,), dtype=torch.uint8, generator=gen).to(dev)
+    slot = lambda: ws[nb - 256:nb - 208].view(torch.int64).cpu()  # slot words 0..5
+    e0 = int(slot()[0])
+    bref = oracle.backward_dgrad(f64(dy_cpu), f64(t["W1"]), f64(h), f64(r), f64(t["gamma"]))
+    for call in (1, 2):
+        dh = B.coda_bwd_dgrad(dy, g["W1"], h, r, g["gamma"], ws=ws)
+        st, detail = B.coda_get_device_status()
+        assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+        w = slot()
+        assert (int(w[0]) - e0) % 2 ** 64 == call, (call, int(w[0]), e0)
+        assert int(w[1]) & (2 ** 64 - 1) == 0xC0DA5107C0DA5107  # the count is prepared
+        assert int(w[2]) == 0  # and zeroed for the next launch
+        check(f"dh (call {call})", f64(dh), bref.dh, TOL_DH)
+
+
 # ----------------------------------------------------------------------------- the dgrad's column-tile ceiling
 def test_dgrad_at_the_column_tile_ceiling(B, mode):
     """The cross-tile data gradient needs every column tile of a row block in
