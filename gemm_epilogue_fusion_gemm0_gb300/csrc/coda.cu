@@ -11,10 +11,12 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <random>
 #include <tuple>
 #include <vector>
 
@@ -239,6 +241,29 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every workspace starts with the 256-byte slot of the launch counter that the
+// completion flags' tokens come from (launch_exit in ptx.cuh); no layout puts
+// data there, so calls of any shape and entry point may share one buffer.
+constexpr size_t kSlotBytes = 256;
+
+// A fresh random 64-bit value per call, mixed into its completion flags: the
+// SplitMix64 output function (Steele, Lea and Flood, "Fast splittable
+// pseudorandom number generators", OOPSLA 2014) applied to a per-process seed
+// plus a counter.
+uint64_t next_salt() {
+  static const uint64_t seed = [] {
+    std::random_device rd;
+    const uint64_t t = static_cast<uint64_t>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+    return (static_cast<uint64_t>(rd()) << 32) ^ rd() ^ t;
+  }();
+  static std::atomic<uint64_t> counter{0};
+  uint64_t z = seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 // First use of the library on the current device (once per device, under a
 // lock): checks the device, sets the kernels' shared-memory limits (which loads
 // the library's device code on this device, the static scratch array of the
@@ -422,7 +447,7 @@ int64_t sk_slots(int64_t tiles) { return std::min<int64_t>(tiles, 2 * kSkMaxPair
 size_t sk_region_bytes(int64_t tiles) {
   const int64_t slots = sk_slots(tiles);
   return align256(static_cast<size_t>(slots) * 2 * kSkSlotFloats * 4) +
-         align256(static_cast<size_t>(slots) * 2 * 8) + 256;
+         align256(static_cast<size_t>(slots) * 2 * 8);
 }
 
 struct SkRegion {
@@ -432,15 +457,15 @@ struct SkRegion {
   int64_t slots = 0;
 };
 
-SkRegion sk_region(void* base, int64_t tiles) {
+// `slot`: the workspace's launch-counter slot (its first 256 bytes).
+SkRegion sk_region(void* base, int64_t tiles, void* slot) {
   SkRegion r;
   r.slots = sk_slots(tiles);
   char* p = static_cast<char*>(base);
   r.part = reinterpret_cast<float*>(p);
   p += align256(static_cast<size_t>(r.slots) * 2 * kSkSlotFloats * 4);
   r.flags = reinterpret_cast<uint64_t*>(p);
-  p += align256(static_cast<size_t>(r.slots) * 2 * 8);
-  r.epoch = reinterpret_cast<uint64_t*>(p);
+  r.epoch = static_cast<uint64_t*>(slot);
   return r;
 }
 
@@ -454,7 +479,8 @@ SkRegion sk_region(void* base, int64_t tiles) {
 // full (GEMM0 there, R/U = 0.74) or tiles are short (llama1b, 32 k-blocks).  So:
 // split only when R <= U / 2 and a tile has at least 64 k-blocks, with at
 // least two waves and enough slots.
-SkParams plan_split_tail(const SkRegion& reg, int64_t num_tiles, int npairs, int64_t nk) {
+SkParams plan_split_tail(const SkRegion& reg, int64_t num_tiles, int npairs, int64_t nk,
+                         uint64_t salt) {
   SkParams sk = kNoSplitTail;
   if (g_split_tail.load() == 0 || reg.part == nullptr || npairs < 1 || npairs > kSkMaxPairs)
     return sk;
@@ -465,6 +491,7 @@ SkParams plan_split_tail(const SkRegion& reg, int64_t num_tiles, int npairs, int
   sk.flags = reg.flags;
   sk.epoch = reg.epoch;
   sk.slots = static_cast<int>(reg.slots);
+  sk.salt = salt;
   return sk;
 }
 
@@ -479,11 +506,12 @@ int64_t fwd_pair_tiles(int64_t M, int64_t d, int64_t N1) {
   return cdiv(M, kPairBM) * std::max(cdiv(d, kBN), cdiv(N1, kBN));
 }
 
+// [slot | act | partials | split-tail region]
 size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t N1, bool fused) {
   const size_t act = align256(static_cast<size_t>(M) * d * 2);
   const size_t part = fused ? align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4) : 0;
   const size_t sk = fused ? sk_region_bytes(fwd_pair_tiles(M, d, N1)) : 0;
-  return act + part + sk;
+  return kSlotBytes + act + part + sk;
 }
 
 enum class FwdKind { kFused, kUnfused, kFusedSwiGLU };
@@ -515,14 +543,16 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   const bool pair = g_mma_mode.load() == 1;
 
   FwdWorkspace ws;
-  ws.act = reinterpret_cast<__nv_bfloat16*>(workspace);
-  ws.part = fused ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+  char* const wsb = static_cast<char*>(workspace);
+  ws.act = reinterpret_cast<__nv_bfloat16*>(wsb + kSlotBytes);
+  ws.part = fused ? reinterpret_cast<float*>(wsb + kSlotBytes +
                                              align256(static_cast<size_t>(M) * d * 2))
                   : nullptr;
   if (fused)
-    ws.sk = sk_region(static_cast<char*>(workspace) + align256(static_cast<size_t>(M) * d * 2) +
+    ws.sk = sk_region(wsb + kSlotBytes + align256(static_cast<size_t>(M) * d * 2) +
                           align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4),
-                      fwd_pair_tiles(M, d, N1));
+                      fwd_pair_tiles(M, d, N1), wsb);
+  const uint64_t salt = next_salt();
 
   CUtensorMap mA0, mB0, mA1, mB1;
   bool ok = tmap_2d(&mA0, x, d, M, kBK, kBM);           // x  [M, d]  K-major
@@ -547,8 +577,8 @@ coda_status_t fwd_impl(FwdKind kind, const coda_bf16* x, const coda_bf16* W0, co
   const int mtp = static_cast<int>(cdiv(M, kPairBM));
   const int64_t nkb = cdiv(d, kBK);  // k-blocks of both GEMMs (K = d)
   const int np0 = std::min(max_pairs, mtp * nt0), np1 = std::min(max_pairs, mtp * nt1);
-  const SkParams sk0 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt0, np0, nkb);
-  const SkParams sk1 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt1, np1, nkb);
+  const SkParams sk0 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt0, np0, nkb, salt);
+  const SkParams sk1 = plan_split_tail(ws.sk, static_cast<int64_t>(mtp) * nt1, np1, nkb, salt);
   cudaError_t e =
       pair ? launch(kPairGemm0, 2 * np0, kThreads, kPairGemm0Smem, stream, sk0.epoch != nullptr,
                     mA0, mB0, Mi, di, di, kPairGroupM, p0, sk0, kNoColPlan, tmo)
@@ -627,19 +657,20 @@ struct DgradWs {
   uint64_t* epoch;
 };
 
+// [slot | qpart | flags]
 size_t dgrad_ws_bytes(int64_t M, int64_t d) {
   const int64_t slabs = 2 * cdiv(M, kPairBM), nt = dgrad_max_col_tiles(d);
-  return align256(static_cast<size_t>(2 * nt) * M * 4) +
-         align256(static_cast<size_t>(slabs) * nt * 8) + 256;
+  return kSlotBytes + align256(static_cast<size_t>(2 * nt) * M * 4) +
+         align256(static_cast<size_t>(slabs) * nt * 8);
 }
 
 DgradWs dgrad_ws(void* base, int64_t M, int64_t d) {
   char* p = static_cast<char*>(base);
   DgradWs w;
-  w.qpart = reinterpret_cast<float*>(p);
+  w.epoch = reinterpret_cast<uint64_t*>(p);
+  w.qpart = reinterpret_cast<float*>(p + kSlotBytes);
   w.flags = reinterpret_cast<uint64_t*>(
-      p + align256(static_cast<size_t>(2 * dgrad_max_col_tiles(d)) * M * 4));
-  w.epoch = reinterpret_cast<uint64_t*>(p + dgrad_ws_bytes(M, d) - 256);
+      p + kSlotBytes + align256(static_cast<size_t>(2 * dgrad_max_col_tiles(d)) * M * 4));
   return w;
 }
 
@@ -808,6 +839,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   p.qpart = dw.qpart;
   p.flags = dw.flags;
   p.epoch = dw.epoch;
+  p.salt = next_salt();
   cudaError_t e =
       pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p, kNoSplitTail,
@@ -825,7 +857,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
 
 size_t coda_fwd_fp8_workspace_bytes(int64_t M, int64_t d, int64_t N1) {
   if (check_common(M, d, N1) != CODA_OK || M == 0) return 0;
-  return align256(static_cast<size_t>(M) * d) +
+  return kSlotBytes + align256(static_cast<size_t>(M) * d) +
          align256(static_cast<size_t>(2 * cdiv(d, kBN)) * M * 4);
 }
 
@@ -855,8 +887,8 @@ coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t* W0_q, fl
   if (st != CODA_OK) return st;
   const uint64_t tmo = g_timeout_ns.load();
   const int Mi = static_cast<int>(M), di = static_cast<int>(d), N1i = static_cast<int>(N1);
-  uint8_t* hq = static_cast<uint8_t*>(workspace);
-  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+  uint8_t* hq = static_cast<uint8_t*>(workspace) + kSlotBytes;
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kSlotBytes +
                                          align256(static_cast<size_t>(M) * d));
 
   CUtensorMap mA0, mB0, mA1, mB1;
@@ -964,7 +996,8 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
       sk_region(rest + align256(static_cast<size_t>(M) * d * 2) +
                     align256(static_cast<size_t>(4 * std::max(2 * cdiv(M, kPairBM), cdiv(M, kBM))) *
                              d * 4),
-                bwd_pair_tiles(M, d, N1));
+                bwd_pair_tiles(M, d, N1), dw.epoch);
+  const uint64_t salt = next_salt();
 
   const uint32_t bbox = pair ? 128 : kBN;
   CUtensorMap mDy, mW1, mH2, mDyMN, mDh, mW0, mX, mDhMN;
@@ -987,6 +1020,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.qpart = dw.qpart;
   p.flags = dw.flags;
   p.epoch = dw.epoch;
+  p.salt = salt;
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
@@ -1014,7 +1048,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   const int ntw1 = static_cast<int>(cdiv(N1, kBN));
   const int64_t nkw = cdiv(M, kBK);  // k-blocks of the weight gradients (K = tokens)
   const int npw1 = std::min(max_pairs, mtw * ntw1);
-  const SkParams skw1 = plan_split_tail(skr, static_cast<int64_t>(mtw) * ntw1, npw1, nkw);
+  const SkParams skw1 = plan_split_tail(skr, static_cast<int64_t>(mtw) * ntw1, npw1, nkw, salt);
   e = pair ? launch(kPairWgrad, 2 * npw1, kThreads, kPairWgradSmem, stream, skw1.epoch != nullptr,
                     mH2, mDyMN, di, N1i, Mi, kPairGroupM, pw1, skw1, kNoColPlan, tmo)
            : launch(kWgrad, std::min(sms, mtw * ntw1), kThreads, kWgradSmem, stream, false, mH2,
@@ -1030,7 +1064,8 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   px.y_out = reinterpret_cast<__nv_bfloat16*>(dx_out);
   const int mtx = static_cast<int>(cdiv(M, pair ? kPairBM : kBM));
   const int npx = std::min(max_pairs, mtx * nt);
-  const SkParams skx = plan_split_tail(skr, static_cast<int64_t>(mtx) * nt, npx, cdiv(d, kBK));
+  const SkParams skx =
+      plan_split_tail(skr, static_cast<int64_t>(mtx) * nt, npx, cdiv(d, kBK), salt);
   e = pair ? launch(kPairXgrad, 2 * npx, kThreads, kPairXgradSmem, stream, skx.epoch != nullptr,
                     mDh, mW0, Mi, di, di, kPairGroupM, px, skx, kNoColPlan, tmo)
            : launch(kXgrad, std::min(sms, mtx * nt), kThreads, kXgradSmem, stream, false, mDh,
@@ -1044,7 +1079,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   EpiStoreF32::Params pw0 = {};
   pw0.out = dW0_out;
   const int npw0 = std::min(max_pairs, mtw * nt);
-  const SkParams skw0 = plan_split_tail(skr, static_cast<int64_t>(mtw) * nt, npw0, nkw);
+  const SkParams skw0 = plan_split_tail(skr, static_cast<int64_t>(mtw) * nt, npw0, nkw, salt);
   e = pair ? launch(kPairWgrad, 2 * npw0, kThreads, kPairWgradSmem, stream, skw0.epoch != nullptr,
                     mX, mDhMN, di, di, Mi, kPairGroupM, pw0, skw0, kNoColPlan, tmo)
            : launch(kWgrad, std::min(sms, mtw * nt), kThreads, kWgradSmem, stream, false, mX,
@@ -1059,7 +1094,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
 
 size_t coda_bwd_swiglu_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1, int64_t Dout) {
   if (check_common(M, d, N1) != CODA_OK || Dout <= 0 || M == 0) return 0;
-  return align256(static_cast<size_t>(2 * cdiv(N1 / 2, kBN)) * M * 4);
+  return kSlotBytes + align256(static_cast<size_t>(2 * cdiv(N1 / 2, kBN)) * M * 4);
 }
 
 coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, const coda_bf16* y,
@@ -1109,7 +1144,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   EpiSwiGLUBackward::Params p0 = {};
   p0.y = reinterpret_cast<const __nv_bfloat16*>(y);
   p0.dy_out = reinterpret_cast<__nv_bfloat16*>(dy_out);
-  p0.spart = reinterpret_cast<float*>(workspace);
+  p0.spart = reinterpret_cast<float*>(static_cast<char*>(workspace) + kSlotBytes);
   cudaError_t e =
       pair ? launch(kPairSwigluBwd, 2 * std::min(max_pairs, mtp * nts), kThreads,
                     kPairSwigluBwdSmem, stream, false, mA0, mB0, Mi, halfi, Douti, kPairGroupM,
@@ -1287,6 +1322,7 @@ extern "C" coda_status_t coda_bwd_dgrad_noalloc(const coda_bf16* dy, const coda_
   p.qpart = reinterpret_cast<float*>(scratch);
   p.flags = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(scratch) + kNoAllocFlagOffset);
   p.epoch = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(scratch) + kNoAllocEpochOffset);
+  p.salt = next_salt();
   cudaError_t e = launch(kDgrad, grid, kThreads, kDgradSmem, stream, true, mA, mB,
                          static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                          g_timeout_ns.load());

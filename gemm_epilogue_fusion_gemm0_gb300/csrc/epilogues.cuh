@@ -391,11 +391,13 @@ struct EpiRowScale : EpiDefaultCols {
 // needs every block of the launch resident (cooperative launch) and tiles in
 // row-major order with at most gridDim.x column tiles per row; then every wait
 // depends only on tiles with smaller index and cannot deadlock.
-// The token is epoch + 1, epoch being a counter in the caller's workspace that
-// the launch reads and that the last of its blocks to finish advances by one
-// (launch_exit).  Flags left by an earlier launch hold an older token, so the
-// workspace never needs clearing, and a launch replayed from a CUDA graph draws
-// a fresh token each time.
+// A flag holds (epoch + 1) ^ salt: epoch is the launch counter at the start of
+// the caller's workspace, which the last of the launch's blocks to finish
+// advances by one (launch_exit), and salt a random value the host draws for
+// each call.  Flags left by an earlier launch on the same counter hold an older
+// token, and anything else in the buffer matches only by a 2^-64 coincidence,
+// so the workspace never needs clearing, and a launch replayed from a CUDA
+// graph draws a fresh token each time.
 // ---------------------------------------------------------------------------
 // kExtras: the full backward's additions (dh_res, h2, dgamma partials) are
 // compiled in; the plain data gradient leaves them out and keeps fewer registers.
@@ -412,6 +414,7 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
     float* qpart;     // [2 * nt][M]
     uint64_t* flags;  // [mt][nt]
     uint64_t* epoch;  // launch counter (any initial value); this launch's token is *epoch + 1
+    uint64_t salt;    // this call's random value; a flag holds token ^ salt
     // Extras of the full backward (read only with kExtras):
     const __nv_bfloat16* dh_res;  // [M, d] gradient reaching h through the residual, or null
     __nv_bfloat16* h2_out;        // [M, d] normalised activation r * h * gamma (dW1's operand)
@@ -420,7 +423,7 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
 
   // This block reads no flag any more: count it out of the launch; the last
   // block to finish advances the epoch.
-  static __device__ __forceinline__ void at_exit(const Params& p) { launch_exit(p.epoch); }
+  static __device__ __forceinline__ void at_exit(const Params& p) { launch_exit(p.epoch, p.salt); }
 
   static __device__ __forceinline__ void apply(const Params& p, const WaitCtl& wc,
                                                const TileCtx& c) {
@@ -480,11 +483,11 @@ struct EpiRmsNormBackwardT : EpiDefaultCols {
     // 128-row slabs the flags cover: two per 256-row block (CTA-pair tiles)
     const bool flags_ok = checked(c.mb < 2 * ((c.M + 255) / 256) && c.nb < c.nt, kChkFlag);
     if (threadIdx.x == kEpiFirstThread && flags_ok) {
-      const uint64_t token = *reinterpret_cast<volatile uint64_t*>(p.epoch) + 1;
+      const uint64_t tag = launch_tag(p.epoch, p.salt);
       __threadfence();
-      st_release_gpu_u64(row_flags + c.nb, token);
+      st_release_gpu_u64(row_flags + c.nb, tag);
       for (int j = 0; j < c.nt; ++j)
-        if (!flag_wait(row_flags + j, token, wc, kSiteRowFlags)) break;
+        if (!flag_wait(row_flags + j, tag, wc, kSiteRowFlags)) break;
       __threadfence();
     }
     named_bar_sync(1, kEpiThreads);

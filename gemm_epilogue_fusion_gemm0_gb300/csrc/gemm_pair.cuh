@@ -61,9 +61,11 @@ static_assert(kPairSmemBytes <= 232448, "exceeds the 227 KB per-block shared mem
 // its TMEM accumulator and runs the policy on the sum.  A partial is always its
 // pair's first tail item and waits for nothing but its own data, so the owner's
 // wait always ends.
-// The flag token is *epoch + 1, epoch being a counter in the caller's workspace
-// that the last block of the launch to finish advances (launch_exit): flags of
-// earlier launches never match, so the slots need no clearing and a launch
+// A flag holds (*epoch + 1) ^ salt, epoch being the launch counter at the start
+// of the caller's workspace, which the last block of the launch to finish
+// advances (launch_exit), and salt a random value the host draws for each call:
+// flags of earlier launches on the counter never match and other contents match
+// only by a 2^-64 coincidence, so the slots need no clearing and a launch
 // replayed from a CUDA graph draws a fresh token.  The owner's wait needs the
 // other pair resident, so such a launch is cooperative.
 // Policies whose epilogue waits on other tiles (the data gradient's row flags)
@@ -75,9 +77,10 @@ struct SkParams {
   uint64_t* flags;  // [S][2 CTAs]
   uint64_t* epoch;  // launch counter (any initial value); null when the tail is not split
   int slots;        // S, the partial slots the workspace holds
+  uint64_t salt;    // this call's random value; a flag holds token ^ salt
 };
 
-constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr, 0};
+constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr, 0, 0};
 
 // A policy opts out of the split tail (its epilogue waits on other tiles) with
 // `static constexpr bool kSplitTail = false;`; the kernel then compiles without it.
@@ -505,13 +508,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __threadfence();
           named_bar_sync(1, kEpiThreads);
           if (threadIdx.x == kEpiFirstThread) {
-            const uint64_t token = *reinterpret_cast<volatile uint64_t*>(sk.epoch) + 1;
-            st_release_gpu_u64(flag, token);
+            st_release_gpu_u64(flag, launch_tag(sk.epoch, sk.salt));
           }
         } else {
           if (threadIdx.x == kEpiFirstThread) {
-            const uint64_t token = *reinterpret_cast<volatile uint64_t*>(sk.epoch) + 1;
-            flag_wait(flag, token, wc, kSiteSplitTail);
+            flag_wait(flag, launch_tag(sk.epoch, sk.salt), wc, kSiteSplitTail);
             __threadfence();
           }
           named_bar_sync(1, kEpiThreads);
@@ -565,7 +566,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // this block out of the launch (the last one advances the launch counter).
   if (threadIdx.x == 0) {
     if (kSplit && sk.epoch != nullptr)
-      launch_exit(sk.epoch);
+      launch_exit(sk.epoch, sk.salt);
     else
       Epi::at_exit(ep);
   }

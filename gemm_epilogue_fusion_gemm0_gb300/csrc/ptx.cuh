@@ -176,37 +176,49 @@ __device__ __forceinline__ uint64_t atom_add_acq_rel_gpu_u64(uint64_t* p, uint64
 
 // End of a launch whose blocks exchange flags tagged with a token taken from a
 // launch counter (the data gradient's row flags, the split tail's partial
-// flags).  `slot` is a 256-byte, 16-byte aligned slot of the caller's
-// workspace, any initial contents:
+// flags).  `slot` is the first 256 bytes of the caller's workspace (16-byte
+// aligned, any initial contents); every workspace layout of this library keeps
+// it there and never writes data into it, so one counter serves every call,
+// shape and entry point that shares the buffer:
 //   slot[0]           launch counter; this launch's token is slot[0] + 1
 //   slot[1]           kSlotReady once slot[2] has been prepared by a launch
 //   slot[2]           blocks of the current launch that have finished (0 at its start)
-//   slot[4], slot[5]  {token, blocks finished}: the count of a first launch
+//   slot[4], slot[5]  {token ^ salt, blocks finished}: the count of a first launch
+// A flag holds token ^ salt, `salt` being a random 64-bit value the host draws
+// for each call (fixed across replays of a captured call, whose tokens the
+// counter keeps distinct).  Flags left by other calls, other buffers or any
+// earlier contents therefore match only by a 2^-64 coincidence.
 // Called by one thread per block once every thread of the block is done with
 // the launch's flags.  The block that completes the count (gridDim.x) prepares
 // slot[2] for the next launch and stores the token as the new launch counter,
 // after which no flag of this launch is read any more.  Nothing waits.  In
 // steady state each block adds 1 to slot[2] (one atomic).  On a slot not yet
 // prepared (a fresh workspace) the count goes through a 128-bit
-// compare-and-swap on {token, count} that any contents cannot fool (a token
-// that does not match restarts the count); every failed compare-and-swap means
-// another block got in, so that loop runs at most gridDim.x + 1 times.  Only the
-// last block writes slot[1], after every block has read it, so all blocks of a
-// launch take the same path.
+// compare-and-swap on {token ^ salt, count} (a tag that does not match
+// restarts the count); every failed compare-and-swap means another block got
+// in, so that loop runs at most gridDim.x + 1 times.  Only the last block
+// writes slot[1], after every block has read it, so all blocks of a launch take
+// the same path.
 constexpr uint64_t kSlotReady = 0xC0DA5107C0DA5107ull;
 
-__device__ __forceinline__ void launch_exit(uint64_t* slot) {
+// The value a flag of this launch carries.
+__device__ __forceinline__ uint64_t launch_tag(const uint64_t* slot, uint64_t salt) {
+  return (*reinterpret_cast<const volatile uint64_t*>(slot) + 1) ^ salt;
+}
+
+__device__ __forceinline__ void launch_exit(uint64_t* slot, uint64_t salt) {
   volatile uint64_t* vs = reinterpret_cast<volatile uint64_t*>(slot);
   const uint64_t token = vs[0] + 1;
   bool last = false;
   if (vs[1] == kSlotReady) {
     last = atom_add_acq_rel_gpu_u64(slot + 2, 1) == gridDim.x - 1;
   } else {
+    const uint64_t tag = token ^ salt;
     uint64_t e_lo = vs[4], e_hi = vs[5];
     for (uint32_t i = 0; i <= gridDim.x; ++i) {
-      const uint64_t n_hi = (e_lo == token) ? e_hi + 1 : 1;
+      const uint64_t n_hi = (e_lo == tag) ? e_hi + 1 : 1;
       uint64_t o_lo, o_hi;
-      if (cas128_gpu(slot + 4, e_lo, e_hi, token, n_hi, o_lo, o_hi)) {
+      if (cas128_gpu(slot + 4, e_lo, e_hi, tag, n_hi, o_lo, o_hi)) {
         last = n_hi == gridDim.x;
         break;
       }

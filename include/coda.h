@@ -29,6 +29,16 @@
  *  - The caller owns every buffer, including the workspace; the library never
  *    allocates, frees or synchronises inside coda_fwd / coda_bwd_dgrad.  Work
  *    is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *  - Workspaces need no clearing and one buffer may serve any sequence of
+ *    calls, of any shape and entry point, as long as calls sharing it do not
+ *    run concurrently.  Its first 256 bytes hold a launch counter that no
+ *    layout puts data into; launches whose blocks exchange completion flags
+ *    tag them with the counter's next value mixed with a random 64-bit salt
+ *    drawn for each call (kept by a call captured in a CUDA graph, whose
+ *    replays the counter tells apart).  Flags of earlier launches on the same
+ *    counter never match, and other contents of the buffer (earlier data,
+ *    another buffer's flags recycled by an allocator) match only by a 2^-64
+ *    coincidence.
  *  - Argument checks happen before anything is enqueued; on any error nothing
  *    is launched.  Device-side failures (a bounded wait that ran out) are
  *    reported later by coda_get_device_status().
@@ -71,18 +81,18 @@ typedef enum {
   CODA_ERR_DEVICE_BOUNDS = 9       /* checked build only: a device-side bounds or alignment check failed */
 } coda_status_t;
 
-/* Bytes of device workspace coda_fwd needs: the bf16 GEMM1 operand
- * hg = h * gamma ([M, d]) and the fp32 partial sums of h^2, two per row and
- * 256-column tile, then the split-tail region of the two GEMMs: up to
- * min(T, 160) partial accumulators of 256 x 256 fp32 (T = the larger GEMM's
- * count of 256 x 256 tiles), one 64-bit flag per 128-row half of each, and a
- * 256-byte slot holding a launch counter.  Returns 0 for M == 0. */
+/* Bytes of device workspace coda_fwd needs: the 256-byte slot of the launch
+ * counter, the bf16 GEMM1 operand hg = h * gamma ([M, d]) and the fp32
+ * partial sums of h^2, two per row and 256-column tile, then the split-tail
+ * region of the two GEMMs: up to min(T, 160) partial accumulators of
+ * 256 x 256 fp32 (T = the larger GEMM's count of 256 x 256 tiles) and one
+ * 64-bit flag per 128-row half of each.  Returns 0 for M == 0. */
 CODA_API size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
-/* Bytes of device workspace coda_bwd_dgrad needs: fp32 partial row
- * statistics (two per row and column tile), one 64-bit completion flag per
- * 128-row slab and column tile, and a 256-byte slot holding the launch counter
- * and its arrival word. */
+/* Bytes of device workspace coda_bwd_dgrad needs: the 256-byte slot holding
+ * the launch counter and its arrival word, fp32 partial row statistics (two
+ * per row and column tile) and one 64-bit completion flag per 128-row slab and
+ * column tile. */
 CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /*
@@ -105,8 +115,9 @@ CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1)
  *   r_out  [M]      fp32 out    (inverse RMS per row; saved for backward)
  *   y_out  [M, N1]  bf16 out
  *   workspace: device memory of at least coda_fwd_workspace_bytes(M, d, N1)
- *   bytes.  Any initial contents work and the call clobbers them, except that
- *   two calls sharing a workspace must not run concurrently.
+ *   bytes (the launch counter, hg, the partial sums and the split-tail
+ *   region).  Any initial contents work and the call clobbers them, except
+ *   that two calls sharing a workspace must not run concurrently.
  * Split tail: when a GEMM's 256 x 256 tiles do not fill whole waves of CTA
  * pairs, its last U + R tiles (U pairs, R tiles past the last full wave) are
  * shared out along K so that every pair ends together; a tile cut in two is
@@ -158,7 +169,8 @@ CODA_API coda_status_t coda_fwd_swiglu(const coda_bf16* x, const coda_bf16* W0, 
  *   3. GEMM1: y = r * (s_hg * sW1) * (hq @ W1_q), stored bf16.
  *   x_q [M, d], W0_q [d, d], W1_q [d, N1]: E4M3 codes (1 byte), row-major.
  *   z [M, d], gamma [d] bf16; h_out [M, d] bf16, r_out [M] fp32, y_out [M, N1] bf16.
- *   workspace: at least coda_fwd_fp8_workspace_bytes(M, d, N1) (hq and partials).
+ *   workspace: at least coda_fwd_fp8_workspace_bytes(M, d, N1) (the launch
+ *   counter's slot, hq and the partial sums).
  * d and N1 must be multiples of 16.  Always runs CTA-pair tiles.
  */
 CODA_API size_t coda_fwd_fp8_workspace_bytes(int64_t M, int64_t d, int64_t N1);
@@ -187,11 +199,12 @@ CODA_API coda_status_t coda_fwd_fp8(const uint8_t* x_q, float sx, const uint8_t*
  *   gamma   [d]     bf16 in
  *   dh_out  [M, d]  bf16 out
  *   workspace: at least coda_bwd_dgrad_workspace_bytes(M, d, N1) bytes.  The
- *   completion flags carry a token taken from a launch counter kept in the
- *   workspace, which every launch advances once all its blocks are done: the
- *   workspace needs no clearing (any initial contents work), and a call
- *   captured in a CUDA graph draws a fresh token at every replay.  Two calls
- *   that share a workspace must not run concurrently.
+ *   completion flags carry a token taken from the launch counter at the
+ *   workspace's start, which every launch advances once all its blocks are
+ *   done, mixed with the call's salt (see the conventions above): the
+ *   workspace needs no clearing, and a call captured in a CUDA graph draws a
+ *   fresh token at every replay.  Two calls that share a workspace must not
+ *   run concurrently.
  * The kernel is a cooperative launch (all its blocks are resident at once):
  * every column tile of a row block must be in flight together, so d is limited
  * to 256 * (CTA pairs resident on the device) columns, 19456 on a 152-SM GB300
@@ -254,8 +267,9 @@ CODA_API coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_b
  *   dh_out [M, d] bf16 (= dz), dx_out [M, d] bf16, dgamma_out [d] fp32,
  *   dW0_out [d, d] fp32, dW1_out [d, N1] fp32                    (outputs)
  *   workspace: at least coda_bwd_workspace_bytes(M, d, N1) bytes: the
- *   coda_bwd_dgrad workspace, h2, the dgamma partials and a split-tail region
- *   as in coda_fwd, sized for the largest of launches 3-5.
+ *   coda_bwd_dgrad workspace (its launch counter serves every launch of the
+ *   call), h2, the dgamma partials and a split-tail region as in coda_fwd,
+ *   sized for the largest of launches 3-5.
  * Launch 1 is cooperative, as in coda_bwd_dgrad; launches 3-5 split their tail
  * (and are then cooperative) under the same conditions as coda_fwd's GEMMs.
  * Conventions as coda_fwd.
@@ -407,7 +421,7 @@ CODA_API coda_status_t coda_watchdog_selftest(uint64_t timeout_ns, cudaStream_t 
  *    forbidden, and before any stream capture.
  *  - Every call uses the same array.  Nothing in it needs clearing (each
  *    launch tags its flags with a fresh token from a launch counter kept in
- *    the array), but calls whose kernels
+ *    the array, mixed with the call's salt), but calls whose kernels
  *    overlap on the GPU, on different streams or from different host threads,
  *    race on it and give wrong results: order them (one stream, or events).
  *  - Otherwise the arguments, checks and errors are those of coda_bwd_dgrad.

@@ -48,9 +48,9 @@ def test_status_strings(lib):
 
 def _split_tail_bytes_for_tiles(tiles):
     # min(T, 160) slots of 256 x 256 fp32 partials, a u64 flag per 128-row half of each
-    # (rounded up to 256 B), a 256-byte launch-counter slot
+    # (rounded up to 256 B); the launch counter is the workspace's first 256 bytes
     slots = min(tiles, 160)
-    return slots * 256 * 256 * 4 + -(-(slots * 16) // 256) * 256 + 256
+    return slots * 256 * 256 * 4 + -(-(slots * 16) // 256) * 256
 
 
 def _split_tail_bytes(M, d, N1):
@@ -59,23 +59,34 @@ def _split_tail_bytes(M, d, N1):
 
 
 def test_workspace_sizes(lib):
-    # hg [M,d] bf16 + partial sums [2 * ceil(d/256), M] fp32, each rounded up to 256 B,
-    # then the split-tail region
+    # Every workspace starts with the 256-byte slot of the launch counter.  The forward:
+    # the slot, hg [M,d] bf16 + partial sums [2 * ceil(d/256), M] fp32, each rounded up to
+    # 256 B, then the split-tail region
     M, d, N1 = 8192, 4096, 28672
-    assert _split_tail_bytes(M, d, N1) == 160 * 262144 + 2560 + 256
-    assert lib.coda_fwd_workspace_bytes(M, d, N1) == M * d * 2 + 32 * M * 4 + _split_tail_bytes(M, d, N1)
-    assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == M * d * 2
-    # qpart [2 * 32, M] fp32 + flags [2 * ceil(M/256) * 32] u64 (one per 128-row slab and column
-    # tile, for up to 2 * ceil(d/256) = 32 column tiles per row block) + a 256-byte slot for the
-    # launch counter
-    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 64 * M * 4 + 64 * 32 * 8 + 256
-    # 2 * 2 x 300 fp32 = 4800 -> 4864; 4 slabs x 2 tiles x 8 = 64 -> 256; + 256
-    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 4864 + 256 + 256
+    assert _split_tail_bytes(M, d, N1) == 160 * 262144 + 2560
+    assert lib.coda_fwd_workspace_bytes(M, d, N1) == (
+        256 + M * d * 2 + 32 * M * 4 + _split_tail_bytes(M, d, N1))
+    assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == 256 + M * d * 2
+    # the slot, qpart [2 * 32, M] fp32 + flags [2 * ceil(M/256) * 32] u64 (one per 128-row
+    # slab and column tile, for up to 2 * ceil(d/256) = 32 column tiles per row block)
+    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 256 + 64 * M * 4 + 64 * 32 * 8
+    # 256; 2 * 2 x 300 fp32 = 4800 -> 4864; 4 slabs x 2 tiles x 8 = 64 -> 256
+    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 256 + 4864 + 256
     assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
-    assert _split_tail_bytes(300, 328, 776) == 8 * 262144 + 256 + 256  # 2 x 4 tiles
+    assert _split_tail_bytes(300, 328, 776) == 8 * 262144 + 256  # 2 x 4 tiles
     assert lib.coda_fwd_workspace_bytes(300, 328, 776) == (  # ragged: rounded up
-        196864 + 4864 + _split_tail_bytes(300, 328, 776))
+        256 + 196864 + 4864 + _split_tail_bytes(300, 328, 776))
     assert lib.coda_fwd_workspace_bytes(10, 12, 16) == 0  # d % 8 != 0: unsupported
+    # the slot, then the SwiGLU statistic's partials [2 * ceil(N1/2 / 256), M] fp32
+    assert lib.coda_bwd_swiglu_dgrad_workspace_bytes(300, 256, 1024, 512) == 256 + 4864
+    # the slot, then hq [M, d] E4M3 codes and the partial sums
+    assert lib.coda_fwd_fp8_workspace_bytes(300, 256, 512) == 256 + 76800 + 2560
+    # the full backward: the data gradient's workspace, h2 [M, d] bf16, the dgamma partials
+    # [4 * 128-row slabs, d] fp32 and the split-tail region sized for its largest GEMM
+    tiles = max(-(-d // 256) * -(-max(d, N1) // 256), -(-M // 256) * -(-d // 256))
+    assert lib.coda_bwd_workspace_bytes(M, d, N1) == (
+        lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) + M * d * 2 + 4 * 64 * d * 4
+        + _split_tail_bytes_for_tiles(tiles))
 
 
 FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced
@@ -158,7 +169,7 @@ def test_fp8_argument_validation(lib):
     assert call(d=264) == E["CODA_ERR_UNSUPPORTED_SHAPE"]  # FP8 rows need d % 16 == 0
     assert call(sx=0.0) == E["CODA_ERR_INVALID_ARG"]
     assert call(shg=float("nan")) == E["CODA_ERR_INVALID_ARG"]
-    assert lib.coda_fwd_fp8_workspace_bytes(8192, 4096, 28672) == 8192 * 4096 + 32 * 8192 * 4
+    assert lib.coda_fwd_fp8_workspace_bytes(8192, 4096, 28672) == 256 + 8192 * 4096 + 32 * 8192 * 4
 
 
 def test_no_device_is_reported_without_gpu(lib):

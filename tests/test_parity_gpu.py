@@ -24,6 +24,7 @@ from gemm_epilogue_fusion_gemm0_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 TOL_HY, TOL_DH, TOL_R, TOL_ELEM = 1e-2, 2e-2, 1e-3, 2.0 ** -4
+U64 = 2 ** 64 - 1
 
 
 @pytest.fixture(scope="module")
@@ -399,10 +400,9 @@ def test_folded_rowreduce_is_bit_identical(B, mode, M, d, N1):
 SPLIT_SHAPES = [(2048, 5120, 5120), (2000, 5000, 5064)]
 
 
-def fwd_epoch(ws):
-    """The forward's launch counter: the last 8-byte slot of its workspace."""
-    n = ws.numel()
-    return int(ws[n - 256:n - 248].view(torch.int64).item())
+def launch_counter(ws):
+    """The launch counter: the first 8 bytes of every workspace."""
+    return int(ws[:8].view(torch.int64).item())
 
 
 def split_launches(M, d, N1, pairs):
@@ -435,13 +435,13 @@ def test_split_tail_forward_matches_oracle(B, M, d, N1):
         outs = {}
         for split in (0, 1):
             B.coda_set_split_tail(split)
-            e0 = fwd_epoch(ws)
+            e0 = launch_counter(ws)
             outs[split] = B.coda_fwd(*args, ws=ws)
             torch.cuda.synchronize()
             st, detail = B.coda_get_device_status()
             assert st == B.CODA_OK, (B.status_string(st), hex(detail))
             want = split_launches(M, d, N1, pairs) if split else 0
-            assert (fwd_epoch(ws) - e0) % 2 ** 64 == want
+            assert (launch_counter(ws) - e0) % 2 ** 64 == want
         dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
         dh = B.coda_bwd_dgrad(dy_cpu.to(dev), g["W1"], outs[1][0], outs[1][1], g["gamma"])
     finally:
@@ -539,14 +539,14 @@ def test_split_tail_is_deterministic_and_replays_from_a_cuda_graph(B):
             for t in (h, y):
                 t.fill_(float("nan"))
             r.fill_(-1.0)
-            e0 = fwd_epoch(ws)
+            e0 = launch_counter(ws)
             graph.replay()
             torch.cuda.synchronize()
             st, detail = B.coda_get_device_status()
             assert st == B.CODA_OK, (B.status_string(st), hex(detail))
             for got, want in zip((h, r, y), ref):
                 assert torch.equal(got, want)
-            assert (fwd_epoch(ws) - e0) % 2 ** 64 == n_split
+            assert (launch_counter(ws) - e0) % 2 ** 64 == n_split
     finally:
         B.coda_set_mma_mode(old)
 
@@ -555,8 +555,8 @@ def test_split_tail_full_backward_matches_oracle(B):
     """coda_bwd at (4040, 4096, 1024): dx (16 x 16 tiles, K = d) and dW0 (16 x 16
     tiles, K = 4040 tokens, ragged: 64 k-blocks) split their tails, dW1 (16 x 4
     tiles) does not; every gradient against the oracle, and the backward's
-    split-tail counter (the last 8-byte slot of its workspace) advances once per
-    split launch."""
+    launch counter (the first 8 bytes of its workspace) advances once for the
+    data gradient and once per split launch."""
     M, d, N1 = 4040, 4096, 1024
     dev = torch.device("cuda:0")
     t = synth.make_forward_inputs(M, d, N1, seed=35)
@@ -568,7 +568,7 @@ def test_split_tail_full_backward_matches_oracle(B):
         dy = synth.make_grad_output(t["_rng"], M, N1)
         res = synth.make_residual_grad(t["_rng"], M, d)
         ws = B.workspace(B.coda_bwd_workspace_bytes(M, d, N1), dev)
-        e0 = fwd_epoch(ws)
+        e0 = launch_counter(ws)
         o = B.coda_bwd(dy.to(dev), g["x"], g["W0"], g["W1"], h, r, g["gamma"], res.to(dev), ws=ws)
         torch.cuda.synchronize()
     finally:
@@ -576,7 +576,7 @@ def test_split_tail_full_backward_matches_oracle(B):
     st, detail = B.coda_get_device_status()
     assert st == B.CODA_OK, (B.status_string(st), hex(detail))
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
-        assert (fwd_epoch(ws) - e0) % 2 ** 64 == 2
+        assert (launch_counter(ws) - e0) % 2 ** 64 == 1 + 2
     ref = oracle.backward_full(f64(dy), f64(t["x"]), f64(t["W0"]), f64(t["W1"]), f64(h.cpu()),
                                f64(r.cpu()), f64(t["gamma"]), f64(res))
     check("dh", f64(o["dh"].cpu()), ref.dh, TOL_DH)
@@ -625,9 +625,11 @@ def test_step_replays_from_a_cuda_graph(B, mode):
     """coda_fwd + coda_bwd_dgrad captured once into a CUDA graph and replayed,
     twice per input set, on three input sets copied into the captured buffers:
     every replay equals the eager calls on the same inputs bit for bit.  The
-    dgrad's launch counter (the last 8 bytes of its workspace) advances by one
-    per replay and every completion flag holds the last replay's token, so
-    flags left by one replay never satisfy the next one's waits."""
+    dgrad's launch counter (the first 8 bytes of its workspace) advances by one
+    per replay and every completion flag holds the last replay's token mixed
+    with the captured call's salt, which stays fixed across replays, so flags
+    left by one replay never satisfy the next one's waits; each eager call
+    draws a salt of its own."""
     dev = torch.device("cuda:0")
     M, d, N1, eps = 640, 512, 1280, 1e-5
     sets = []
@@ -651,7 +653,7 @@ def test_step_replays_from_a_cuda_graph(B, mode):
         B.coda_bwd_dgrad(buf["dy"], buf["W1"], h, r, buf["gamma"], dh=dh, ws=ws_b, stream=st)
 
     def epoch():
-        return int(ws_b[nb - 256:nb - 248].view(torch.int64).item())
+        return int(ws_b[:8].view(torch.int64).item()) & U64
 
     for k in buf:
         buf[k].copy_(sets[0][k])
@@ -663,12 +665,22 @@ def test_step_replays_from_a_cuda_graph(B, mode):
     ntmax = 2 * ((d + 255) // 256)  # the workspace holds up to 2 ceil(d/256) column tiles
     # 128-row slabs: two per 256-row block of CTA-pair tiles, else one per 128-row tile
     slabs = 2 * ((M + 255) // 256) if mode == 1 else (M + 127) // 128
-    flags = ws_b[((2 * ntmax * M * 4 + 255) // 256) * 256:][: slabs * ntmax * 8].view(torch.int64)
+    f0 = 256 + (2 * ntmax * M * 4 + 255) // 256 * 256  # after the slot and the partials
+    flags = ws_b[f0:f0 + slabs * ntmax * 8].view(torch.int64)
+    nt = (d + 255) // 256
+
+    def salt_of_last_launch():
+        f = [int(v) & U64 for v in flags[: slabs * nt].cpu()]
+        assert len(set(f)) == 1, "every flag of the launch holds one value"
+        return f[0] ^ epoch()
+
+    graph_salt, eager_salts = None, set()
     for data in sets:
         for k in buf:
             buf[k].copy_(data[k])
         step()
         torch.cuda.synchronize()
+        eager_salts.add(salt_of_last_launch())
         ref = [t.clone() for t in (h, r, y, dh)]
         for t in (h, y, dh):
             t.fill_(float("nan"))
@@ -684,9 +696,10 @@ def test_step_replays_from_a_cuda_graph(B, mode):
         e2 = epoch()
         assert (e2 - e0) % 2 ** 64 == 2  # the counter starts at whatever the workspace held
         # the launch used the first slabs * nt flags, nt its column tiles per row block
-        k = int((flags == e2).sum())
-        assert k > 0 and k % slabs == 0 and k // slabs >= (d + 255) // 256, k
-        assert torch.all(flags[:k] == e2), "every flag holds the last replay's token"
+        salt = salt_of_last_launch()
+        graph_salt = salt if graph_salt is None else graph_salt
+        assert salt == graph_salt, "replays of one captured call keep its salt"
+    assert len(eager_salts) == len(sets) and graph_salt not in eager_salts
 
 
 @pytest.mark.parametrize("entry", ["fwd_swiglu", "bwd_swiglu_dgrad", "bwd", "fwd_fp8"])
@@ -787,7 +800,7 @@ def test_dgrad_workspace_with_random_contents(B, mode):
     nb = B.coda_bwd_dgrad_workspace_bytes(M, d, N1)
     gen = torch.Generator(device="cpu").manual_seed(99)
     ws = torch.randint(0, 256, (nb,), dtype=torch.uint8, generator=gen).to(dev)
-    slot = lambda: ws[nb - 256:nb - 208].view(torch.int64).cpu()  # slot words 0..5
+    slot = lambda: ws[:48].view(torch.int64).cpu()  # slot words 0..5
     e0 = int(slot()[0])
     bref = oracle.backward_dgrad(f64(dy_cpu), f64(t["W1"]), f64(h), f64(r), f64(t["gamma"]))
     for call in (1, 2):
@@ -799,6 +812,66 @@ def test_dgrad_workspace_with_random_contents(B, mode):
         assert int(w[1]) & (2 ** 64 - 1) == 0xC0DA5107C0DA5107  # the count is prepared
         assert int(w[2]) == 0  # and zeroed for the next launch
         check(f"dh (call {call})", f64(dh), bref.dh, TOL_DH)
+
+
+# ----------------------------------------------------------------------------- one workspace, many calls
+def test_workspace_shared_across_shapes_and_entry_points(B, mode):
+    """One buffer serves a sequence of calls of different shapes and entry
+    points.  At d = 512 the data gradient's flag array starts 16640 bytes in for
+    M = 520, which is where the M = 512 call's flags end: the launch counter
+    sits at the buffer's start, so a larger call never reads a smaller call's
+    counter or flags as its own.  Between the two, a forward writes its operands
+    over the same bytes.  Then a buffer whose first word is 0 and every other
+    8-byte word 1 (the token a fresh counter implies) must not satisfy any
+    wait.  Every call matches the oracle; the counter advances by one per
+    data-gradient launch, and the flags of each call hold its token mixed with
+    a salt of its own."""
+    dev = torch.device("cuda:0")
+    d, N1, eps = 512, 1280, 1e-5
+    ntmax, nt = 2 * ((d + 255) // 256), (d + 255) // 256
+    Ms = (512, 520)
+    nb = max(B.coda_bwd_dgrad_workspace_bytes(m, d, N1) for m in Ms)
+    nb = max(nb, B.coda_fwd_workspace_bytes(Ms[0], d, N1))
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    word = lambda i: int(ws[8 * i:8 * i + 8].view(torch.int64).item()) & U64
+
+    def flags_of(M):
+        slabs = 2 * ((M + 255) // 256) if mode == 1 else (M + 127) // 128
+        f0 = 256 + (2 * ntmax * M * 4 + 255) // 256 * 256
+        return [int(v) & U64 for v in ws[f0:f0 + slabs * nt * 8].view(torch.int64).cpu()]
+
+    def dgrad_case(M, seed):
+        t = synth.make_dgrad_inputs(M, d, N1, seed=seed)
+        r = oracle.inverse_rms(oracle.mean_square(f64(t["h"])), eps).astype(np.float32)
+        g = {k: v.to(dev) for k, v in t.items()}
+        bref = oracle.backward_dgrad(f64(t["dy"]), f64(t["W1"]), f64(t["h"]), r.astype(np.float64),
+                                     f64(t["gamma"]))
+        e0 = word(0)
+        dh = B.coda_bwd_dgrad(g["dy"], g["W1"], g["h"], torch.from_numpy(r).to(dev), g["gamma"],
+                              ws=ws)
+        st, detail = B.coda_get_device_status()
+        assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+        check(f"dh (M={M})", f64(dh), bref.dh, TOL_DH)
+        e1 = word(0)
+        assert (e1 - e0) & U64 == 1
+        f = flags_of(M)
+        assert len(set(f)) == 1, "every flag of the launch holds one value"
+        return f[0] ^ e1  # the call's salt
+
+    salts = [dgrad_case(Ms[0], 41)]
+    t = synth.make_forward_inputs(Ms[0], d, N1, seed=42)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    e0 = word(0)
+    h, r, y = B.coda_fwd(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], eps, ws=ws)
+    ref = oracle.forward(f64(t["x"]), f64(t["W0"]), f64(t["z"]), f64(t["gamma"]), f64(t["W1"]), eps)
+    check("y (forward on the shared buffer)", f64(y), ref.y, TOL_HY)
+    assert word(0) == e0  # no launch of this forward exchanges flags
+    salts.append(dgrad_case(Ms[1], 43))
+    ws.view(torch.int64).fill_(1)
+    ws[:8].zero_()
+    salts.append(dgrad_case(Ms[0], 44))
+    assert word(1) == 0xC0DA5107C0DA5107 and word(2) == 0  # the count is prepared
+    assert len(set(salts)) == len(salts) and 0 not in salts
 
 
 # ----------------------------------------------------------------------------- the dgrad's column-tile ceiling
