@@ -107,10 +107,14 @@ def _check(status: int, where: str) -> None:
         raise CodaError(status, where)
 
 
-def _stream_ptr(stream) -> int:
+def _stream_ptr(stream, device=None) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+        stream = torch.cuda.current_stream(device)
+    if not hasattr(stream, "cuda_stream"):
+        return int(stream)  # a raw cudaStream_t handle
+    if device is not None and stream.device != torch.device(device):
+        raise ValueError(f"the stream is on {stream.device}, the call's tensors on {device}")
+    return int(stream.cuda_stream)
 
 
 def _dev(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str) -> int:
@@ -123,6 +127,39 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, shape: tuple, name: str) -> int:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+class _Call:
+    """Marshalling for one call: every tensor must be a contiguous CUDA tensor
+    of the stated dtype and shape on the device of the call's first tensor,
+    and the C function runs with that device current (the C ABI works on the
+    current device, so a tensor on another one would hand the kernels a
+    pointer they cannot use)."""
+
+    def __init__(self, where: str, device: torch.device):
+        self.where, self.device = where, torch.device(device)
+
+    def t(self, t, dtype, shape, name) -> int:
+        p = _dev(t, dtype, shape, name)
+        if t.device != self.device:
+            raise ValueError(f"{self.where}: {name} is on {t.device}, the call's first tensor on "
+                             f"{self.device}")
+        return p
+
+    def opt(self, t, dtype, shape, name):
+        return None if t is None else self.t(t, dtype, shape, name)
+
+    def ws(self, ws) -> tuple:
+        if not isinstance(ws, torch.Tensor) or not ws.is_cuda or not ws.is_contiguous():
+            raise TypeError(f"{self.where}: the workspace must be a contiguous CUDA tensor")
+        if ws.device != self.device:
+            raise ValueError(f"{self.where}: the workspace is on {ws.device}, the call's first "
+                             f"tensor on {self.device}")
+        return ws.data_ptr(), ws.numel() * ws.element_size()
+
+    def run(self, fn, *args, stream=None) -> None:
+        with torch.cuda.device(self.device):
+            _check(fn(*args, _stream_ptr(stream, self.device)), self.where)
 
 
 # --------------------------------------------------------------------------- sizes
@@ -157,13 +194,11 @@ def _fwd_common(fn, wsfn, x, W0, z, gamma, W1, eps, h, r, y, ws, stream):
     if ws is None:
         ws = workspace(wsfn(M, d, N1), dev)
     bf = torch.bfloat16
-    args = (
-        _dev(x, bf, (M, d), "x"), _dev(W0, bf, (d, d), "W0"), _dev(z, bf, (M, d), "z"),
-        _dev(gamma, bf, (d,), "gamma"), _dev(W1, bf, (d, N1), "W1"), float(eps), M, d, N1,
-        _dev(h, bf, (M, d), "h"), _dev(r, torch.float32, (M,), "r"), _dev(y, bf, (M, N1), "y"),
-        ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream),
-    )
-    _check(fn(*args), fn.__name__)
+    c = _Call(fn.__name__, dev)
+    c.run(fn, c.t(x, bf, (M, d), "x"), c.t(W0, bf, (d, d), "W0"), c.t(z, bf, (M, d), "z"),
+          c.t(gamma, bf, (d,), "gamma"), c.t(W1, bf, (d, N1), "W1"), float(eps), M, d, N1,
+          c.t(h, bf, (M, d), "h"), c.t(r, torch.float32, (M,), "r"), c.t(y, bf, (M, N1), "y"),
+          *c.ws(ws), stream=stream)
     return h, r, y
 
 
@@ -194,14 +229,12 @@ def coda_fwd_swiglu(x, W0, z, gamma, W1, eps, h=None, r=None, a=None, y=None, wa
         y = torch.empty((M, N1), dtype=bf, device=dev)
     if ws is None:
         ws = workspace(coda_fwd_workspace_bytes(M, d, N1), dev)
-    st = _lib.coda_fwd_swiglu(
-        _dev(x, bf, (M, d), "x"), _dev(W0, bf, (d, d), "W0"), _dev(z, bf, (M, d), "z"),
-        _dev(gamma, bf, (d,), "gamma"), _dev(W1, bf, (d, N1), "W1"), float(eps), M, d, N1,
-        _dev(h, bf, (M, d), "h"), _dev(r, torch.float32, (M,), "r"),
-        None if y is None else _dev(y, bf, (M, N1), "y"), _dev(a, bf, (M, N1 // 2), "a"),
-        ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream),
-    )
-    _check(st, "coda_fwd_swiglu")
+    c = _Call("coda_fwd_swiglu", dev)
+    c.run(_lib.coda_fwd_swiglu,
+          c.t(x, bf, (M, d), "x"), c.t(W0, bf, (d, d), "W0"), c.t(z, bf, (M, d), "z"),
+          c.t(gamma, bf, (d,), "gamma"), c.t(W1, bf, (d, N1), "W1"), float(eps), M, d, N1,
+          c.t(h, bf, (M, d), "h"), c.t(r, torch.float32, (M,), "r"), c.opt(y, bf, (M, N1), "y"),
+          c.t(a, bf, (M, N1 // 2), "a"), *c.ws(ws), stream=stream)
     return (h, r, a, y) if y is not None else (h, r, a)
 
 
@@ -222,20 +255,18 @@ def coda_fwd_fp8(x_q, sx, W0_q, sW0, z, gamma, W1_q, sW1, s_hg, eps, h=None, r=N
     y = torch.empty((M, N1), dtype=bf, device=dev) if y is None else y
     if ws is None:
         ws = workspace(coda_fwd_fp8_workspace_bytes(M, d, N1), dev)
+    c = _Call("coda_fwd_fp8", dev)
 
     def code(t, shape, name):
         if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
             raise TypeError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")
-        return _dev(t, t.dtype, shape, name)
+        return c.t(t, t.dtype, shape, name)
 
-    st = _lib.coda_fwd_fp8(
-        code(x_q, (M, d), "x_q"), float(sx), code(W0_q, (d, d), "W0_q"), float(sW0),
-        _dev(z, bf, (M, d), "z"), _dev(gamma, bf, (d,), "gamma"), code(W1_q, (d, N1), "W1_q"),
-        float(sW1), float(s_hg), float(eps), M, d, N1, _dev(h, bf, (M, d), "h"),
-        _dev(r, torch.float32, (M,), "r"), _dev(y, bf, (M, N1), "y"), ws.data_ptr(),
-        ws.numel() * ws.element_size(), _stream_ptr(stream),
-    )
-    _check(st, "coda_fwd_fp8")
+    c.run(_lib.coda_fwd_fp8,
+          code(x_q, (M, d), "x_q"), float(sx), code(W0_q, (d, d), "W0_q"), float(sW0),
+          c.t(z, bf, (M, d), "z"), c.t(gamma, bf, (d,), "gamma"), code(W1_q, (d, N1), "W1_q"),
+          float(sW1), float(s_hg), float(eps), M, d, N1, c.t(h, bf, (M, d), "h"),
+          c.t(r, torch.float32, (M,), "r"), c.t(y, bf, (M, N1), "y"), *c.ws(ws), stream=stream)
     return h, r, y
 
 
@@ -248,13 +279,11 @@ def coda_bwd_dgrad(dy, W1, h, r, gamma, dh=None, ws=None, stream=None):
     if ws is None:
         ws = workspace(coda_bwd_dgrad_workspace_bytes(M, d, N1), dy.device)
     bf = torch.bfloat16
-    st = _lib.coda_bwd_dgrad(
-        _dev(dy, bf, (M, N1), "dy"), _dev(W1, bf, (d, N1), "W1"), _dev(h, bf, (M, d), "h"),
-        _dev(r, torch.float32, (M,), "r"), _dev(gamma, bf, (d,), "gamma"), M, d, N1,
-        _dev(dh, bf, (M, d), "dh"), ws.data_ptr(), ws.numel() * ws.element_size(),
-        _stream_ptr(stream),
-    )
-    _check(st, "coda_bwd_dgrad")
+    c = _Call("coda_bwd_dgrad", dy.device)
+    c.run(_lib.coda_bwd_dgrad,
+          c.t(dy, bf, (M, N1), "dy"), c.t(W1, bf, (d, N1), "W1"), c.t(h, bf, (M, d), "h"),
+          c.t(r, torch.float32, (M,), "r"), c.t(gamma, bf, (d,), "gamma"), M, d, N1,
+          c.t(dh, bf, (M, d), "dh"), *c.ws(ws), stream=stream)
     return dh
 
 
@@ -277,14 +306,13 @@ def coda_bwd_swiglu_dgrad(dout, W2, y, W1, h, r, gamma, dy=None, s=None, dh=None
     dh = torch.empty((M, d), dtype=bf, device=dev) if dh is None else dh
     if ws is None:
         ws = workspace(coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout), dev)
-    st = _lib.coda_bwd_swiglu_dgrad(
-        _dev(dout, bf, (M, Dout), "dout"), _dev(W2, bf, (half, Dout), "W2"),
-        _dev(y, bf, (M, N1), "y"), _dev(W1, bf, (d, N1), "W1"), _dev(h, bf, (M, d), "h"),
-        _dev(r, torch.float32, (M,), "r"), _dev(gamma, bf, (d,), "gamma"), M, d, N1, Dout,
-        _dev(dy, bf, (M, N1), "dy"), _dev(s, torch.float32, (M,), "s"), _dev(dh, bf, (M, d), "dh"),
-        ws.data_ptr(), ws.numel() * ws.element_size(), _stream_ptr(stream),
-    )
-    _check(st, "coda_bwd_swiglu_dgrad")
+    c = _Call("coda_bwd_swiglu_dgrad", dev)
+    c.run(_lib.coda_bwd_swiglu_dgrad,
+          c.t(dout, bf, (M, Dout), "dout"), c.t(W2, bf, (half, Dout), "W2"),
+          c.t(y, bf, (M, N1), "y"), c.t(W1, bf, (d, N1), "W1"), c.t(h, bf, (M, d), "h"),
+          c.t(r, torch.float32, (M,), "r"), c.t(gamma, bf, (d,), "gamma"), M, d, N1, Dout,
+          c.t(dy, bf, (M, N1), "dy"), c.t(s, torch.float32, (M,), "s"), c.t(dh, bf, (M, d), "dh"),
+          *c.ws(ws), stream=stream)
     return dy, s, dh
 
 
@@ -306,16 +334,14 @@ def coda_bwd(dy, x, W0, W1, h, r, gamma, dh_res=None, out=None, ws=None, stream=
     o.setdefault("dW1", torch.empty((d, N1), dtype=f32, device=dev))
     if ws is None:
         ws = workspace(coda_bwd_workspace_bytes(M, d, N1), dev)
-    st = _lib.coda_bwd(
-        _dev(dy, bf, (M, N1), "dy"), _dev(x, bf, (M, d), "x"), _dev(W0, bf, (d, d), "W0"),
-        _dev(W1, bf, (d, N1), "W1"), _dev(h, bf, (M, d), "h"), _dev(r, f32, (M,), "r"),
-        _dev(gamma, bf, (d,), "gamma"), None if dh_res is None else _dev(dh_res, bf, (M, d), "dh_res"),
-        M, d, N1, _dev(o["dh"], bf, (M, d), "dh"), _dev(o["dx"], bf, (M, d), "dx"),
-        _dev(o["dgamma"], f32, (d,), "dgamma"), _dev(o["dW0"], f32, (d, d), "dW0"),
-        _dev(o["dW1"], f32, (d, N1), "dW1"), ws.data_ptr(), ws.numel() * ws.element_size(),
-        _stream_ptr(stream),
-    )
-    _check(st, "coda_bwd")
+    c = _Call("coda_bwd", dev)
+    c.run(_lib.coda_bwd,
+          c.t(dy, bf, (M, N1), "dy"), c.t(x, bf, (M, d), "x"), c.t(W0, bf, (d, d), "W0"),
+          c.t(W1, bf, (d, N1), "W1"), c.t(h, bf, (M, d), "h"), c.t(r, f32, (M,), "r"),
+          c.t(gamma, bf, (d,), "gamma"), c.opt(dh_res, bf, (M, d), "dh_res"),
+          M, d, N1, c.t(o["dh"], bf, (M, d), "dh"), c.t(o["dx"], bf, (M, d), "dx"),
+          c.t(o["dgamma"], f32, (d,), "dgamma"), c.t(o["dW0"], f32, (d, d), "dW0"),
+          c.t(o["dW1"], f32, (d, N1), "dW1"), *c.ws(ws), stream=stream)
     return o
 
 

@@ -203,3 +203,22 @@ def test_binding_refuses_to_load_without_the_library(tmp_path):
                          timeout=300)
     assert res.returncode == 0, res.stdout + res.stderr
     assert "libcoda.so not found" in res.stdout
+
+
+def test_binding_checks_tensors_before_calling_the_library(lib):
+    """The binding refuses, before any C call, tensors that are not CUDA tensors
+    and a workspace that is not one either; a raw stream handle passes through."""
+    import torch
+
+    M, d, N1 = 4, 8, 8
+    bf = torch.bfloat16
+    dy, W1 = torch.zeros(M, N1, dtype=bf), torch.zeros(d, N1, dtype=bf)
+    h, r, g = torch.zeros(M, d, dtype=bf), torch.ones(M), torch.ones(d, dtype=bf)
+    with pytest.raises(TypeError, match="dy must be a CUDA tensor"):
+        lib.coda_bwd_dgrad(dy, W1, h, r, g, ws=torch.zeros(16, dtype=torch.uint8))
+    call = lib._Call("probe", torch.device("cuda", 0))
+    with pytest.raises(TypeError, match="workspace"):
+        call.ws(torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="x must be a CUDA tensor"):
+        call.t(h, bf, (M, d), "x")
+    assert lib._stream_ptr(1234) == 1234
