@@ -252,10 +252,16 @@ constexpr size_t kSlotBytes = 256;
 // plus a counter.
 uint64_t next_salt() {
   static const uint64_t seed = [] {
-    std::random_device rd;
-    const uint64_t t = static_cast<uint64_t>(
+    uint64_t v = static_cast<uint64_t>(
         std::chrono::steady_clock::now().time_since_epoch().count());
-    return (static_cast<uint64_t>(rd()) << 32) ^ rd() ^ t;
+    v ^= reinterpret_cast<uintptr_t>(&v);  // differs between processes under ASLR
+    try {
+      std::random_device rd;
+      v ^= (static_cast<uint64_t>(rd()) << 32) ^ rd();
+    } catch (...) {
+      // no entropy source: the clock and the address above still differ per process
+    }
+    return v;
   }();
   static std::atomic<uint64_t> counter{0};
   uint64_t z = seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
