@@ -66,12 +66,16 @@ def main():
         clean(f"swiglu bwd mode {mode}")
         T.run_full_bwd(B, 300, 328, 776, 1e-5)
         clean(f"full bwd mode {mode}")
+        T.test_workspace_shared_across_shapes_and_entry_points(B, mode)
+        clean(f"one workspace for several shapes mode {mode}")
     B.coda_set_mma_mode(1)
     T.run_fp8(B, 300, 336, 784, 1e-5)
     clean("fp8 fwd")
     for (M, d, N1) in T.SPLIT_SHAPES:
         T.test_split_tail_forward_matches_oracle(B, M, d, N1)
         clean(f"split tail {M}x{d}x{N1}")
+    T.test_one_workspace_for_split_forward_and_dgrad(B)
+    clean("one workspace for a split forward and the dgrad")
     for (M, d, N1) in T.SWEEP_SHAPES[:4]:
         T.test_split_tail_shape_sweep(B, M, d, N1)
         clean(f"split sweep {M}x{d}x{N1}")

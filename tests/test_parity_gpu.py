@@ -874,6 +874,49 @@ def test_workspace_shared_across_shapes_and_entry_points(B, mode):
     assert len(set(salts)) == len(salts) and 0 not in salts
 
 
+def test_one_workspace_for_split_forward_and_dgrad(B):
+    """A forward whose GEMMs split their tails (2048 x 5120 x 5120: 160 tiles on
+    76 CTA pairs) and the data gradient on one buffer sized for both, then the
+    forward again: the shared launch counter advances once per split GEMM and
+    once per data gradient, the repeated forward is bit-identical, and every
+    output matches the oracle."""
+    M, d, N1 = SPLIT_SHAPES[0]
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=51)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    dy_cpu = synth.make_grad_output(t["_rng"], M, N1)
+    args = (g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5)
+    nb = max(B.coda_fwd_workspace_bytes(M, d, N1), B.coda_bwd_dgrad_workspace_bytes(M, d, N1))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    n_split = split_launches(M, d, N1, pairs)
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        e0 = launch_counter(ws)
+        h, r, y = B.coda_fwd(*args, ws=ws)
+        e1 = launch_counter(ws)
+        dh = B.coda_bwd_dgrad(dy_cpu.to(dev), g["W1"], h, r, g["gamma"], ws=ws)
+        e2 = launch_counter(ws)
+        h2, r2, y2 = B.coda_fwd(*args, ws=ws)
+        e3 = launch_counter(ws)
+    finally:
+        B.coda_set_mma_mode(old)
+    st, detail = B.coda_get_device_status()
+    assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+    assert [(e1 - e0) & U64, (e2 - e1) & U64, (e3 - e2) & U64] == [n_split, 1, n_split]
+    if pairs == 76:
+        assert n_split == 2
+    for a, b in ((h, h2), (r, r2), (y, y2)):
+        assert torch.equal(a, b)
+    ref = oracle.forward(f64(t["x"]), f64(t["W0"]), f64(t["z"]), f64(t["gamma"]), f64(t["W1"]), 1e-5)
+    check("h", f64(h), ref.h, TOL_HY)
+    check_r(f64(r), ref.r)
+    check("y", f64(y), ref.y, TOL_HY)
+    bref = oracle.backward_dgrad(f64(dy_cpu), f64(t["W1"]), f64(h), f64(r), f64(t["gamma"]))
+    check("dh", f64(dh), bref.dh, TOL_DH)
+
+
 # ----------------------------------------------------------------------------- the dgrad's column-tile ceiling
 def test_dgrad_at_the_column_tile_ceiling(B, mode):
     """The cross-tile data gradient needs every column tile of a row block in
