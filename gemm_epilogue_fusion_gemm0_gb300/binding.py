@@ -112,7 +112,7 @@ def _stream_ptr(stream, device=None) -> int:
         stream = torch.cuda.current_stream(device)
     if not hasattr(stream, "cuda_stream"):
         return int(stream)  # a raw cudaStream_t handle
-    if device is not None and stream.device != torch.device(device):
+    if device is not None and stream.device != device:
         raise ValueError(f"the stream is on {stream.device}, the call's tensors on {device}")
     return int(stream.cuda_stream)
 
@@ -158,6 +158,9 @@ class _Call:
         return ws.data_ptr(), ws.numel() * ws.element_size()
 
     def run(self, fn, *args, stream=None) -> None:
+        if self.device.index == torch.cuda.current_device():
+            _check(fn(*args, _stream_ptr(stream, self.device)), self.where)
+            return
         with torch.cuda.device(self.device):
             _check(fn(*args, _stream_ptr(stream, self.device)), self.where)
 
