@@ -81,6 +81,8 @@ EXPORTS = {
     "coda_set_col_plan": (_st, [ctypes.c_int]),
     "coda_set_serpentine_k": (_st, [ctypes.c_int]),
     "coda_get_serpentine_k": (ctypes.c_int, []),
+    "coda_set_dgrad_pieces": (_st, [ctypes.c_int]),
+    "coda_get_dgrad_pieces": (ctypes.c_int, []),
     "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
                            _vp, _vp, _vp, _sz, _vp]),
@@ -384,6 +386,16 @@ def coda_set_serpentine_k(enable: int) -> None:
 
 def coda_get_serpentine_k() -> int:
     return int(_lib.coda_get_serpentine_k())
+
+
+def coda_set_dgrad_pieces(enable: int) -> None:
+    """1 (default): the CTA-pair data gradients may cut their last row blocks' tiles into K
+    pieces when whole tiles would leave the last wave partly idle; 0: whole tiles."""
+    _check(_lib.coda_set_dgrad_pieces(int(enable)), "coda_set_dgrad_pieces")
+
+
+def coda_get_dgrad_pieces() -> int:
+    return int(_lib.coda_get_dgrad_pieces())
 
 
 def coda_get_mma_mode() -> int:

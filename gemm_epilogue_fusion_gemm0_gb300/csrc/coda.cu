@@ -654,30 +654,123 @@ std::atomic<int> g_dgrad_kserp{0};  // 1: the data gradients load every other wa
 // Most column tiles per row block the data-gradient workspace is sized for.
 int64_t dgrad_max_col_tiles(int64_t d) { return 2 * cdiv(d, kBN); }
 
-// The data gradient's workspace: qpart [2 * max tiles][M] fp32, then flags
-// [slabs][max tiles] (a launch uses the first slabs * nt), then the 256-byte slot
-// of the launch counter.
+// Partial slots (each two CTA halves of 128 x 256 fp32) the data-gradient
+// workspace holds for the pieces of its last row blocks (PieceWork): three per
+// 256 x 256 tile, at most 192 (48 MiB).
+int64_t dgrad_piece_slots(int64_t M, int64_t d) {
+  return std::min<int64_t>(3 * cdiv(M, kPairBM) * cdiv(d, kBN), 192);
+}
+
+// The data gradient's workspace: the 256-byte slot of the launch counter, qpart
+// [2 * max tiles][M] fp32, flags [slabs][max tiles] (a launch uses the first
+// slabs * nt), then the pieces' partial slots and their flags.
 struct DgradWs {
+  uint64_t* epoch;
   float* qpart;
   uint64_t* flags;
-  uint64_t* epoch;
+  float* ppart;      // [pslots][2 CTAs][128 x 256]
+  uint64_t* pflags;  // [pslots][2 CTAs]
+  int64_t pslots;
 };
 
-// [slot | qpart | flags]
+// [slot | qpart | flags | piece partials | piece flags]
 size_t dgrad_ws_bytes(int64_t M, int64_t d) {
   const int64_t slabs = 2 * cdiv(M, kPairBM), nt = dgrad_max_col_tiles(d);
+  const int64_t ps = dgrad_piece_slots(M, d);
   return kSlotBytes + align256(static_cast<size_t>(2 * nt) * M * 4) +
-         align256(static_cast<size_t>(slabs) * nt * 8);
+         align256(static_cast<size_t>(slabs) * nt * 8) +
+         align256(static_cast<size_t>(ps) * 2 * kSkSlotFloats * 4) +
+         align256(static_cast<size_t>(ps) * 2 * 8);
 }
 
 DgradWs dgrad_ws(void* base, int64_t M, int64_t d) {
+  const int64_t slabs = 2 * cdiv(M, kPairBM), nt = dgrad_max_col_tiles(d);
   char* p = static_cast<char*>(base);
   DgradWs w;
   w.epoch = reinterpret_cast<uint64_t*>(p);
-  w.qpart = reinterpret_cast<float*>(p + kSlotBytes);
-  w.flags = reinterpret_cast<uint64_t*>(
-      p + kSlotBytes + align256(static_cast<size_t>(2 * dgrad_max_col_tiles(d)) * M * 4));
+  p += kSlotBytes;
+  w.qpart = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(2 * nt) * M * 4);
+  w.flags = reinterpret_cast<uint64_t*>(p);
+  p += align256(static_cast<size_t>(slabs) * nt * 8);
+  w.pslots = dgrad_piece_slots(M, d);
+  w.ppart = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(w.pslots) * 2 * kSkSlotFloats * 4);
+  w.pflags = reinterpret_cast<uint64_t*>(p);
   return w;
+}
+
+// ---------------------------------------------------------------------------
+// Piece split of the CTA-pair data gradient's last row blocks (gemm_pair.cuh,
+// PieceWork).
+// ---------------------------------------------------------------------------
+std::atomic<int> g_dgrad_pieces{1};  // 1: the planner below may cut the last row blocks
+
+struct PiecePlan {
+  int dp_tiles = 0, pieces = 0, lvl_first = 0, lvl = 0;
+};
+
+// The k last row blocks (R = k nt tiles, R <= npairs) cut into P pieces of at
+// least 16 k-blocks, dealt as PieceWork deals them.  The model counts each
+// pair's work in tiles: a whole tile 1, a piece 1.5 / P (pieces run slower
+// than their share of K: fewer pairs share each operand slice in L2; 1.5 fits
+// the GB300 measurements of 14 shapes, from 0.88 to 1.08 of the whole-tile
+// time), plus, for the owners that finish the launch, about 2 us per partial
+// they add (a k-block takes about 0.33 us).  A plan is taken when it shortens
+// the busiest pair's work by at least 3 %.
+PiecePlan plan_dgrad_pieces(int mt, int nt, int npairs, int64_t nk, int64_t slots) {
+  PiecePlan best;
+  if (npairs < 2 || nt < 1 || nk < 32) return best;
+  const int64_t total = static_cast<int64_t>(mt) * nt;
+  const double whole = static_cast<double>((total + npairs - 1) / npairs);
+  double best_t = 0.97 * whole;
+  for (int k = 1; k <= mt && k * nt <= npairs; ++k) {
+    const int64_t R = static_cast<int64_t>(k) * nt, dp = total - R;
+    const int64_t W = dp / npairs, E = dp % npairs;
+    for (int P = 2; P <= 8 && nk / P >= 16; ++P) {
+      if (R * (P - 1) > slots) break;
+      int lvl_first = npairs, lvl = 0;
+      if (E > 0) {
+        lvl_first = static_cast<int>(E);
+        lvl = static_cast<int>(std::min<int64_t>(P, (P - 1) * R / (npairs - E)));
+      }
+      const int64_t rr = R * P - static_cast<int64_t>(npairs - lvl_first) * lvl;
+      if (rr < R) continue;
+      double mx = 0.0;
+      for (int p = 0; p < npairs; ++p) {
+        const int64_t pieces = (p >= lvl_first ? lvl : 0) + rr / npairs + (p < rr % npairs ? 1 : 0);
+        mx = std::max(mx, static_cast<double>(W + (p < E ? 1 : 0)) + 1.5 * pieces / P);
+      }
+      const double t = mx + (P - 1) * 6.0 / static_cast<double>(nk);
+      if (t < best_t) {
+        best_t = t;
+        best.dp_tiles = static_cast<int>(dp);
+        best.pieces = P;
+        best.lvl_first = lvl_first;
+        best.lvl = lvl;
+      }
+    }
+  }
+  return best;
+}
+
+// The piece split's parameters for a launch on `npairs` pairs (kNoSplitTail
+// when no plan pays or the switch is off).
+SkParams dgrad_pieces(const DgradWs& dw, int mt, int nt, int npairs, int64_t nk, uint64_t salt) {
+  SkParams sk = kNoSplitTail;
+  if (g_dgrad_pieces.load() == 0) return sk;
+  const PiecePlan pp = plan_dgrad_pieces(mt, nt, npairs, nk, dw.pslots);
+  if (pp.pieces == 0) return sk;
+  sk.dp_tiles = pp.dp_tiles;
+  sk.part = dw.ppart;
+  sk.flags = dw.pflags;
+  sk.epoch = dw.epoch;
+  sk.slots = static_cast<int>(dw.pslots);
+  sk.salt = salt;
+  sk.pieces = pp.pieces;
+  sk.lvl_first = pp.lvl_first;
+  sk.lvl = pp.lvl;
+  return sk;
 }
 
 // Largest per-pair load of a plan with tiles handed out round-robin in
@@ -828,7 +921,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
   cp.kserp = g_dgrad_kserp.load();
   const int nt = cp.nt > 0 ? cp.nt : static_cast<int>(cdiv(d, kBN));
-  const int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
+  int units = pair ? std::min(max_pairs, mt * nt) : std::min(sms, mt * nt);
   if (nt > units) return CODA_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap mA, mB;
@@ -837,6 +930,11 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   if (!ok) return CODA_ERR_LAUNCH;
 
   const DgradWs dw = dgrad_ws(workspace, M, d);
+  const uint64_t salt = next_salt();
+  // the last row blocks cut into K pieces, when the planner finds it pays (every pair runs)
+  const SkParams sk =
+      (pair && cp.nt == 0) ? dgrad_pieces(dw, mt, nt, max_pairs, cdiv(N1, kBK), salt) : kNoSplitTail;
+  if (sk.pieces > 0) units = max_pairs;
   EpiRmsNormBackward::Params p = {};
   p.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
@@ -845,11 +943,11 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   p.qpart = dw.qpart;
   p.flags = dw.flags;
   p.epoch = dw.epoch;
-  p.salt = next_salt();
+  p.salt = salt;
   cudaError_t e =
       pair ? launch(kPairDgrad, 2 * units, kThreads, kPairDgradSmem, stream, true, mA, mB,
-                    static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p, kNoSplitTail,
-                    cp, g_timeout_ns.load())
+                    static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p, sk, cp,
+                    g_timeout_ns.load())
            : launch(kDgrad, units, kThreads, kDgradSmem, stream, true, mA, mB,
                     static_cast<int>(M), static_cast<int>(d), static_cast<int>(N1), 1, p,
                     g_timeout_ns.load());
@@ -989,7 +1087,7 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   ColPlan cp = pair ? plan_dgrad_cols(mt, d, N1, max_pairs) : kNoColPlan;
   cp.kserp = g_dgrad_kserp.load();
   const int nt1 = cp.nt > 0 ? cp.nt : nt;
-  const int units = pair ? std::min(max_pairs, mt * nt1) : std::min(sms, mt * nt1);
+  int units = pair ? std::min(max_pairs, mt * nt1) : std::min(sms, mt * nt1);
   if (nt1 > units) return CODA_ERR_UNSUPPORTED_SHAPE;
   const int slabs = pair ? 2 * mt : mt;
 
@@ -1027,11 +1125,15 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.flags = dw.flags;
   p.epoch = dw.epoch;
   p.salt = salt;
+  const SkParams skd = (pair && cp.nt == 0)
+                           ? dgrad_pieces(dw, mt, nt1, max_pairs, cdiv(N1, kBK), salt)
+                           : kNoSplitTail;
+  if (skd.pieces > 0) units = max_pairs;
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
   p.gpart = gpart;
   cudaError_t e = pair ? launch(kPairDgradFull, 2 * units, kThreads, kPairDgradFullSmem, stream,
-                                true, mDy, mW1, Mi, di, N1i, 1, p, kNoSplitTail, cp, tmo)
+                                true, mDy, mW1, Mi, di, N1i, 1, p, skd, cp, tmo)
                        : launch(kDgradFull, units, kThreads, kDgradFullSmem, stream, true, mDy, mW1,
                                 Mi, di, N1i, 1, p, tmo);
   if (e != cudaSuccess) {
@@ -1250,6 +1352,14 @@ coda_status_t coda_set_serpentine_k(int enable) {
 }
 
 int coda_get_serpentine_k(void) { return g_dgrad_kserp.load(); }
+
+coda_status_t coda_set_dgrad_pieces(int enable) {
+  if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;
+  g_dgrad_pieces.store(enable);
+  return CODA_OK;
+}
+
+int coda_get_dgrad_pieces(void) { return g_dgrad_pieces.load(); }
 
 coda_status_t coda_set_fold_rowreduce(int enable) {
   if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;

@@ -78,9 +78,13 @@ struct SkParams {
   uint64_t* epoch;  // launch counter (any initial value); null when the tail is not split
   int slots;        // S, the partial slots the workspace holds
   uint64_t salt;    // this call's random value; a flag holds token ^ salt
+  // Piece split (policies with kSplitTail = false, see PieceWork); 0: none
+  int pieces;       // P, K pieces per tile past dp_tiles
+  int lvl_first;    // pairs from lvl_first on take lvl pieces each before the others
+  int lvl;
 };
 
-constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr, 0, 0};
+constexpr SkParams kNoSplitTail = {0x7fffffff, nullptr, nullptr, nullptr, 0, 0, 0, 0, 0};
 
 // A policy opts out of the split tail (its epilogue waits on other tiles) with
 // `static constexpr bool kSplitTail = false;`; the kernel then compiles without it.
@@ -95,6 +99,7 @@ constexpr int kItemTail = 2;   // k-blocks [kb0, nk): writes the partial
 
 struct WorkItem {
   int tile, kb0, kb1, kind;
+  int piece = 0;  // the K piece of a pieced tile (PieceWork)
 };
 
 // The split items of one CTA pair, in order (the same sequence in the producer,
@@ -117,6 +122,61 @@ struct SplitWork {
     w.kb1 = static_cast<int>(min(static_cast<long long>(nk), w.kb0 + (kend - kpos)));
     w.kind = w.kb0 > 0 ? kItemTail : (w.kb1 < nk ? kItemOwner : kItemWhole);
     kpos += w.kb1 - w.kb0;
+    return true;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Piece split, for policies whose epilogue waits on other tiles (the data
+// gradient's row statistic: kSplitTail = false).  The stream-K tail above cuts
+// each pair's share of the last tiles at a different K offset, so the pairs
+// stop walking K in step and the long-K operands stop being shared in L2; and
+// a split tile that waited on its row block while holding TMEM could block the
+// pair's later items.  Instead, with R tiles past dp_tiles (whole row blocks,
+// R <= pairs):
+//   - every tile past dp_tiles is cut into P pieces along K, piece q holding
+//     k-blocks [q nk / P, (q + 1) nk / P);
+//   - the R P pieces are dealt in piece-major order (unit u = q R + tile): the
+//     first (U - lvl_first) lvl units go, lvl at a time, to the pairs from
+//     lvl_first on (those with one whole tile fewer), the rest round-robin to
+//     pairs 0, 1, ...; so at any time only two or three piece indices are in
+//     flight and the pairs of each walk K in step;
+//   - piece P - 1 of a tile is its owner: the last R units, dealt last, so an
+//     owner is the last item of its pair and no pair holds two; the host
+//     keeps the levelled units clear of them.  Every other piece writes its
+//     fp32 accumulator to a partial slot and publishes a flag; the owner waits
+//     for its tile's P - 1 flags, adds the partials into its accumulator and
+//     runs the policy (which may then wait on its row block's other owners).
+// Pieces never wait and owners wait only on pieces and on other owners, all
+// resident (a cooperative launch), so every wait ends.  Slots: tile
+// dp_tiles + i, piece q < P - 1, CTA r is slot (i (P - 1) + q) 2 + r.
+// ---------------------------------------------------------------------------
+struct PieceWork {
+  int R, P, nk, base, npairs, pair, lvl_first, lvl, lvl_units, rr_units;
+  int i = 0, j = 0;
+  __device__ __forceinline__ PieceWork(const SkParams& sk, int pair_, int npairs_, int num_tiles,
+                                       int nk_)
+      : R(num_tiles - sk.dp_tiles), P(sk.pieces), nk(nk_), base(sk.dp_tiles), npairs(npairs_),
+        pair(pair_), lvl_first(sk.lvl_first), lvl(sk.lvl) {
+    lvl_units = (npairs - lvl_first) * lvl;
+    rr_units = R * P - lvl_units;
+  }
+  __device__ __forceinline__ bool next(WorkItem& w) {
+    int u;
+    if (pair >= lvl_first && i < lvl) {
+      u = (pair - lvl_first) * lvl + i++;
+    } else {
+      const int v = pair + j * npairs;
+      if (v >= rr_units) return false;
+      ++j;
+      u = lvl_units + v;
+    }
+    const int q = u / R;
+    w.tile = base + (u - q * R);
+    w.kb0 = static_cast<int>(static_cast<long long>(q) * nk / P);
+    w.kb1 = static_cast<int>(static_cast<long long>(q + 1) * nk / P);
+    w.kind = q == P - 1 ? kItemOwner : kItemTail;
+    w.piece = q;
     return true;
   }
 };
@@ -276,7 +336,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const WaitCtl wc{timeout_ns, &g_coda_status, abort_flag};
   constexpr bool kSplit = SplitsTail<Epi>::value;
   // whole tiles below dp_end; a split needs the slots (never planned without them)
-  const int dp_end = (kSplit && sk.part != nullptr) ? min(sk.dp_tiles, num_tiles) : num_tiles;
+  // tiles past dp_end cut into K pieces (PieceWork), for the policies without a split tail
+  const bool pieced = kPlanCapable && !planned && sk.pieces > 1 && sk.part != nullptr;
+  const int dp_end =
+      ((kSplit && sk.part != nullptr) || pieced) ? min(sk.dp_tiles, num_tiles) : num_tiles;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -389,6 +452,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         WorkItem w;
         while (ok && work.next(w)) loads(w);
       }
+      if (kPlanCapable && pieced) {
+        PieceWork work(sk, pair, npairs, num_tiles, nk);
+        WorkItem w;
+        while (ok && work.next(w)) loads(w);
+      }
       if (!ok && leader) {
         // Let every issued copy (of both CTAs) land before the pair can exit.
         for (int i = 0; i < kPairStages; ++i)
@@ -465,6 +533,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           WorkItem w;
           for (; ok && work.next(w); ++it) mmas(w);
         }
+        if (kPlanCapable && pieced) {
+          PieceWork work(sk, pair, npairs, num_tiles, nk);
+          WorkItem w;
+          for (; ok && work.next(w); ++it) mmas(w);
+        }
         // Always signal `drain` in both CTAs once every MMA issued here is done.
         umma_commit_pair_mc(bar_drain, 0x3);
       }
@@ -524,7 +597,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
       }
-      if (!kSplit || w.kind != kItemTail) {
+      if (kPlanCapable && w.kind != kItemWhole) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
+        const int p1 = sk.pieces - 1;
+        const size_t first = static_cast<size_t>(w.tile - sk.dp_tiles) * p1;  // the tile's slots
+        if constexpr (kChecked) {
+          if (!epi_all(checked(sk.part != nullptr && w.tile >= sk.dp_tiles &&
+                                   (first + p1) * 2 <= 2 * static_cast<size_t>(sk.slots),
+                               kChkSplitSlot)))
+            return false;  // leave the role (every epilogue thread agrees)
+        }
+        if (w.kind == kItemTail) {
+          const size_t slot = (first + w.piece) * 2 + rank;
+          sk_write_partial(taddr, reinterpret_cast<float4*>(sk.part + slot * kSkSlotFloats), half,
+                           row);
+          __threadfence();
+          named_bar_sync(1, kEpiThreads);
+          if (threadIdx.x == kEpiFirstThread)
+            st_release_gpu_u64(sk.flags + slot, launch_tag(sk.epoch, sk.salt));
+        } else {
+          if (threadIdx.x == kEpiFirstThread) {
+            const uint64_t tag = launch_tag(sk.epoch, sk.salt);
+            for (int q = 0; q < p1; ++q)
+              if (!flag_wait(sk.flags + (first + q) * 2 + rank, tag, wc, kSitePieces)) break;
+            __threadfence();
+          }
+          named_bar_sync(1, kEpiThreads);
+          for (int q = 0; q < p1; ++q)
+            sk_add_partial(taddr,
+                           reinterpret_cast<const float4*>(sk.part +
+                                                           ((first + q) * 2 + rank) * kSkSlotFloats),
+                           half, row);
+          tc_fence_before();
+          named_bar_sync(1, kEpiThreads);
+          tc_fence_after();
+        }
+      }
+      if (w.kind != kItemTail) {
         TileCtx c;
         c.taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * kBN;
         c.mb = mb * 2 + static_cast<int>(rank);  // this CTA's 128-row slab
@@ -550,6 +659,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int t = pair; go && t < dp_end; t += npairs, ++it) go = drain(WorkItem{t, 0, nk, kItemWhole});
     if constexpr (kSplit) {
       SplitWork work(pair, npairs, num_tiles, dp_end, nk);
+      WorkItem w;
+      for (; go && work.next(w); ++it) go = drain(w);
+    }
+    if (kPlanCapable && pieced) {
+      PieceWork work(sk, pair, npairs, num_tiles, nk);
       WorkItem w;
       for (; go && work.next(w); ++it) go = drain(w);
     }

@@ -92,6 +92,7 @@ enum WaitSite : uint32_t {
   kSiteSelftestBarrier = 7,
   kSiteSelftestFlag = 8,
   kSiteSplitTail = 9,  // owner of a split tile waiting for its partial
+  kSitePieces = 10,    // owner of a tile cut into K pieces waiting for the pieces' partials
 };
 
 struct WaitCtl {

@@ -91,8 +91,10 @@ CODA_API size_t coda_fwd_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /* Bytes of device workspace coda_bwd_dgrad needs: the 256-byte slot holding
  * the launch counter and its arrival word, fp32 partial row statistics (two
- * per row and column tile) and one 64-bit completion flag per 128-row slab and
- * column tile. */
+ * per row and column tile), one 64-bit completion flag per 128-row slab and
+ * column tile, and min(3 T, 192) fp32 partial accumulators of 256 x 256 with
+ * their flags for the pieces of the last row blocks (T = the count of
+ * 256 x 256 tiles; see coda_set_dgrad_pieces). */
 CODA_API size_t coda_bwd_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1);
 
 /*
@@ -342,6 +344,20 @@ CODA_API coda_status_t coda_set_col_plan(int enable);
  * coda_get_serpentine_k returns the current setting.  Process-wide. */
 CODA_API coda_status_t coda_set_serpentine_k(int enable);
 CODA_API int coda_get_serpentine_k(void);
+
+/* 1 (the default): the CTA-pair data gradients (coda_bwd_dgrad and launch 1
+ * of coda_bwd) may cut the tiles of their last row blocks into P pieces along
+ * K when whole 256 x 256 tiles would leave the last wave of CTA pairs partly
+ * idle.  The pieces are dealt so that the pairs keep walking K in step, every
+ * piece but the last of a tile writes an fp32 partial to the workspace, and
+ * the pair holding the last piece adds them before the epilogue.  A host-side
+ * model picks the row blocks and P (at llama7b: the last 4 row blocks in 4
+ * pieces, 6.75 tiles of work on the busiest pair instead of 7).  Results
+ * differ from whole tiles only in fp32 summation order.  0: whole tiles.
+ * Returns CODA_ERR_INVALID_ARG for any other value; coda_get_dgrad_pieces
+ * returns the current setting.  Process-wide. */
+CODA_API coda_status_t coda_set_dgrad_pieces(int enable);
+CODA_API int coda_get_dgrad_pieces(void);
 
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records

@@ -76,6 +76,9 @@ def main():
         clean(f"split tail {M}x{d}x{N1}")
     T.test_one_workspace_for_split_forward_and_dgrad(B)
     clean("one workspace for a split forward and the dgrad")
+    for shape, slots in T.PIECE_SHAPES:
+        T.test_dgrad_pieces_match_oracle(B, shape, slots)
+        clean(f"dgrad in K pieces {shape}")
     for (M, d, N1) in T.SWEEP_SHAPES[:4]:
         T.test_split_tail_shape_sweep(B, M, d, N1)
         clean(f"split sweep {M}x{d}x{N1}")

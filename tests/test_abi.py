@@ -68,10 +68,14 @@ def test_workspace_sizes(lib):
         256 + M * d * 2 + 32 * M * 4 + _split_tail_bytes(M, d, N1))
     assert lib.coda_fwd_unfused_workspace_bytes(M, d, N1) == 256 + M * d * 2
     # the slot, qpart [2 * 32, M] fp32 + flags [2 * ceil(M/256) * 32] u64 (one per 128-row
-    # slab and column tile, for up to 2 * ceil(d/256) = 32 column tiles per row block)
-    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == 256 + 64 * M * 4 + 64 * 32 * 8
-    # 256; 2 * 2 x 300 fp32 = 4800 -> 4864; 4 slabs x 2 tiles x 8 = 64 -> 256
-    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 256 + 4864 + 256
+    # slab and column tile, for up to 2 * ceil(d/256) = 32 column tiles per row block), then
+    # min(3 T, 192) partial slots of 2 x 128 x 256 fp32 and their 2 flags each for the
+    # pieces of the last row blocks (T = 32 x 16 tiles of 256 x 256)
+    assert lib.coda_bwd_dgrad_workspace_bytes(M, d, N1) == (
+        256 + 64 * M * 4 + 64 * 32 * 8 + 192 * 262144 + 192 * 16)
+    # 256; 2 * 2 x 300 fp32 = 4800 -> 4864; 4 slabs x 2 tiles x 8 = 64 -> 256; 3 x 2 x 1
+    # tiles = 6 slots of 256 KiB; 6 x 16 = 96 -> 256
+    assert lib.coda_bwd_dgrad_workspace_bytes(300, 256, 512) == 256 + 4864 + 256 + 6 * 262144 + 256
     assert lib.coda_fwd_workspace_bytes(0, d, N1) == 0
     assert _split_tail_bytes(300, 328, 776) == 8 * 262144 + 256  # 2 x 4 tiles
     assert lib.coda_fwd_workspace_bytes(300, 328, 776) == (  # ragged: rounded up

@@ -917,6 +917,104 @@ def test_one_workspace_for_split_forward_and_dgrad(B):
     check("dh", f64(dh), bref.dh, TOL_DH)
 
 
+# ----------------------------------------------------------------------------- the dgrad's last row blocks in K pieces
+# Shapes whose last row blocks the planner cuts into K pieces on 76 CTA pairs,
+# with the partial slots (tiles x (pieces - 1)) that uses: (last row blocks,
+# pieces) = (1, 3) ragged everywhere and (2, 3), both with the pairs that hold a
+# whole tile fewer taking pieces first, and (1, 4) with no such levelling (the
+# whole tiles fill whole waves).
+PIECE_SHAPES = [((2000, 5000, 5064), 20 * 2), ((1536, 4096, 8192), 32 * 2), ((5000, 4096, 6000), 16 * 3)]
+
+
+def piece_flags(ws, M, d):
+    """The piece flags of the data gradient's workspace (after the launch
+    counter's slot, the partial row statistics, the row flags and the piece
+    partials), as unsigned 64-bit values."""
+    a = lambda n: (n + 255) // 256 * 256
+    ntmax, slabs = 2 * ((d + 255) // 256), 2 * ((M + 255) // 256)
+    slots = min(3 * ((M + 255) // 256) * ((d + 255) // 256), 192)
+    f0 = 256 + a(2 * ntmax * M * 4) + a(slabs * ntmax * 8) + a(slots * 2 * 128 * 256 * 4)
+    return [int(v) & U64 for v in ws[f0:f0 + slots * 2 * 8].view(torch.int64).cpu()]
+
+
+@pytest.mark.parametrize("shape,slots", PIECE_SHAPES)
+def test_dgrad_pieces_match_oracle(B, shape, slots):
+    """The CTA-pair data gradient with its last row blocks cut into K pieces
+    (the default where the planner finds it pays) and with whole tiles: both
+    match the oracle on every row and each other to fp32 summation order; with
+    pieces every piece but the last of each tile published its partial's flag
+    (two CTA halves each) with the launch's tag, which the row flags carry too."""
+    M, d, N1 = shape
+    dev = torch.device("cuda:0")
+    t = synth.make_dgrad_inputs(M, d, N1, seed=61)
+    r = oracle.inverse_rms(oracle.mean_square(f64(t["h"])), 1e-5).astype(np.float32)
+    g = {k: v.to(dev) for k, v in t.items()}
+    rg = torch.from_numpy(r).to(dev)
+    ws = torch.zeros(B.coda_bwd_dgrad_workspace_bytes(M, d, N1), dtype=torch.uint8, device=dev)
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    old_mode, old_pieces = B.coda_get_mma_mode(), B.coda_get_dgrad_pieces()
+    B.coda_set_mma_mode(1)
+    outs = {}
+    try:
+        for pieces in (1, 0):
+            B.coda_set_dgrad_pieces(pieces)
+            outs[pieces] = B.coda_bwd_dgrad(g["dy"], g["W1"], g["h"], rg, g["gamma"], ws=ws)
+            torch.cuda.synchronize()
+            st, detail = B.coda_get_device_status()
+            assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+            if pieces:
+                tag = int(launch_counter(ws)) & U64
+                ntmax = 2 * ((d + 255) // 256)
+                f0 = 256 + (2 * ntmax * M * 4 + 255) // 256 * 256
+                row_tag = int(ws[f0:f0 + 8].view(torch.int64).item()) & U64
+                published = sum(1 for v in piece_flags(ws, M, d) if v == row_tag)
+                if pairs == 76:
+                    assert published == 2 * slots, (published, slots)
+                assert published > 0 and tag != 0
+    finally:
+        B.coda_set_dgrad_pieces(old_pieces)
+        B.coda_set_mma_mode(old_mode)
+    bref = oracle.backward_dgrad(f64(t["dy"]), f64(t["W1"]), f64(t["h"]), r.astype(np.float64),
+                                 f64(t["gamma"]))
+    for pieces, dh in outs.items():
+        check(f"dh (pieces {pieces})", f64(dh), bref.dh, TOL_DH)
+    check("dh pieces against whole tiles", f64(outs[1]), f64(outs[0]), 1e-3)
+
+
+def test_dgrad_pieces_replay_from_a_cuda_graph(B):
+    """The data gradient at a shape cut into pieces, captured once and replayed
+    twice on the same buffers: each replay equals the eager call bit for bit
+    (the piece flags take a fresh token at every replay)."""
+    M, d, N1 = PIECE_SHAPES[0][0]
+    dev = torch.device("cuda:0")
+    t = synth.make_dgrad_inputs(M, d, N1, seed=62)
+    r = oracle.inverse_rms(oracle.mean_square(f64(t["h"])), 1e-5).astype(np.float32)
+    g = {k: v.to(dev) for k, v in t.items()}
+    rg = torch.from_numpy(r).to(dev)
+    ws = B.workspace(B.coda_bwd_dgrad_workspace_bytes(M, d, N1), dev)
+    dh = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        call = lambda: B.coda_bwd_dgrad(g["dy"], g["W1"], g["h"], rg, g["gamma"], dh=dh, ws=ws,
+                                        stream=torch.cuda.current_stream())
+        call()
+        torch.cuda.synchronize()
+        ref = dh.clone()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        for _ in range(2):
+            dh.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            st, detail = B.coda_get_device_status()
+            assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+            assert torch.equal(dh, ref)
+    finally:
+        B.coda_set_mma_mode(old)
+
+
 # ----------------------------------------------------------------------------- the dgrad's column-tile ceiling
 def test_dgrad_at_the_column_tile_ceiling(B, mode):
     """The cross-tile data gradient needs every column tile of a row block in
