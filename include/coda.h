@@ -351,8 +351,10 @@ CODA_API int coda_get_serpentine_k(void);
  * idle.  The pieces are dealt so that the pairs keep walking K in step, every
  * piece but the last of a tile writes an fp32 partial to the workspace, and
  * the pair holding the last piece adds them before the epilogue.  A host-side
- * model picks the row blocks and P (at llama7b: the last 4 row blocks in 4
- * pieces, 6.75 tiles of work on the busiest pair instead of 7).  Results
+ * model, fitted to GB300 measurements (a piece runs about 1.5 times its share
+ * of K), picks the row blocks and P, and keeps whole tiles unless the cut
+ * saves at least 3 % (llama1b's data gradient: the last 4 row blocks in 2
+ * pieces, 8.9 % faster; llama7b and llama70b keep whole tiles).  Results
  * differ from whole tiles only in fp32 summation order.  0: whole tiles.
  * Returns CODA_ERR_INVALID_ARG for any other value; coda_get_dgrad_pieces
  * returns the current setting.  Process-wide. */
