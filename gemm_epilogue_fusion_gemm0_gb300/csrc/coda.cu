@@ -712,12 +712,14 @@ struct PiecePlan {
 
 // The k last row blocks (R = k nt tiles, R <= npairs) cut into P pieces of at
 // least 16 k-blocks, dealt as PieceWork deals them.  The model counts each
-// pair's work in tiles: a whole tile 1, a piece 1.5 / P (pieces run slower
-// than their share of K: fewer pairs share each operand slice in L2; 1.5 fits
-// the GB300 measurements of 14 shapes, from 0.88 to 1.08 of the whole-tile
-// time), plus, for the owners that finish the launch, about 2 us per partial
-// they add (a k-block takes about 0.33 us).  A plan is taken when it shortens
-// the busiest pair's work by at least 3 %.
+// pair's work in tiles: a whole tile 1, a piece 1.5 / P (pieces finish later
+// than their share of K: a pair's last whole tile may wait, holding one of
+// the two TMEM accumulators, for its row block's tiles in the next wave, which
+// a short piece after it cannot cover; 1.5 fits the GB300 measurements of 14
+// shapes, 0.88 to 1.08 of the whole-tile time), plus, for the owners that
+// finish the launch, about 2 us per partial they add (a k-block takes about
+// 0.33 us).  A plan is taken when it shortens the busiest pair's work by at
+// least 3 %.
 PiecePlan plan_dgrad_pieces(int mt, int nt, int npairs, int64_t nk, int64_t slots) {
   PiecePlan best;
   if (npairs < 2 || nt < 1 || nk < 32) return best;
