@@ -356,8 +356,9 @@ def col_plan_ab(B, stream, barrier, call):
     """Per-call medians, calls interleaved one by one (see interleaved), of
     `call` (a data gradient) as by default against K loaded forwards in every
     wave (coda_set_serpentine_k(0)), K loaded backwards in every other wave
-    ((1)) and the column plans (coda_set_col_plan(1): widths in steps of 16;
-    (2): multiples of 64)."""
+    ((1)), the column plans (coda_set_col_plan(1): widths in steps of 16;
+    (2): multiples of 64) and whole tiles only (coda_set_dgrad_pieces(0): no
+    K pieces for the last row blocks)."""
     def planned(mode):
         def f():
             B.coda_set_col_plan(mode)
@@ -376,8 +377,15 @@ def col_plan_ab(B, stream, barrier, call):
             finally:
                 B.coda_set_serpentine_k(old)
         return f
+    def whole_tiles():
+        old = B.coda_get_dgrad_pieces()
+        B.coda_set_dgrad_pieces(0)
+        try:
+            call()
+        finally:
+            B.coda_set_dgrad_pieces(old)
     forms = {"col_plan_16": planned(1), "col_plan_64": planned(2), "k_forward": k_order(0),
-             "k_serpentine": k_order(1), "default": call}
+             "k_serpentine": k_order(1), "whole_tiles": whole_tiles, "default": call}
     for f in forms.values():
         f()
     return interleaved(stream, barrier, forms)
