@@ -981,6 +981,22 @@ def test_dgrad_pieces_match_oracle(B, shape, slots):
     check("dh pieces against whole tiles", f64(outs[1]), f64(outs[0]), 1e-3)
 
 
+def test_full_backward_with_pieces_matches_oracle(B):
+    """coda_bwd at a shape whose data-gradient launch (with the full backward's
+    extras: residual gradient, h2 and the dgamma partials, all formed by the
+    owners of the pieced tiles) cuts its last row block into K pieces on 76 CTA
+    pairs: every gradient against the oracle, dW1 reading the h2 those owners
+    wrote."""
+    M, d, N1 = PIECE_SHAPES[0][0]
+    old_mode, old_pieces = B.coda_get_mma_mode(), B.coda_get_dgrad_pieces()
+    B.coda_set_mma_mode(1)
+    try:
+        run_full_bwd(B, M, d, N1, 1e-5, seed=63)
+    finally:
+        B.coda_set_dgrad_pieces(old_pieces)
+        B.coda_set_mma_mode(old_mode)
+
+
 def test_dgrad_pieces_replay_from_a_cuda_graph(B):
     """The data gradient at a shape cut into pieces, captured once and replayed
     twice on the same buffers: each replay equals the eager call bit for bit
