@@ -712,20 +712,22 @@ struct PiecePlan {
 
 // The k last row blocks (R = k nt tiles, R <= npairs) cut into P pieces of at
 // least 16 k-blocks, dealt as PieceWork deals them.  The model counts each
-// pair's work in tiles: a whole tile 1, a piece 1.5 / P (pieces finish later
-// than their share of K: a pair's last whole tile may wait, holding one of
-// the two TMEM accumulators, for its row block's tiles in the next wave, which
-// a short piece after it cannot cover; 1.5 fits the GB300 measurements of 14
+// pair's work in tiles: a whole tile 1, a piece piece_cost / P (for the data
+// gradient with the row statistic 1.5: pieces finish later than their share
+// of K there, because a pair's last whole tile may wait, holding one of the
+// two TMEM accumulators, for its row block's tiles in the next wave, which a
+// short piece after it cannot cover; 1.5 fits the GB300 measurements of 14
 // shapes, 0.88 to 1.08 of the whole-tile time), plus, for the owners that
 // finish the launch, about 2 us per partial they add (a k-block takes about
 // 0.33 us).  A plan is taken when it shortens the busiest pair's work by at
 // least 3 %.
-PiecePlan plan_dgrad_pieces(int mt, int nt, int npairs, int64_t nk, int64_t slots) {
+PiecePlan plan_dgrad_pieces(int mt, int nt, int npairs, int64_t nk, int64_t slots,
+                            double piece_cost = 1.5, double min_gain = 0.03) {
   PiecePlan best;
   if (npairs < 2 || nt < 1 || nk < 32) return best;
   const int64_t total = static_cast<int64_t>(mt) * nt;
   const double whole = static_cast<double>((total + npairs - 1) / npairs);
-  double best_t = 0.97 * whole;
+  double best_t = (1.0 - min_gain) * whole;
   for (int k = 1; k <= mt && k * nt <= npairs; ++k) {
     const int64_t R = static_cast<int64_t>(k) * nt, dp = total - R;
     const int64_t W = dp / npairs, E = dp % npairs;
@@ -741,7 +743,7 @@ PiecePlan plan_dgrad_pieces(int mt, int nt, int npairs, int64_t nk, int64_t slot
       double mx = 0.0;
       for (int p = 0; p < npairs; ++p) {
         const int64_t pieces = (p >= lvl_first ? lvl : 0) + rr / npairs + (p < rr % npairs ? 1 : 0);
-        mx = std::max(mx, static_cast<double>(W + (p < E ? 1 : 0)) + 1.5 * pieces / P);
+        mx = std::max(mx, static_cast<double>(W + (p < E ? 1 : 0)) + piece_cost * pieces / P);
       }
       const double t = mx + (P - 1) * 6.0 / static_cast<double>(nk);
       if (t < best_t) {
@@ -1202,9 +1204,18 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   return CODA_OK;
 }
 
+// [slot | s-partials | piece partials | piece flags]: launch 3 (the tile-local
+// data gradient) may cut its last tiles into K pieces, like the data gradient.
+size_t swiglu_spart_bytes(int64_t M, int64_t N1) {
+  return align256(static_cast<size_t>(2 * cdiv(N1 / 2, kBN)) * M * 4);
+}
+
 size_t coda_bwd_swiglu_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1, int64_t Dout) {
   if (check_common(M, d, N1) != CODA_OK || Dout <= 0 || M == 0) return 0;
-  return kSlotBytes + align256(static_cast<size_t>(2 * cdiv(N1 / 2, kBN)) * M * 4);
+  const int64_t ps = dgrad_piece_slots(M, d);
+  return kSlotBytes + swiglu_spart_bytes(M, N1) +
+         align256(static_cast<size_t>(ps) * 2 * kSkSlotFloats * 4) +
+         align256(static_cast<size_t>(ps) * 2 * 8);
 }
 
 coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, const coda_bf16* y,
@@ -1274,16 +1285,36 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
     return CODA_ERR_LAUNCH;
   }
   after_launch(1, stream);
-  // 3. RMSNorm-branch data gradient, tile-local with s given
+  // 3. RMSNorm-branch data gradient, tile-local with s given; its last tiles may
+  // be cut into K pieces (any tiles: no row statistic ties them together)
   EpiRmsNormBackwardGivenS::Params p1 = {};
   p1.h = reinterpret_cast<const __nv_bfloat16*>(h);
   p1.gamma = reinterpret_cast<const __nv_bfloat16*>(gamma);
   p1.r = r;
   p1.s = s_out;
   p1.dh_out = reinterpret_cast<__nv_bfloat16*>(dh_out);
-  e = pair ? launch(kPairDgradGivenS, 2 * std::min(max_pairs, mtp * ntd), kThreads,
-                    kPairDgradGivenSSmem, stream, false, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, kNoSplitTail,
-                    kNoColPlan, tmo)
+  SkParams sk3 = kNoSplitTail;
+  if (pair && g_dgrad_pieces.load() != 0) {
+    const int64_t pslots = dgrad_piece_slots(M, d);
+    const PiecePlan pp =
+        plan_dgrad_pieces(mtp * ntd, 1, max_pairs, cdiv(N1, kBK), pslots, 1.0, 0.01);
+    if (pp.pieces > 0) {
+      char* pbase = static_cast<char*>(workspace) + kSlotBytes + swiglu_spart_bytes(M, N1);
+      sk3.dp_tiles = pp.dp_tiles;
+      sk3.part = reinterpret_cast<float*>(pbase);
+      sk3.flags = reinterpret_cast<uint64_t*>(
+          pbase + align256(static_cast<size_t>(pslots) * 2 * kSkSlotFloats * 4));
+      sk3.epoch = static_cast<uint64_t*>(workspace);
+      sk3.slots = static_cast<int>(pslots);
+      sk3.salt = next_salt();
+      sk3.pieces = pp.pieces;
+      sk3.lvl_first = pp.lvl_first;
+      sk3.lvl = pp.lvl;
+    }
+  }
+  const int units3 = sk3.pieces > 0 ? max_pairs : std::min(max_pairs, mtp * ntd);
+  e = pair ? launch(kPairDgradGivenS, 2 * units3, kThreads, kPairDgradGivenSSmem, stream,
+                    sk3.pieces > 0, mA1, mB1, Mi, di, N1i, kPairGroupM, p1, sk3, kNoColPlan, tmo)
            : launch(kDgradGivenS, std::min(sms, mt * ntd), kThreads, kDgradGivenSSmem, stream,
                     false, mA1, mB1, Mi, di, N1i, kGroupM, p1, tmo);
   if (e != cudaSuccess) {

@@ -742,6 +742,9 @@ struct EpiSwiGLUBackward : EpiDefaultCols {
 // ---------------------------------------------------------------------------
 struct EpiRmsNormBackwardGivenS : EpiDefaultCols {
   static constexpr uint32_t kStageBytesPerWarp = Stage64::kBytes;  // h / dh
+  // K-long tiles (K = N1): the last ones are cut into K pieces (PieceWork)
+  // rather than shared out by the split tail, whose slices stream K unaligned.
+  static constexpr bool kSplitTail = false;
 
   struct Params {
     const __nv_bfloat16* h;

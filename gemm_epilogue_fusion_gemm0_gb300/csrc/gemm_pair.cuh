@@ -679,8 +679,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Both CTAs are past their last flag access (cluster barrier above): count
   // this block out of the launch (the last one advances the launch counter).
   if (threadIdx.x == 0) {
-    if (kSplit && sk.epoch != nullptr)
-      launch_exit(sk.epoch, sk.salt);
+    if ((kSplit || pieced) && sk.epoch != nullptr)
+      launch_exit(sk.epoch, sk.salt);  // the data gradient's own counter is this same slot
     else
       Epi::at_exit(ep);
   }

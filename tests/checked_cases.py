@@ -79,6 +79,9 @@ def main():
     for shape, slots in T.PIECE_SHAPES:
         T.test_dgrad_pieces_match_oracle(B, shape, slots)
         clean(f"dgrad in K pieces {shape}")
+    for shape in T.SWIGLU_PIECE_SHAPES:
+        T.test_swiglu_backward_in_pieces_matches_oracle(B, *shape)
+        clean(f"swiglu backward in K pieces {shape}")
     for (M, d, N1) in T.SWEEP_SHAPES[:4]:
         T.test_split_tail_shape_sweep(B, M, d, N1)
         clean(f"split sweep {M}x{d}x{N1}")

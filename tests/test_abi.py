@@ -81,8 +81,10 @@ def test_workspace_sizes(lib):
     assert lib.coda_fwd_workspace_bytes(300, 328, 776) == (  # ragged: rounded up
         256 + 196864 + 4864 + _split_tail_bytes(300, 328, 776))
     assert lib.coda_fwd_workspace_bytes(10, 12, 16) == 0  # d % 8 != 0: unsupported
-    # the slot, then the SwiGLU statistic's partials [2 * ceil(N1/2 / 256), M] fp32
-    assert lib.coda_bwd_swiglu_dgrad_workspace_bytes(300, 256, 1024, 512) == 256 + 4864
+    # the slot, the SwiGLU statistic's partials [2 * ceil(N1/2 / 256), M] fp32, then the piece
+    # slots of its tile-local data gradient as for coda_bwd_dgrad (3 x 2 x 1 tiles = 6)
+    assert lib.coda_bwd_swiglu_dgrad_workspace_bytes(300, 256, 1024, 512) == (
+        256 + 4864 + 6 * 262144 + 256)
     # the slot, then hq [M, d] E4M3 codes and the partial sums
     assert lib.coda_fwd_fp8_workspace_bytes(300, 256, 512) == 256 + 76800 + 2560
     # the full backward: the data gradient's workspace, h2 [M, d] bf16, the dgamma partials

@@ -997,6 +997,69 @@ def test_full_backward_with_pieces_matches_oracle(B):
         B.coda_set_mma_mode(old_mode)
 
 
+# Shapes whose SwiGLU backward cuts the last tiles of its tile-local data gradient
+# into K pieces on 76 CTA pairs (tiles cut, pieces): (8, 4) ragged in every
+# dimension, and (32, 2) where every tile is cut (a single wave of tiles).
+SWIGLU_PIECE_SHAPES = [(2000, 5000, 5072, 1000), (1000, 2048, 8192, 512)]
+
+
+@pytest.mark.parametrize("M,d,N1,Dout", SWIGLU_PIECE_SHAPES)
+def test_swiglu_backward_in_pieces_matches_oracle(B, M, d, N1, Dout):
+    """coda_bwd_swiglu_dgrad with the last tiles of its tile-local data gradient
+    cut into K pieces (the default where the planner finds it pays) and with
+    whole tiles: dy, s and dh against the oracle on every row, both ways."""
+    old_mode, old_pieces = B.coda_get_mma_mode(), B.coda_get_dgrad_pieces()
+    B.coda_set_mma_mode(1)
+    try:
+        for pieces in (1, 0):
+            B.coda_set_dgrad_pieces(pieces)
+            run_swiglu_bwd(B, M, d, N1, Dout, 1e-5, seed=64)
+    finally:
+        B.coda_set_dgrad_pieces(old_pieces)
+        B.coda_set_mma_mode(old_mode)
+
+
+def test_swiglu_backward_in_pieces_replays_from_a_cuda_graph(B):
+    """The SwiGLU backward at a shape whose tile-local data gradient is cut into
+    pieces, captured once and replayed twice: each replay equals the eager call
+    bit for bit (its piece flags take a fresh token at every replay)."""
+    M, d, N1, Dout = SWIGLU_PIECE_SHAPES[0]
+    dev = torch.device("cuda:0")
+    t = synth.make_forward_inputs(M, d, N1, seed=65)
+    g = {k: v.to(dev) for k, v in t.items() if k != "_rng"}
+    old = B.coda_get_mma_mode()
+    B.coda_set_mma_mode(1)
+    try:
+        h, r, _, y = B.coda_fwd_swiglu(g["x"], g["W0"], g["z"], g["gamma"], g["W1"], 1e-5, want_y=True)
+        bw = synth.make_down_proj_backward(t["_rng"], M, N1, Dout)
+        dout, W2 = bw["dout"].to(dev), bw["W2"].to(dev)
+        bf = torch.bfloat16
+        dy = torch.empty((M, N1), dtype=bf, device=dev)
+        s_out = torch.empty((M,), dtype=torch.float32, device=dev)
+        dh = torch.empty((M, d), dtype=bf, device=dev)
+        ws = B.workspace(B.coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout), dev)
+        call = lambda: B.coda_bwd_swiglu_dgrad(dout, W2, y, g["W1"], h, r, g["gamma"], dy=dy, s=s_out,
+                                               dh=dh, ws=ws, stream=torch.cuda.current_stream())
+        call()
+        torch.cuda.synchronize()
+        ref = [x.clone() for x in (dy, s_out, dh)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        for _ in range(2):
+            for x in (dy, dh):
+                x.fill_(float("nan"))
+            s_out.fill_(-1.0)
+            graph.replay()
+            torch.cuda.synchronize()
+            st, detail = B.coda_get_device_status()
+            assert st == B.CODA_OK, (B.status_string(st), hex(detail))
+            for got, want in zip((dy, s_out, dh), ref):
+                assert torch.equal(got, want)
+    finally:
+        B.coda_set_mma_mode(old)
+
+
 def test_dgrad_pieces_replay_from_a_cuda_graph(B):
     """The data gradient at a shape cut into pieces, captured once and replayed
     twice on the same buffers: each replay equals the eager call bit for bit
