@@ -235,7 +235,9 @@ CODA_API coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, 
  *   y      [M, N1]    bf16 in     (pre-activation [g | u] saved by coda_fwd_swiglu)
  *   W1     [d, N1]    bf16 in     h [M, d] bf16, r [M] fp32, gamma [d] bf16 in
  *   dy_out [M, N1]    bf16 out    s_out [M] fp32 out     dh_out [M, d] bf16 out
- *   workspace: at least coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout).
+ *   workspace: at least coda_bwd_swiglu_dgrad_workspace_bytes(M, d, N1, Dout): the
+ *   launch counter's slot, the partial sums of s, and the piece slots of launch 3
+ *   as in coda_bwd_dgrad.
  * N1 must be a multiple of 16 and Dout of 8.  Conventions as coda_bwd_dgrad.
  */
 CODA_API size_t coda_bwd_swiglu_dgrad_workspace_bytes(int64_t M, int64_t d, int64_t N1,
@@ -345,17 +347,21 @@ CODA_API coda_status_t coda_set_col_plan(int enable);
 CODA_API coda_status_t coda_set_serpentine_k(int enable);
 CODA_API int coda_get_serpentine_k(void);
 
-/* 1 (the default): the CTA-pair data gradients (coda_bwd_dgrad and launch 1
- * of coda_bwd) may cut the tiles of their last row blocks into P pieces along
- * K when whole 256 x 256 tiles would leave the last wave of CTA pairs partly
- * idle.  The pieces are dealt so that the pairs keep walking K in step, every
+/* 1 (the default): the CTA-pair data gradients (coda_bwd_dgrad, launch 1 of
+ * coda_bwd and launch 3 of coda_bwd_swiglu_dgrad) may cut the tiles of their
+ * last row blocks (for the tile-local launch 3: any last tiles) into P pieces
+ * along K when whole 256 x 256 tiles would leave the last wave of CTA pairs
+ * partly idle.  The pieces are dealt so that the pairs keep walking K in step, every
  * piece but the last of a tile writes an fp32 partial to the workspace, and
  * the pair holding the last piece adds them before the epilogue.  A host-side
  * model, fitted to GB300 measurements (a piece runs about 1.5 times its share
  * of K), picks the row blocks and P, and keeps whole tiles unless the cut
  * saves at least 3 % (llama1b's data gradient: the last 4 row blocks in 2
- * pieces, 8.9 % faster; llama7b and llama70b keep whole tiles).  Results
- * differ from whole tiles only in fp32 summation order.  0: whole tiles.
+ * pieces, 8.9 % faster; llama7b and llama70b keep whole tiles).  Launch 3 of
+ * coda_bwd_swiglu_dgrad waits on no other tile, so there a piece counts its
+ * share of K and a 1 % saving suffices (llama7b: the last 56 tiles in 4
+ * pieces, 3.5 % faster).  Results differ from whole tiles only in fp32
+ * summation order.  0: whole tiles.
  * Returns CODA_ERR_INVALID_ARG for any other value; coda_get_dgrad_pieces
  * returns the current setting.  Process-wide. */
 CODA_API coda_status_t coda_set_dgrad_pieces(int enable);
