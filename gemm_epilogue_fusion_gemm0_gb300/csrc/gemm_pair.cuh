@@ -232,6 +232,39 @@ __device__ __forceinline__ void sk_add_partial(uint32_t taddr, const float4* slo
   tmem_st_wait();
 }
 
+// The epilogue of a piece (PieceWork) for this thread's row and half: a piece
+// writes its accumulator to its partial slot and publishes the slot's flag; the
+// owner (the tile's last piece) waits for the tile's p1 flags and adds the
+// partials into its accumulator.  Kept out of line so that the policies'
+// epilogues keep their registers.
+__device__ __noinline__ void piece_epilogue(float* part, uint64_t* flags, uint64_t* epoch,
+                                           uint64_t salt, WaitCtl wc, uint32_t taddr, size_t first,
+                                           int p1, int piece, bool is_piece, uint32_t rank, int half,
+                                           int row) {
+  if (is_piece) {
+    const size_t slot = (first + piece) * 2 + rank;
+    sk_write_partial(taddr, reinterpret_cast<float4*>(part + slot * kSkSlotFloats), half, row);
+    __threadfence();
+    named_bar_sync(1, kEpiThreads);
+    if (threadIdx.x == kEpiFirstThread) st_release_gpu_u64(flags + slot, launch_tag(epoch, salt));
+  } else {
+    if (threadIdx.x == kEpiFirstThread) {
+      const uint64_t tag = launch_tag(epoch, salt);
+      for (int q = 0; q < p1; ++q)
+        if (!flag_wait(flags + (first + q) * 2 + rank, tag, wc, kSitePieces)) break;
+      __threadfence();
+    }
+    named_bar_sync(1, kEpiThreads);
+    for (int q = 0; q < p1; ++q)
+      sk_add_partial(taddr,
+                     reinterpret_cast<const float4*>(part + ((first + q) * 2 + rank) * kSkSlotFloats),
+                     half, row);
+    tc_fence_before();
+    named_bar_sync(1, kEpiThreads);
+    tc_fence_after();
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Column plan: tiles narrower than 256 columns, so that a launch's tiles spread
 // evenly over the CTA pairs.  With 256-column tiles a row block of d columns has
@@ -607,31 +640,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                kChkSplitSlot)))
             return false;  // leave the role (every epilogue thread agrees)
         }
-        if (w.kind == kItemTail) {
-          const size_t slot = (first + w.piece) * 2 + rank;
-          sk_write_partial(taddr, reinterpret_cast<float4*>(sk.part + slot * kSkSlotFloats), half,
-                           row);
-          __threadfence();
-          named_bar_sync(1, kEpiThreads);
-          if (threadIdx.x == kEpiFirstThread)
-            st_release_gpu_u64(sk.flags + slot, launch_tag(sk.epoch, sk.salt));
-        } else {
-          if (threadIdx.x == kEpiFirstThread) {
-            const uint64_t tag = launch_tag(sk.epoch, sk.salt);
-            for (int q = 0; q < p1; ++q)
-              if (!flag_wait(sk.flags + (first + q) * 2 + rank, tag, wc, kSitePieces)) break;
-            __threadfence();
-          }
-          named_bar_sync(1, kEpiThreads);
-          for (int q = 0; q < p1; ++q)
-            sk_add_partial(taddr,
-                           reinterpret_cast<const float4*>(sk.part +
-                                                           ((first + q) * 2 + rank) * kSkSlotFloats),
-                           half, row);
-          tc_fence_before();
-          named_bar_sync(1, kEpiThreads);
-          tc_fence_after();
-        }
+        piece_epilogue(sk.part, sk.flags, sk.epoch, sk.salt, wc, taddr, first, p1, w.piece,
+                       w.kind == kItemTail, rank, half, row);
       }
       if (w.kind != kItemTail) {
         TileCtx c;
