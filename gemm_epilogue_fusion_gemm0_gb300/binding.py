@@ -83,6 +83,8 @@ EXPORTS = {
     "coda_get_serpentine_k": (ctypes.c_int, []),
     "coda_set_dgrad_pieces": (_st, [ctypes.c_int]),
     "coda_get_dgrad_pieces": (ctypes.c_int, []),
+    "coda_dgrad_piece_plan": (ctypes.c_int, [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_int32)]),
     "coda_fwd_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "coda_fwd_fp8": (_st, [_vp, _f32, _vp, _f32, _vp, _vp, _vp, _f32, _f32, _f32, _i64, _i64, _i64, _vp,
                            _vp, _vp, _vp, _sz, _vp]),
@@ -396,6 +398,16 @@ def coda_set_dgrad_pieces(enable: int) -> None:
 
 def coda_get_dgrad_pieces() -> int:
     return int(_lib.coda_get_dgrad_pieces())
+
+
+def coda_dgrad_piece_plan(M: int, d: int, N1: int, npairs: int, tile_local: bool = False):
+    """The data gradient's piece plan on `npairs` CTA pairs as (tiles whole, pieces,
+    first levelled pair, levelling pieces per such pair), or None for whole tiles."""
+    out = (ctypes.c_int32 * 4)()
+    rc = int(_lib.coda_dgrad_piece_plan(M, d, N1, int(npairs), int(bool(tile_local)), out))
+    if rc < 0:
+        raise ValueError("coda_dgrad_piece_plan: invalid arguments")
+    return tuple(int(v) for v in out) if rc == 1 else None
 
 
 def coda_get_mma_mode() -> int:

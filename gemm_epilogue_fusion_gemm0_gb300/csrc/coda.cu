@@ -758,12 +758,24 @@ PiecePlan plan_dgrad_pieces(int mt, int nt, int npairs, int64_t nk, int64_t slot
   return best;
 }
 
-// The piece split's parameters for a launch on `npairs` pairs (kNoSplitTail
-// when no plan pays or the switch is off).
-SkParams dgrad_pieces(const DgradWs& dw, int mt, int nt, int npairs, int64_t nk, uint64_t salt) {
+// The piece plan of a CTA-pair data gradient of the given shape on `npairs`
+// pairs: the row-statistic launch cuts whole row blocks (a piece counting 1.5
+// times its share of K, at least 3 % saved); the tile-local launch of the
+// SwiGLU backward cuts any last tiles (a piece counting its share, at least 1 %).
+PiecePlan piece_plan_for(int64_t M, int64_t d, int64_t N1, int npairs, bool tile_local) {
+  const int mt = static_cast<int>(cdiv(M, kPairBM)), nt = static_cast<int>(cdiv(d, kBN));
+  const int64_t nk = cdiv(N1, kBK), slots = dgrad_piece_slots(M, d);
+  return tile_local ? plan_dgrad_pieces(mt * nt, 1, npairs, nk, slots, 1.0, 0.01)
+                    : plan_dgrad_pieces(mt, nt, npairs, nk, slots);
+}
+
+// The piece split's parameters for a row-statistic launch on `npairs` pairs
+// (kNoSplitTail when no plan pays or the switch is off).
+SkParams dgrad_pieces(const DgradWs& dw, int64_t M, int64_t d, int64_t N1, int npairs,
+                      uint64_t salt) {
   SkParams sk = kNoSplitTail;
   if (g_dgrad_pieces.load() == 0) return sk;
-  const PiecePlan pp = plan_dgrad_pieces(mt, nt, npairs, nk, dw.pslots);
+  const PiecePlan pp = piece_plan_for(M, d, N1, npairs, false);
   if (pp.pieces == 0) return sk;
   sk.dp_tiles = pp.dp_tiles;
   sk.part = dw.ppart;
@@ -937,7 +949,7 @@ coda_status_t coda_bwd_dgrad(const coda_bf16* dy, const coda_bf16* W1, const cod
   const uint64_t salt = next_salt();
   // the last row blocks cut into K pieces, when the planner finds it pays (every pair runs)
   const SkParams sk =
-      (pair && cp.nt == 0) ? dgrad_pieces(dw, mt, nt, max_pairs, cdiv(N1, kBK), salt) : kNoSplitTail;
+      (pair && cp.nt == 0) ? dgrad_pieces(dw, M, d, N1, max_pairs, salt) : kNoSplitTail;
   if (sk.pieces > 0) units = max_pairs;
   EpiRmsNormBackward::Params p = {};
   p.h = reinterpret_cast<const __nv_bfloat16*>(h);
@@ -1129,9 +1141,8 @@ coda_status_t coda_bwd(const coda_bf16* dy, const coda_bf16* x, const coda_bf16*
   p.flags = dw.flags;
   p.epoch = dw.epoch;
   p.salt = salt;
-  const SkParams skd = (pair && cp.nt == 0)
-                           ? dgrad_pieces(dw, mt, nt1, max_pairs, cdiv(N1, kBK), salt)
-                           : kNoSplitTail;
+  const SkParams skd =
+      (pair && cp.nt == 0) ? dgrad_pieces(dw, M, d, N1, max_pairs, salt) : kNoSplitTail;
   if (skd.pieces > 0) units = max_pairs;
   p.dh_res = reinterpret_cast<const __nv_bfloat16*>(dh_res);
   p.h2_out = h2;
@@ -1296,8 +1307,7 @@ coda_status_t coda_bwd_swiglu_dgrad(const coda_bf16* dout, const coda_bf16* W2, 
   SkParams sk3 = kNoSplitTail;
   if (pair && g_dgrad_pieces.load() != 0) {
     const int64_t pslots = dgrad_piece_slots(M, d);
-    const PiecePlan pp =
-        plan_dgrad_pieces(mtp * ntd, 1, max_pairs, cdiv(N1, kBK), pslots, 1.0, 0.01);
+    const PiecePlan pp = piece_plan_for(M, d, N1, max_pairs, true);
     if (pp.pieces > 0) {
       char* pbase = static_cast<char*>(workspace) + kSlotBytes + swiglu_spart_bytes(M, N1);
       sk3.dp_tiles = pp.dp_tiles;
@@ -1393,6 +1403,17 @@ coda_status_t coda_set_dgrad_pieces(int enable) {
 }
 
 int coda_get_dgrad_pieces(void) { return g_dgrad_pieces.load(); }
+
+int coda_dgrad_piece_plan(int64_t M, int64_t d, int64_t N1, int npairs, int tile_local,
+                          int32_t* plan) {
+  if (plan == nullptr || npairs < 1 || check_common(M, d, N1) != CODA_OK || M == 0) return -1;
+  const PiecePlan pp = piece_plan_for(M, d, N1, npairs, tile_local != 0);
+  plan[0] = pp.dp_tiles;
+  plan[1] = pp.pieces;
+  plan[2] = pp.lvl_first;
+  plan[3] = pp.lvl;
+  return pp.pieces > 0 ? 1 : 0;
+}
 
 coda_status_t coda_set_fold_rowreduce(int enable) {
   if (enable != 0 && enable != 1) return CODA_ERR_INVALID_ARG;

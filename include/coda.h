@@ -367,6 +367,18 @@ CODA_API int coda_get_serpentine_k(void);
 CODA_API coda_status_t coda_set_dgrad_pieces(int enable);
 CODA_API int coda_get_dgrad_pieces(void);
 
+/* The piece plan the CTA-pair data gradient would use for the shape on `npairs`
+ * CTA pairs (the device has SMs / 2 of them), whatever coda_set_dgrad_pieces
+ * says; host-only, no device needed.  tile_local = 0: the row-statistic launch
+ * (coda_bwd_dgrad, launch 1 of coda_bwd); 1: launch 3 of coda_bwd_swiglu_dgrad.
+ * Writes plan[4] = {tiles handed out whole (the cut tiles follow them in the
+ * launch's tile order), pieces per cut tile, first of the pairs that hold one
+ * whole tile fewer and take levelling pieces, levelling pieces per such pair}.
+ * Returns 1 when a plan is taken, 0 when the launch keeps whole tiles (plan
+ * zeroed) and -1 for invalid arguments. */
+CODA_API int coda_dgrad_piece_plan(int64_t M, int64_t d, int64_t N1, int npairs, int tile_local,
+                                   int32_t* plan);
+
 /* Upper bound, in nanoseconds, of every device-side wait launched after this
  * call (default 1e9 = 1 s).  A wait that runs out records
  * CODA_ERR_DEVICE_TIMEOUT and lets its kernel finish without hanging. */
